@@ -1,0 +1,286 @@
+/*
+ * pagedkv_oracle.c -- plain, slow, obviously correct CPU oracle for the paged
+ * KV cache hot path: slot-mapped append, block copy, and PagedAttention decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; it is written from the definitions on the source pages:
+ *
+ *  [CS349D-L3]  "Lecture 3: memory and prefix reuse in serving engines --
+ *               vLLM PagedAttention and SGLang RadixAttention"
+ *               (semidirectx.com, Stanford CS349D lecture 3 notes)
+ *  [11868-L24]  "Lecture 24: PagedAttention and vLLM"
+ *               (semidirectx.com, CMU 11-868 lecture 24 notes)
+ *  [RL-Part3]   "Part 3: single node -- engines that optimise memory"
+ *               (random-liu.github.io, LLM inference from principle to production)
+ *  [S06]        "S06 memory and KV cache: PagedAttention"
+ *               (llminference.xinbetween.com)
+ *
+ * Arithmetic: every floating-point step is done in fp64 with libm's exp.
+ * No blocking, no split, no online softmax: the attention is the textbook
+ * softmax(q K^T * scale) V over the gathered context.
+ *
+ * Layout (the pool layout [S06] "Implementation" gives for k_cache):
+ *   pool  [num_blocks, block_size, num_kv_heads, head_dim]   (K and V separate)
+ *   q/out [batch, num_q_heads, head_dim]
+ *   block_tables int32 [batch, max_blocks_per_seq], seq_lens int32 [batch]
+ *   slot_mapping int64 [num_tokens]
+ *   pairs int32 [num_pairs, 2] = (src, dst)
+ *
+ * Element types: 0 = IEEE binary32, 1 = IEEE binary16, 2 = bfloat16 (the top
+ * 16 bits of a binary32).  Decoding is written from the formats' definitions.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+
+static size_t elem_size(int dtype) { return dtype == OR_F32 ? 4u : 2u; }
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double decode_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);              /* subnormal: f * 2^-14 / 1024 */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the 16 high-order bits of a binary32. */
+static double decode_bf16(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return (double)x;
+}
+
+static double load_elem(const void* base, size_t idx, int dtype) {
+    if (dtype == OR_F32) {
+        float x;
+        memcpy(&x, (const char*)base + 4 * idx, 4);
+        return (double)x;
+    }
+    uint16_t h;
+    memcpy(&h, (const char*)base + 2 * idx, 2);
+    return dtype == OR_F16 ? decode_f16(h) : decode_bf16(h);
+}
+
+/* Exposed so the tests can pin the element decoders against library ones. */
+double oracle_decode_elem(const void* base, size_t idx, int dtype) {
+    return load_elem(base, idx, dtype);
+}
+
+/*
+ * Slot-mapped append ([RL-Part3] ch. 13 sec. 1, "slot_mapping": the GPU does
+ * kv_cache[slot_mapping[i]] = new_kv; [CS349D-L3] sec. 3.1 slot arithmetic).
+ * A slot addresses one token row of the pool: block slot / bs, row slot % bs,
+ * which in the [num_blocks, bs, Hkv, D] layout is row `slot` of the pool viewed
+ * as [num_blocks * bs, Hkv * D].  Each row is copied byte for byte.
+ * Negative slots are padding and are skipped; slots >= num_blocks * bs are
+ * skipped and counted.  Returns the number of out-of-range slots.
+ */
+long oracle_append(void* k_pool, void* v_pool, long num_blocks, long block_size,
+                   long num_kv_heads, long head_dim, int dtype,
+                   const void* k_new, const void* v_new,
+                   const int64_t* slot_mapping, long num_tokens) {
+    size_t row = (size_t)num_kv_heads * head_dim * elem_size(dtype);
+    long nrows = num_blocks * block_size;
+    long bad = 0;
+    for (long i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= nrows) { ++bad; continue; }
+        long blk = (long)(slot / block_size), off = (long)(slot % block_size);
+        size_t dst = ((size_t)blk * block_size + off) * row;
+        memcpy((char*)k_pool + dst, (const char*)k_new + (size_t)i * row, row);
+        memcpy((char*)v_pool + dst, (const char*)v_new + (size_t)i * row, row);
+    }
+    return bad;
+}
+
+/*
+ * Copy-on-write block copy ([CS349D-L3] sec. 4.1: allocate, copy the content,
+ * remap, then write; sec. 3.2: the many small copies go in one launch).
+ * For each pair in order: K[dst] <- K[src], V[dst] <- V[src], whole blocks.
+ * Pairs with an id outside [0, num_blocks) are skipped and counted.
+ */
+long oracle_copy_blocks(void* k_pool, void* v_pool, long num_blocks,
+                        long block_size, long num_kv_heads, long head_dim,
+                        int dtype, const int32_t* pairs, long num_pairs) {
+    size_t blk = (size_t)block_size * num_kv_heads * head_dim * elem_size(dtype);
+    long bad = 0;
+    for (long p = 0; p < num_pairs; ++p) {
+        long src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        memmove((char*)k_pool + dst * blk, (const char*)k_pool + src * blk, blk);
+        memmove((char*)v_pool + dst * blk, (const char*)v_pool + src * blk, blk);
+    }
+    return bad;
+}
+
+typedef struct {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    int dtype;
+    long num_blocks, block_size, num_kv_heads, head_dim;
+    const int32_t* block_tables;
+    long max_blocks_per_seq;
+    const int32_t* seq_lens;
+    long batch, num_q_heads;
+    double scale;
+    double* out;        /* [batch, num_q_heads, head_dim], fp64 */
+    long b_begin, b_end;
+    long bad;           /* out-of-range block ids met */
+} decode_job;
+
+/*
+ * Attention for one sequence ([S06] "Implementation": walk the block table,
+ * take the first n rows of each physical block, score q . k / sqrt(d), one
+ * softmax over every position of every block, weighted sum of V;
+ * [CS349D-L3] sec. 3.2: the softmax denominator sums over all positions of all
+ * blocks, and only the written rows of the last block take part;
+ * [RL-Part3] ch. 9 sec. 1: query heads are grouped, each group shares one KV
+ * head, here in contiguous groups: kv head g = h / (Hq / Hkv)).
+ *
+ * Steps, all in fp64:
+ *   1. gather K and V of kv head g for positions 0..L-1 through the table
+ *      into contiguous arrays (the "gather" the pages describe);
+ *   2. s_t = scale * sum_d q[d] k_t[d];
+ *   3. w = softmax(s) with the maximum subtracted;
+ *   4. out = sum_t w_t v_t.
+ * L = 0 gives zeros.
+ */
+static void decode_one_seq(decode_job* J, long b, double* kbuf, double* vbuf,
+                           double* s, double* qbuf) {
+    long bs = J->block_size, Hkv = J->num_kv_heads, D = J->head_dim;
+    long Hq = J->num_q_heads, group = Hq / Hkv;
+    long L = J->seq_lens[b];
+    if (L > J->max_blocks_per_seq * bs) {  /* table too short: use what exists */
+        J->bad++;
+        L = J->max_blocks_per_seq * bs;
+    }
+    const int32_t* table = J->block_tables + b * J->max_blocks_per_seq;
+    for (long h = 0; h < Hq; ++h) {
+        double* o = J->out + ((size_t)b * Hq + h) * D;
+        for (long d = 0; d < D; ++d) o[d] = 0.0;
+        if (L <= 0) continue;
+        long g = h / group;
+        /* 1. gather */
+        long n = 0;
+        for (long t = 0; t < L; ++t) {
+            long phys = table[t / bs];
+            if (phys < 0 || phys >= J->num_blocks) {  /* invalid entry: skip */
+                J->bad++;
+                continue;
+            }
+            size_t row = (((size_t)phys * bs + t % bs) * Hkv + g) * D;
+            for (long d = 0; d < D; ++d) {
+                kbuf[n * D + d] = load_elem(J->k_pool, row + d, J->dtype);
+                vbuf[n * D + d] = load_elem(J->v_pool, row + d, J->dtype);
+            }
+            ++n;
+        }
+        if (n == 0) continue;
+        /* 2. scores */
+        size_t qoff = ((size_t)b * Hq + h) * D;
+        for (long d = 0; d < D; ++d) qbuf[d] = load_elem(J->q, qoff + d, J->dtype);
+        for (long t = 0; t < n; ++t) {
+            double acc = 0.0;
+            for (long d = 0; d < D; ++d) acc += qbuf[d] * kbuf[t * D + d];
+            s[t] = J->scale * acc;
+        }
+        /* 3. softmax with max subtraction */
+        double m = -INFINITY;
+        for (long t = 0; t < n; ++t) if (s[t] > m) m = s[t];
+        double denom = 0.0;
+        for (long t = 0; t < n; ++t) { s[t] = exp(s[t] - m); denom += s[t]; }
+        /* 4. weighted sum of V */
+        for (long t = 0; t < n; ++t) {
+            double w = s[t] / denom;
+            for (long d = 0; d < D; ++d) o[d] += w * vbuf[t * D + d];
+        }
+    }
+}
+
+static void* decode_worker(void* arg) {
+    decode_job* J = (decode_job*)arg;
+    long maxL = J->max_blocks_per_seq * J->block_size;
+    double* kbuf = (double*)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1) * J->head_dim);
+    double* vbuf = (double*)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1) * J->head_dim);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
+    double* qbuf = (double*)malloc(sizeof(double) * (size_t)J->head_dim);
+    if (!kbuf || !vbuf || !s || !qbuf) {
+        J->bad = -1;
+    } else {
+        for (long b = J->b_begin; b < J->b_end; ++b) decode_one_seq(J, b, kbuf, vbuf, s, qbuf);
+    }
+    free(kbuf);
+    free(vbuf);
+    free(s);
+    free(qbuf);
+    return NULL;
+}
+
+/*
+ * PagedAttention decode for a batch.  Sequences are independent; with
+ * num_threads > 1 contiguous ranges of sequences go to separate threads (the
+ * arithmetic of each sequence is unchanged).  Returns 0 when every table entry
+ * that was read is a valid block id and every seq_len fits its table, a
+ * positive count of such problems otherwise (the offending positions are
+ * skipped), or -1 on bad arguments / no memory.
+ */
+long oracle_decode(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                   long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                   const int32_t* block_tables, long max_blocks_per_seq,
+                   const int32_t* seq_lens, long batch, long num_q_heads,
+                   double scale, double* out, int num_threads) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 ||
+        head_dim <= 0 || batch < 0)
+        return -1;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > batch) num_threads = batch > 0 ? (int)batch : 1;
+    decode_job* jobs = (decode_job*)calloc((size_t)num_threads, sizeof(decode_job));
+    pthread_t* tids = (pthread_t*)calloc((size_t)num_threads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return -1; }
+    for (int i = 0; i < num_threads; ++i) {
+        decode_job* J = &jobs[i];
+        J->q = q; J->k_pool = k_pool; J->v_pool = v_pool; J->dtype = dtype;
+        J->num_blocks = num_blocks; J->block_size = block_size;
+        J->num_kv_heads = num_kv_heads; J->head_dim = head_dim;
+        J->block_tables = block_tables; J->max_blocks_per_seq = max_blocks_per_seq;
+        J->seq_lens = seq_lens; J->batch = batch; J->num_q_heads = num_q_heads;
+        J->scale = scale; J->out = out;
+        J->b_begin = batch * i / num_threads;
+        J->b_end = batch * (i + 1) / num_threads;
+    }
+    long bad = 0;
+    if (num_threads == 1) {
+        decode_worker(&jobs[0]);
+    } else {
+        for (int i = 0; i < num_threads; ++i)
+            pthread_create(&tids[i], NULL, decode_worker, &jobs[i]);
+        for (int i = 0; i < num_threads; ++i) pthread_join(tids[i], NULL);
+    }
+    for (int i = 0; i < num_threads; ++i) {
+        if (jobs[i].bad < 0) { bad = -1; break; }
+        bad += jobs[i].bad;
+    }
+    free(jobs);
+    free(tids);
+    return bad;
+}
