@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Decode-step benchmark for the paged KV cache library on GB300.
+
+A step is the whole hot path over one batch: copy_blocks (this step's
+copy-on-write pairs) -> kv_append (one new K/V row per sequence) ->
+paged_attention_decode (split + log-sum-exp combine).  Default workload: the
+Llama-3-8B-shaped GQA step (32 query / 8 KV heads, head_dim 128, bf16, block
+size 16, batch 256, lognormal context lengths with median 1024 clipped to
+[16, 8192], blocks scattered over a pool 1.5x the need), inputs resident in
+HBM.  The L2 is flushed (512 MB write) between timed steps, outside the timed
+events.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+this machine's host cores instead (the reference arm).  Under torchrun every
+rank runs an independent replica of the workload (weak scaling, no collective
+on the data path); the timed region is bracketed by barriers and the slowest
+rank's time is reported.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), seq-steps/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_decode_split_llama3_8b_gqa.md")
+DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "decode_kernel.cuh")
+
+WORKLOAD_TEXT = {
+    "llama3_8b_gqa": "Llama-3-8B-shaped GQA decode step: 32 query / 8 KV heads, head_dim 128, bf16, "
+                     "block_size 16, batch 256, context ~ clip(round(lognormal(ln 1024, 1.0)), 16, 8192), "
+                     "blocks scattered in a pool 1.5x the need, 1 layer, append + attention",
+    "opt13b_mha": "OPT-13B-shaped MHA decode step: 40 = 40 heads, head_dim 128, fp16, block_size 16, "
+                  "batch 64, context ~ U[128, 2048], pool 1.5x, 1 layer, append + attention",
+    "shared_prefix": "shared-prefix parallel sampling: Llama-3-8B GQA shape, bf16, bs 16, 32 prompts x "
+                     "2000 tokens, n = 4 samples, 0-256 divergent tokens, CoW copies + append + attention",
+    "long_context": "long-context split-KV decode: 32/8 heads, head_dim 128, bf16, batch 8, "
+                    "context ~ U[32768, 131072], block_size 16",
+}
+
+
+# ------------------------------------------------------------------ helpers --
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="llama3_8b_gqa")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--placement", choices=["random", "identity"], default="random")
+    return ap.parse_args(argv)
+
+
+def make_workload(name: str, seed: int, device, placement: str = "random"):
+    from paged_kv_cache_68_gb300 import workloads as wl
+    if name == "llama3_8b_gqa":
+        return wl.llama3_8b_gqa(seed, device=device, placement=placement)
+    if name == "opt13b_mha":
+        return wl.opt13b_mha(seed, device=device)
+    if name == "shared_prefix":
+        return wl.shared_prefix(seed, device=device)
+    if name == "long_context":
+        return wl.long_context(seed, device=device)
+    raise ValueError(name)
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        sha = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return int(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip() for l in self.file.read().splitlines() if l.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(dev) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def reduce_max_sum(local_ms: float, local_units: float):
+    """(max over ranks of local_ms, sum over ranks of local_units)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return local_ms, local_units
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ----------------------------------------------------------- CPU baseline --
+
+def oracle_sample_step(host_w, seqs, threads):
+    """One oracle step (copy, append, attention) restricted to `seqs`;
+    returns (seconds, algorithmic bytes of that sample)."""
+    import numpy as np
+    from oracle import c_oracle
+    k, v = host_w.k_pool, host_w.v_pool          # state: appends are idempotent
+    t0 = time.perf_counter()
+    c_oracle.copy_blocks(k, v, host_w.pairs, host_w.dtype)
+    c_oracle.append(k, v, host_w.k_new[seqs], host_w.v_new[seqs], host_w.slot_mapping[seqs],
+                    host_w.dtype)
+    c_oracle.decode(np.ascontiguousarray(host_w.q[seqs]), k, v, host_w.dtype,
+                    np.ascontiguousarray(host_w.block_tables[seqs]),
+                    np.ascontiguousarray(host_w.seq_lens[seqs]), host_w.scale,
+                    host_w.num_kv_heads, num_threads=threads)
+    dt = time.perf_counter() - t0
+    L = host_w.seq_lens[seqs].astype(np.int64)
+    row = host_w.num_kv_heads * host_w.head_dim * host_w.elem_bytes
+    nbytes = int(L.sum()) * row * 2 + len(seqs) * row * 4 + host_w.copy_bytes()
+    return dt, nbytes
+
+
+def pick_sample(host_w, budget_s, threads):
+    """Sequences (a prefix of a fixed shuffle) whose oracle step takes about budget_s."""
+    import numpy as np
+    order = np.random.default_rng(1234).permutation(host_w.batch)
+    n = min(host_w.batch, max(1, threads))
+    dt, _ = oracle_sample_step(host_w, order[:n], threads)
+    if dt < budget_s and n < host_w.batch:
+        n = int(min(host_w.batch, max(n, n * budget_s / max(dt, 1e-3))))
+    return np.sort(order[:n])
+
+
+# --------------------------------------------------------------- our arm --
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_68_gb300 import pagedkv
+    from paged_kv_cache_68_gb300 import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pagedkv.load()
+    w = make_workload(args.workload, args.seed, dev, args.placement)
+    tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
+    k_pool, v_pool = w.k_pool, w.v_pool
+    q, k_new, v_new = tv(w.q), tv(w.k_new), tv(w.v_new)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    tables = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev)
+    lens = torch.from_numpy(w.seq_lens).to(dev)
+    pairs = torch.from_numpy(np.ascontiguousarray(w.pairs, dtype=np.int32)).to(dev)
+    pool = pagedkv.KVPool(k_pool, v_pool)
+    out = torch.empty_like(q)
+    ws = pool.workspace(w.batch, w.num_q_heads)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    n_pairs = int(w.pairs.shape[0])
+    launches_per_step = (1 if n_pairs else 0) + 1 + 2
+
+    def step():
+        pool.copy_blocks(pairs)
+        pool.append(k_new, v_new, slots)
+        pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert pool.get_error() == 0, "device error word set during warm-up"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid(dev))
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()                                   # L2 flush, outside the events
+        e = ev[i]
+        e[0].record()
+        pool.copy_blocks(pairs)
+        pool.append(k_new, v_new, slots)
+        e[1].record()
+        pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
+        e[2].record()
+        e[3].record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    step_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / K
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    assert pool.get_error() == 0, "device error word set during the timed steps"
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    host = {n: t.cpu().pin_memory() for n, t in
+            (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots),
+             ("tables", tables), ("lens", lens), ("pairs", pairs))}
+    dst = {"q": q, "k_new": k_new, "v_new": v_new, "slots": slots, "tables": tables,
+           "lens": lens, "pairs": pairs}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    KE = max(1, min(args.e2e_steps, K))
+    eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(KE):
+        flush.zero_()
+        eve[i][0].record()
+        for n, t in host.items():
+            dst[n].copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        eve[i][1].record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eve) / KE
+
+    step_bytes = w.step_bytes()
+    att_bytes = w.attention_bytes()
+    max_step_ms, total_bytes = reduce_max_sum(step_ms, step_bytes)
+    max_e2e_ms, _ = reduce_max_sum(e2e_ms, step_bytes)
+    max_dec_ms, _ = reduce_max_sum(dec_ms, att_bytes)
+    total_seqs = w.batch * world
+    value = total_bytes / (max_step_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    achieved = att_bytes / (dec_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_w = wl.on_host(w)
+        threads = os.cpu_count() or 1
+        seqs = pick_sample(host_w, 10.0, threads)
+        dt, nb = oracle_sample_step(host_w, seqs, threads)
+        cpu = {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(seqs)} of {w.batch} sequences of the same step (copy + append + "
+                         f"attention, fp64 C oracle), one pass, {dt:.1f} s"}
+
+    pool.close()
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(max_step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
+                   "placement": args.placement, "global_batch": w.batch * world,
+                   "tokens_per_replica": int(w.seq_lens.sum()),
+                   "kv_bytes_per_replica": w.kv_bytes(), "step_bytes_per_replica": step_bytes,
+                   "l2": "flushed (512 MB write) between timed steps; KV 1.7 GB > 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "seq_steps_per_s": round(total_seqs / (max_step_ms * 1e-3), 1),
+        "attention_gbs": round(att_bytes * world / (max_dec_ms * 1e-3) / 1e9, 2),
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (split + combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
+                     "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
+                     "traffic": profiled_traffic(), "algorithmic_bytes": att_bytes},
+        "e2e": {"value": round(total_bytes / (max_e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(max_e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * K,
+        "cpu_baseline": cpu,
+    }
+
+
+# -------------------------------------------------------- reference arm --
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import torch
+
+    from oracle import c_oracle
+    from paged_kv_cache_68_gb300 import workloads as wl
+    c_oracle.build()
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    w = wl.on_host(make_workload(args.workload, args.seed, dev, args.placement))
+    threads = os.cpu_count() or 1
+    per_step = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    seqs = pick_sample(w, per_step, threads)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, seqs, threads)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample_step(w, seqs, threads)
+        tot_t += dt
+        tot_b += nb
+    value = tot_b / tot_t / 1e9
+    ms = tot_t / args.steps * 1e3
+    sample = (f"{len(seqs)} of {w.batch} sequences per step (copy + append + attention, "
+              f"fp64 C oracle), {args.steps} steps")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
+                   "placement": args.placement},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV cache hot path for NVIDIA GB300 (sm_103a).
+ *
+ * Three operations on a pool of fixed-size KV blocks:
+ *
+ *   copy_blocks             batched copy-on-write block copies (src -> dst);
+ *   kv_append               slot-mapped write of each new token's K and V row
+ *                           (the pages' reshape-and-cache step);
+ *   paged_attention_decode  single-query attention per sequence, reading K and
+ *                           V through the sequence's block table inside the
+ *                           kernel (split over the GPU, merged by log-sum-exp).
+ *
+ * Sources, by page title and section:
+ *   "Lecture 3: memory and prefix reuse in serving engines -- vLLM
+ *   PagedAttention and SGLang RadixAttention" (semidirectx.com, CS349D notes),
+ *   sec. 3.1 (blocks, block tables), sec. 3.2 (attention over scattered blocks;
+ *   fused write-by-block-table kernel; copy-on-write copies batched into one
+ *   launch), sec. 4.1 (copy-on-write);
+ *   "Lecture 24: PagedAttention and vLLM" (semidirectx.com, CMU 11-868
+ *   notes), sec. 3.2 (block-wise scores merged with an online softmax, the
+ *   Flash-Decoding trick);
+ *   "Part 3: single node" (random-liu.github.io), ch. 9 sec. 1 (grouped-query
+ *   heads), ch. 11 sec. 3 (block table [max_num_reqs, max_num_blocks_per_req]),
+ *   ch. 13 sec. 1 (slot_mapping: kv_cache[slot_mapping[i]] = new_kv);
+ *   "S06 memory and KV cache: PagedAttention" (llminference.xinbetween.com),
+ *   "Implementation" (pool layout [num_blocks, block_size, n_kv_heads,
+ *   head_dim]; the block-table indirection happens inside the kernel).
+ *
+ * Conventions shared by every call
+ *   - Memory: every device pointer is owned by the caller and must stay valid
+ *     until the work queued on the stream has finished.  Pointers to element
+ *     data and to the workspace must be 16-byte aligned; tensors are dense,
+ *     row-major, with the layouts stated below.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Calls only enqueue work; none synchronises the host,
+ *     except kv_pool_get_error.
+ *   - Errors: argument checks run on the host before anything is enqueued and
+ *     return a kv_status; nothing is enqueued on failure.  Data-dependent
+ *     faults (an out-of-range slot, block id or copy pair; a too-short block
+ *     table) are found by the kernels: the offending item is skipped, a bit is
+ *     set in the pool's device error word, and kv_pool_get_error reports it.
+ *   - Element types: q, out, new K/V rows and the pools all use the pool's
+ *     kv_dtype.  Arithmetic in attention is fp32; one rounding to the output
+ *     type at the end (round to nearest even).
+ *   - Devices: a pool belongs to the device that was current when it was
+ *     created; every call on it must be made with that device current.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KV_OK = 0,
+    KV_EINVAL = 1,        /* a null pointer, bad size, misalignment, mismatch   */
+    KV_EUNSUPPORTED = 2,  /* valid but not built: head_dim, group size, dtype  */
+    KV_ECUDA = 3,         /* a CUDA runtime or driver call failed              */
+    KV_ERANGE = 4,        /* kv_pool_get_error: the device error word is set   */
+    KV_ENOWORKSPACE = 5   /* workspace too small (see the size query)          */
+} kv_status;
+
+typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype;
+
+/* Bits of the device error word (kv_pool_get_error). */
+#define KV_DEVERR_SLOT_RANGE   0x1  /* kv_append: slot >= num_blocks*block_size     */
+#define KV_DEVERR_BLOCK_RANGE  0x2  /* decode: table entry outside [0, num_blocks)  */
+#define KV_DEVERR_PAIR_RANGE   0x4  /* copy_blocks: src or dst outside the pool     */
+#define KV_DEVERR_SEQ_RANGE    0x8  /* decode: seq_len > max_blocks_per_seq*bs      */
+#define KV_DEVERR_TIMEOUT      0x10 /* a pipeline wait gave up (work was skipped)    */
+
+typedef struct kv_pool* kv_pool_t;
+
+/*
+ * kv_pool_create -- describe a KV block pool held in caller memory.
+ *
+ * k_pool, v_pool: device pointers, each [num_blocks, block_size, num_kv_heads,
+ *   head_dim] of `dtype` (the layout of the S06 page's k_cache), 16-byte aligned.
+ * Limits: 1 <= block_size <= 256; head_dim in {64, 128}; num_kv_heads >= 1;
+ *   num_blocks >= 1 and num_blocks * block_size < 2^31.
+ * On success *out receives a handle.  The handle owns no pool memory: it holds
+ *   the geometry, two TMA descriptors built from k_pool / v_pool, and a 4-byte
+ *   device error word that this call allocates (freed by kv_pool_destroy).
+ * Errors: KV_EINVAL (null or misaligned pointer, size out of range),
+ *   KV_EUNSUPPORTED (head_dim, dtype), KV_ECUDA.
+ */
+kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         kv_dtype dtype, void* k_pool, void* v_pool, kv_pool_t* out);
+
+/* kv_pool_destroy -- free the handle and its error word (not the pools).
+ * Work already queued with the handle must have finished.  NULL is a no-op. */
+kv_status kv_pool_destroy(kv_pool_t pool);
+
+/*
+ * kv_append -- write each new token's K and V row into its slot
+ * ("Part 3: single node", ch. 13 sec. 1: kv_cache[slot_mapping[i]] = new_kv).
+ *
+ * k_new, v_new: device [num_tokens, num_kv_heads, head_dim] of the pool dtype.
+ * slot_mapping: device int64 [num_tokens]; slot = block * block_size + offset.
+ *   A negative slot is padding and is skipped.  A slot >= num_blocks *
+ *   block_size is skipped and sets KV_DEVERR_SLOT_RANGE.
+ * Two tokens with the same slot: one of the rows wins (unspecified which).
+ * num_tokens = 0 enqueues nothing.
+ */
+kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
+                    const int64_t* slot_mapping, int num_tokens, void* stream);
+
+/*
+ * copy_blocks -- copy-on-write block copies in one launch ("Lecture 3", sec. 3.2
+ * and sec. 4.1): for every pair, K[dst] <- K[src] and V[dst] <- V[src], whole
+ * blocks (block_size * num_kv_heads * head_dim elements each).
+ *
+ * pairs: device int32 [num_pairs, 2] holding (src, dst).  Precondition: the dst
+ *   ids are distinct and no dst is also a src in the same call (the copies run
+ *   concurrently).  A pair with an id outside [0, num_blocks) is skipped and
+ *   sets KV_DEVERR_PAIR_RANGE.  num_pairs = 0 enqueues nothing.
+ */
+kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void* stream);
+
+/*
+ * paged_attention_workspace_size -- bytes of device workspace that
+ * paged_attention_decode needs for this pool, batch and head count on the
+ * current device.  The value depends only on these arguments and the device.
+ */
+kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_heads,
+                                         size_t* bytes);
+
+/*
+ * paged_attention_decode -- one query token per sequence attends over its
+ * whole cached context ("Lecture 3", sec. 3.2; S06 "Implementation").
+ *
+ * For sequence b and query head h, with g = h / (num_q_heads / num_kv_heads)
+ * (consecutive query heads share a KV head, "Part 3", ch. 9 sec. 1) and
+ * L = seq_lens[b]:
+ *     s_t = scale * dot(q[b,h,:], K[block_tables[b, t / bs], t % bs, g, :])
+ *     out[b,h,:] = sum_t softmax(s)_t * V[block_tables[b, t / bs], t % bs, g, :]
+ * over t = 0 .. L-1.  L = 0 gives zeros.  Only table entries
+ * 0 .. ceil(L / bs) - 1 and only the first L rows are read.
+ *
+ * q, out: device [batch, num_q_heads, head_dim] of the pool dtype.
+ * block_tables: device int32 [batch, max_blocks_per_seq] (row-major).
+ * seq_lens: device int32 [batch], the context length including the token the
+ *   step appended.  L > max_blocks_per_seq * bs is clamped to the table and
+ *   sets KV_DEVERR_SEQ_RANGE; an entry outside [0, num_blocks) is skipped
+ *   (its tokens do not take part) and sets KV_DEVERR_BLOCK_RANGE.
+ * num_kv_heads must equal the pool's; num_q_heads / num_kv_heads in {1,2,4,8};
+ *   1 <= batch <= 4096.
+ * workspace: device scratch of at least paged_attention_workspace_size bytes,
+ *   16-byte aligned, owned by the caller; it holds no state between calls.
+ *   Calls that use the same workspace must not overlap in time.
+ * Errors: KV_EINVAL, KV_EUNSUPPORTED, KV_ENOWORKSPACE, KV_ECUDA.
+ */
+kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int num_q_heads,
+                                 float scale, int num_kv_heads, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * kv_pool_get_error -- read the pool's device error word (KV_DEVERR_* bits,
+ * OR-ed over every call since the last clear).  Synchronises the device.
+ * Returns KV_ERANGE when any bit is set, KV_OK when none is.
+ */
+kv_status kv_pool_get_error(kv_pool_t pool, int* device_error_bits);
+
+/* kv_pool_clear_error -- zero the device error word (synchronous). */
+kv_status kv_pool_clear_error(kv_pool_t pool);
+
+/* kv_strerror -- static text for a status code. */
+const char* kv_strerror(kv_status status);
+
+/* kv_last_cuda_error -- the text of the last CUDA error this library met on
+ * the calling thread ("" if none). */
+const char* kv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,269 @@
+// C-ABI front end: argument checks, pool descriptors (TMA tensor maps), launch
+// planning and dispatch.  Every entry point validates on the host, enqueues on
+// the caller's stream and returns; see pagedkv.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "decode_kernel.cuh"
+#include "pagedkv_internal.cuh"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+kv_status cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where,
+                  cudaGetErrorString(e));
+    return KV_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(kv_dtype d) { return d == KV_F32 ? 4 : 2; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// The pool viewed as [N*bs rows][Hkv][D]; one box = the bs rows of one block
+// for one KV head: {D, 1, bs}.
+bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t elt = (cuuint64_t)p.elem_bytes;
+    cuuint64_t dims[3] = {(cuuint64_t)p.head_dim, (cuuint64_t)p.num_kv_heads,
+                          (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_size};
+    cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * elt,
+                             (cuuint64_t)p.num_kv_heads * p.head_dim * elt};
+    cuuint32_t box[3] = {(cuuint32_t)p.head_dim, 1u, (cuuint32_t)p.block_size};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapDataType dt =
+        p.elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    return enc(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr size_t kRingBytes = 64 * 1024;   // shared-memory ring per CTA (target)
+constexpr size_t kMaxSmem = 227 * 1024;
+
+}  // namespace
+
+namespace pagedkv {
+
+cudaError_t plan_decode(const kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan) {
+    const int G = num_q_heads / pool.num_kv_heads;
+    const int D = pool.head_dim, bs = pool.block_size, elt = pool.elem_bytes;
+    const size_t stage = 2ull * bs * D * elt;
+    int S = (int)(kRingBytes / stage);
+    S = S < 2 ? 2 : (S > 32 ? 32 : S);
+    size_t smem = 0;
+    for (;; --S) {
+        smem = dec::Layout(S, batch, bs, G, D, elt).total + 1024;
+        if (smem <= kMaxSmem || S == 2) break;
+    }
+    if (smem > kMaxSmem) return cudaErrorNotSupported;
+    int occ = 0;
+    cudaError_t e = cudaErrorNotSupported;
+    if (pool.dtype == KV_F32) e = decode_attrs_f32(D, G, smem, &occ);
+    if (pool.dtype == KV_F16) e = decode_attrs_f16(D, G, smem, &occ);
+    if (pool.dtype == KV_BF16) e = decode_attrs_bf16(D, G, smem, &occ);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorNotSupported;
+    plan->group = G;
+    plan->stages = S;
+    plan->smem_bytes = smem;
+    plan->num_ctas = pool.num_sms * occ;
+    size_t off = 0;
+    plan->ws_prefix_off = off;
+    off = align_up(off + 4ull * (batch + 1), 256);
+    plan->ws_part_o_off = off;
+    off = align_up(off + 4ull * plan->num_ctas * 2 * G * D, 256);
+    plan->ws_part_lse_off = off;
+    off = align_up(off + 4ull * plan->num_ctas * 2 * G, 256);
+    plan->ws_bytes = off;
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
+                          cudaStream_t stream) {
+    switch (pool.dtype) {
+        case KV_F32: return decode_dispatch_f32(pool, call, plan, stream);
+        case KV_F16: return decode_dispatch_f16(pool, call, plan, stream);
+        case KV_BF16: return decode_dispatch_bf16(pool, call, plan, stream);
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace pagedkv
+
+extern "C" {
+
+kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         kv_dtype dtype, void* k_pool, void* v_pool, kv_pool_t* out) {
+    if (!out) return KV_EINVAL;
+    *out = nullptr;
+    if (dtype != KV_F32 && dtype != KV_F16 && dtype != KV_BF16) return KV_EUNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return KV_EUNSUPPORTED;
+    if (num_blocks < 1 || block_size < 1 || block_size > 256 || num_kv_heads < 1 ||
+        num_kv_heads > 1024)
+        return KV_EINVAL;
+    if ((long long)num_blocks * block_size >= (1ll << 31)) return KV_EINVAL;
+    if (!k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool)) return KV_EINVAL;
+    kv_pool* p = new (std::nothrow) kv_pool();
+    if (!p) return KV_EINVAL;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->num_kv_heads = num_kv_heads;
+    p->head_dim = head_dim;
+    p->dtype = dtype;
+    p->elem_bytes = elem_bytes(dtype);
+    p->k = k_pool;
+    p->v = v_pool;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
+    if (e != cudaSuccess) {
+        if (p->d_err) cudaFree(p->d_err);
+        delete p;
+        return cuda_fail(e, "kv_pool_create");
+    }
+    if (!encode_pool_map(&p->tmap_k, k_pool, *p) || !encode_pool_map(&p->tmap_v, v_pool, *p)) {
+        cudaFree(p->d_err);
+        delete p;
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+                      "kv_pool_create: cuTensorMapEncodeTiled failed");
+        return KV_ECUDA;
+    }
+    *out = p;
+    return KV_OK;
+}
+
+kv_status kv_pool_destroy(kv_pool_t pool) {
+    if (!pool) return KV_OK;
+    cudaError_t e = cudaFree(pool->d_err);
+    delete pool;
+    return e == cudaSuccess ? KV_OK : cuda_fail(e, "kv_pool_destroy");
+}
+
+kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
+                    const int64_t* slot_mapping, int num_tokens, void* stream) {
+    if (!pool || num_tokens < 0) return KV_EINVAL;
+    if (num_tokens == 0) return KV_OK;
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return KV_EINVAL;
+    cudaError_t e = pagedkv::launch_append(*pool, k_new, v_new, slot_mapping, num_tokens,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KV_OK : cuda_fail(e, "kv_append");
+}
+
+kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void* stream) {
+    if (!pool || num_pairs < 0 || num_pairs > (1 << 30)) return KV_EINVAL;
+    if (num_pairs == 0) return KV_OK;
+    if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 7u)) return KV_EINVAL;
+    cudaError_t e = pagedkv::launch_copy_blocks(*pool, pairs, num_pairs,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KV_OK : cuda_fail(e, "copy_blocks");
+}
+
+static kv_status check_decode_shape(kv_pool_t pool, int batch, int num_q_heads) {
+    if (!pool || batch < 1 || num_q_heads < 1) return KV_EINVAL;
+    if (batch > pagedkv::kMaxBatch) return KV_EUNSUPPORTED;
+    if (num_q_heads % pool->num_kv_heads) return KV_EINVAL;
+    const int g = num_q_heads / pool->num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return KV_EUNSUPPORTED;
+    return KV_OK;
+}
+
+kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_heads,
+                                         size_t* bytes) {
+    if (!bytes) return KV_EINVAL;
+    kv_status st = check_decode_shape(pool, batch, num_q_heads);
+    if (st != KV_OK) return st;
+    pagedkv::DecodePlan plan;
+    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, &plan);
+    if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_workspace_size");
+    *bytes = plan.ws_bytes;
+    return KV_OK;
+}
+
+kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                                 int num_kv_heads, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    kv_status st = check_decode_shape(pool, batch, num_q_heads);
+    if (st != KV_OK) return st;
+    if (num_kv_heads != pool->num_kv_heads) return KV_EINVAL;
+    if (!q || !out || !block_tables || !seq_lens || !workspace) return KV_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return KV_EINVAL;
+    if (max_blocks_per_seq < 1) return KV_EINVAL;
+    if ((long long)batch * max_blocks_per_seq * pool->num_kv_heads >= (1ll << 31))
+        return KV_EUNSUPPORTED;
+    if (!(scale == scale)) return KV_EINVAL;
+    pagedkv::DecodePlan plan;
+    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, &plan);
+    if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode(plan)");
+    if (workspace_bytes < plan.ws_bytes) return KV_ENOWORKSPACE;
+    pagedkv::DecodeCall call{q, out, block_tables, max_blocks_per_seq, seq_lens,
+                             batch, num_q_heads, scale, workspace, workspace_bytes};
+    e = pagedkv::launch_decode(*pool, call, plan, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KV_OK : cuda_fail(e, "paged_attention_decode");
+}
+
+kv_status kv_pool_get_error(kv_pool_t pool, int* device_error_bits) {
+    if (!pool || !device_error_bits) return KV_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(device_error_bits, pool->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_pool_get_error");
+    return *device_error_bits ? KV_ERANGE : KV_OK;
+}
+
+kv_status kv_pool_clear_error(kv_pool_t pool) {
+    if (!pool) return KV_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemset(pool->d_err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return e == cudaSuccess ? KV_OK : cuda_fail(e, "kv_pool_clear_error");
+}
+
+const char* kv_strerror(kv_status status) {
+    switch (status) {
+        case KV_OK: return "ok";
+        case KV_EINVAL: return "invalid argument";
+        case KV_EUNSUPPORTED: return "unsupported shape or type";
+        case KV_ECUDA: return "CUDA error";
+        case KV_ERANGE: return "device error word set (out-of-range slot, block, pair or length)";
+        case KV_ENOWORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+const char* kv_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,16 @@
+// Decode kernels for bf16 pools (one translation unit per element type so the
+// instantiations compile in parallel).
+#include "decode_kernel.cuh"
+
+namespace pagedkv {
+
+cudaError_t decode_dispatch_bf16(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
+                               cudaStream_t stream) {
+    return dec::dispatch<__nv_bfloat16>(pool, call, plan, stream);
+}
+
+cudaError_t decode_attrs_bf16(int head_dim, int group, size_t smem, int* ctas_per_sm) {
+    return dec::attrs<__nv_bfloat16>(head_dim, group, smem, ctas_per_sm);
+}
+
+}  // namespace pagedkv

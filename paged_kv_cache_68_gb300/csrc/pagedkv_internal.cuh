@@ -1,0 +1,78 @@
+// Internal declarations shared by the C-ABI front end and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+struct kv_pool {
+    int num_blocks;
+    int block_size;
+    int num_kv_heads;
+    int head_dim;
+    kv_dtype dtype;
+    int elem_bytes;
+    void* k;
+    void* v;
+    int* d_err;             // device error word (KV_DEVERR_* bits)
+    CUtensorMap tmap_k;     // 3-D {head_dim, num_kv_heads, num_blocks*block_size}
+    CUtensorMap tmap_v;
+    int device;
+    int num_sms;
+};
+
+namespace pagedkv {
+
+constexpr int kMaxBatch = 4096;
+
+// Bounded waits: a pipeline wait gives up after this many nanoseconds, sets
+// KV_DEVERR_TIMEOUT and lets the kernel finish without the missing data.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+cudaError_t launch_append(const kv_pool& pool, const void* k_new, const void* v_new,
+                          const int64_t* slots, int num_tokens, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(const kv_pool& pool, const int32_t* pairs, int num_pairs,
+                               cudaStream_t stream);
+
+struct DecodeCall {
+    const void* q;
+    void* out;
+    const int32_t* block_tables;
+    int max_blocks;
+    const int32_t* seq_lens;
+    int batch;
+    int num_q_heads;
+    float scale;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+// Launch plan of one decode: grid size, ring depth, shared memory, workspace.
+struct DecodePlan {
+    int group;
+    int stages;
+    int num_ctas;
+    size_t smem_bytes;
+    size_t ws_bytes;
+    size_t ws_prefix_off, ws_part_o_off, ws_part_lse_off;
+};
+
+// Fill `plan` for this pool / batch / head count on the current device.
+// Returns cudaErrorNotSupported for shapes with no compiled kernel.
+cudaError_t plan_decode(const kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan);
+
+cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
+                          cudaStream_t stream);
+
+// Per-dtype entry points (one translation unit each).
+cudaError_t decode_dispatch_f32(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
+cudaError_t decode_dispatch_f16(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
+cudaError_t decode_dispatch_bf16(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
+cudaError_t decode_attrs_f32(int head_dim, int group, size_t smem, int* ctas_per_sm);
+cudaError_t decode_attrs_f16(int head_dim, int group, size_t smem, int* ctas_per_sm);
+cudaError_t decode_attrs_bf16(int head_dim, int group, size_t smem, int* ctas_per_sm);
+
+}  // namespace pagedkv

@@ -1,0 +1,218 @@
+"""Python binding of ``libpagedkv`` (the C ABI in ``include/pagedkv.h``).
+
+Argument marshalling only: torch tensors are used for device memory and
+streams, and every step of the hot path runs in the library's CUDA kernels.
+There is no fallback: if the library cannot be built or loaded, or a call
+fails, an exception is raised.
+
+The module-level functions carry the C names (``kv_pool_create``,
+``kv_append``, ``copy_blocks``, ``paged_attention_workspace_size``,
+``paged_attention_decode``, ``kv_pool_get_error``, ``kv_pool_clear_error``,
+``kv_pool_destroy``); ``KVPool`` bundles them for convenience.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+KV_OK, KV_EINVAL, KV_EUNSUPPORTED, KV_ECUDA, KV_ERANGE, KV_ENOWORKSPACE = range(6)
+KV_DEVERR_SLOT_RANGE = 0x1
+KV_DEVERR_BLOCK_RANGE = 0x2
+KV_DEVERR_PAIR_RANGE = 0x4
+KV_DEVERR_SEQ_RANGE = 0x8
+KV_DEVERR_TIMEOUT = 0x10
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        lib = load()
+        msg = lib.kv_strerror(status).decode()
+        cuda = lib.kv_last_cuda_error().decode()
+        super().__init__(f"{what}: {msg}" + (f" ({cuda})" if status == KV_ECUDA and cuda else ""))
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build: bool = True) -> ctypes.CDLL:
+    """Load ``libpagedkv.so`` (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build:
+            _build.build()
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"libpagedkv is not built ({_build.LIB_PATH} missing)")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "kv_pool_create": ([I, I, I, I, I, P, P, ctypes.POINTER(P)], I),
+            "kv_pool_destroy": ([P], I),
+            "kv_append": ([P, P, P, P, I, P], I),
+            "copy_blocks": ([P, P, I, P], I),
+            "paged_attention_workspace_size": ([P, I, I, ctypes.POINTER(S)], I),
+            "paged_attention_decode": ([P, P, P, P, I, P, I, I, F, I, P, S, P], I),
+            "kv_pool_get_error": ([P, ctypes.POINTER(I)], I),
+            "kv_pool_clear_error": ([P], I),
+            "kv_strerror": ([I], ctypes.c_char_p),
+            "kv_last_cuda_error": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = args, res
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != KV_OK:
+        raise PagedKVError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+# -- the C entry points, by name -----------------------------------------------
+
+def kv_pool_create(k_pool: torch.Tensor, v_pool: torch.Tensor) -> ctypes.c_void_p:
+    """Describe pools [num_blocks, block_size, num_kv_heads, head_dim]."""
+    if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype or k_pool.dim() != 4:
+        raise ValueError("k_pool and v_pool must be equal-shaped 4-D tensors")
+    if k_pool.dtype not in DTYPE_CODE:
+        raise ValueError(f"unsupported pool dtype {k_pool.dtype}")
+    n, bs, hkv, d = k_pool.shape
+    h = ctypes.c_void_p()
+    _check(load().kv_pool_create(n, bs, hkv, d, DTYPE_CODE[k_pool.dtype],
+                                 _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(h)),
+           "kv_pool_create")
+    return h
+
+
+def kv_pool_destroy(handle) -> None:
+    _check(load().kv_pool_destroy(handle), "kv_pool_destroy")
+
+
+def kv_append(handle, k_new, v_new, slot_mapping, dtype, stream=None) -> None:
+    t = int(slot_mapping.shape[0])
+    _check(load().kv_append(handle, _dev(k_new, "k_new", dtype), _dev(v_new, "v_new", dtype),
+                            _dev(slot_mapping, "slot_mapping", torch.int64), t, _stream(stream)),
+           "kv_append")
+
+
+def copy_blocks(handle, pairs, stream=None) -> None:
+    n = int(pairs.shape[0]) if pairs.numel() else 0
+    ptr = _dev(pairs, "pairs", torch.int32) if n else None
+    _check(load().copy_blocks(handle, ptr, n, _stream(stream)), "copy_blocks")
+
+
+def paged_attention_workspace_size(handle, batch: int, num_q_heads: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().paged_attention_workspace_size(handle, batch, num_q_heads, ctypes.byref(out)),
+           "paged_attention_workspace_size")
+    return int(out.value)
+
+
+def paged_attention_decode(handle, q, out, block_tables, seq_lens, scale: float,
+                           num_kv_heads: int, workspace, dtype, stream=None) -> None:
+    b, hq, _ = q.shape
+    _check(load().paged_attention_decode(
+        handle, _dev(q, "q", dtype), _dev(out, "out", dtype),
+        _dev(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), int(b), int(hq), float(scale), int(num_kv_heads),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "paged_attention_decode")
+
+
+def kv_pool_get_error(handle) -> int:
+    bits = ctypes.c_int()
+    st = load().kv_pool_get_error(handle, ctypes.byref(bits))
+    if st not in (KV_OK, KV_ERANGE):
+        _check(st, "kv_pool_get_error")
+    return int(bits.value)
+
+
+def kv_pool_clear_error(handle) -> None:
+    _check(load().kv_pool_clear_error(handle), "kv_pool_clear_error")
+
+
+# -- convenience wrapper ------------------------------------------------------------
+
+class KVPool:
+    """A KV block pool (two caller-owned tensors) plus its library handle."""
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor):
+        self.k_pool, self.v_pool = k_pool, v_pool
+        self.dtype = k_pool.dtype
+        self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim = k_pool.shape
+        self.handle = kv_pool_create(k_pool, v_pool)
+        self._ws: Optional[torch.Tensor] = None
+
+    def close(self) -> None:
+        if self.handle is not None:
+            kv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def append(self, k_new, v_new, slot_mapping, stream=None) -> None:
+        kv_append(self.handle, k_new, v_new, slot_mapping, self.dtype, stream)
+
+    def copy_blocks(self, pairs, stream=None) -> None:
+        copy_blocks(self.handle, pairs, stream)
+
+    def workspace(self, batch: int, num_q_heads: int) -> torch.Tensor:
+        """A cached device workspace large enough for (batch, num_q_heads)."""
+        need = paged_attention_workspace_size(self.handle, batch, num_q_heads)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.k_pool.device)
+        return self._ws
+
+    def decode(self, q, block_tables, seq_lens, scale: float, out=None, workspace=None,
+               stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(q)
+        if workspace is None:
+            workspace = self.workspace(q.shape[0], q.shape[1])
+        paged_attention_decode(self.handle, q, out, block_tables, seq_lens, scale,
+                               self.num_kv_heads, workspace, self.dtype, stream)
+        return out
+
+    def get_error(self) -> int:
+        return kv_pool_get_error(self.handle)
+
+    def clear_error(self) -> None:
+        kv_pool_clear_error(self.handle)

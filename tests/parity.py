@@ -1,0 +1,97 @@
+"""Shared helpers for the GPU parity tests: run one decode step through the
+C ABI, run the same step through the CPU oracle, compare.
+
+Tolerances (spec bar, written here once):
+  * append / copy: the whole K and V pools must match the oracle byte for byte;
+  * attention, fp32: max |gpu - oracle| <= 1e-5;
+  * attention, fp16 / bf16: max |gpu - oracle| <= 2e-3 per element and
+    max |gpu - oracle| / max |oracle| <= 1e-2.  A bf16 output with
+    |oracle| >= 1 cannot meet 2e-3 (half a bf16 ulp there is 3.9e-3), so such
+    elements must instead lie within one bf16 ulp of the oracle; they are
+    counted and reported.
+"""
+
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+from oracle import c_oracle, np_oracle
+from paged_kv_cache_68_gb300 import pagedkv
+from paged_kv_cache_68_gb300 import workloads as wl
+
+TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+ORACLE_THREADS = max(1, (os.cpu_count() or 2) - 1)
+
+
+def gpu_step(w: wl.Workload, device="cuda", return_pools=True):
+    """copy_blocks -> kv_append -> paged_attention_decode through the C ABI.
+
+    Returns (k_pool, v_pool, out, error_bits); pools/out as raw host arrays.
+    """
+    tv = lambda a: wl.value_to_torch(a, w.dtype, device)
+    k, v = tv(w.k_pool).clone(), tv(w.v_pool).clone()
+    q, kn, vn = tv(w.q), tv(w.k_new), tv(w.v_new)
+    slots = torch.from_numpy(w.slot_mapping).to(device)
+    tables = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device)
+    lens = torch.from_numpy(w.seq_lens).to(device)
+    pairs = torch.from_numpy(np.ascontiguousarray(w.pairs, dtype=np.int32)).to(device)
+    pool = pagedkv.KVPool(k, v)
+    try:
+        pool.copy_blocks(pairs)
+        pool.append(kn, vn, slots)
+        out = pool.decode(q, tables, lens, w.scale)
+        torch.cuda.synchronize()
+        err = pool.get_error()
+    finally:
+        pool.close()
+    res_out = wl.value_to_numpy(out, w.dtype)
+    if not return_pools:
+        return None, None, res_out, err
+    return wl.value_to_numpy(k, w.dtype), wl.value_to_numpy(v, w.dtype), res_out, err
+
+
+def oracle_step(w: wl.Workload, seqs=None):
+    """The same step on the CPU oracle; attention only for `seqs` if given."""
+    h = wl.on_host(w)
+    k, v = h.k_pool.copy(), h.v_pool.copy()
+    assert c_oracle.copy_blocks(k, v, h.pairs, h.dtype) == 0
+    assert c_oracle.append(k, v, h.k_new, h.v_new, h.slot_mapping, h.dtype) == 0
+    sel = np.arange(h.batch) if seqs is None else np.asarray(seqs)
+    out = c_oracle.decode(np.ascontiguousarray(h.q[sel]), k, v, h.dtype,
+                          np.ascontiguousarray(h.block_tables[sel]),
+                          np.ascontiguousarray(h.seq_lens[sel]), h.scale, h.num_kv_heads,
+                          num_threads=ORACLE_THREADS)
+    return k, v, out
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    e = np.floor(np.log2(np.maximum(np.abs(x), 1e-30)))
+    return np.exp2(e - 7)
+
+
+def check_attention(out_raw: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
+    got = np_oracle.to_f64(out_raw, dtype)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    if dtype == "f32":
+        assert err.max() <= 1e-5, f"{what}: max abs err {err.max():.3e} > 1e-5"
+        return {"max_abs": float(err.max()), "exempt": 0}
+    scale = max(float(np.abs(ref).max()), 1e-30)
+    rel = float(err.max()) / scale
+    assert rel <= 1e-2, f"{what}: max rel err {rel:.3e} > 1e-2"
+    exempt = (np.abs(ref) >= 1.0) if dtype == "bf16" else np.zeros_like(ref, dtype=bool)
+    bad = (err > 2e-3) & ~exempt
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements over 2e-3 (max {err[~exempt].max():.3e})"
+    if exempt.any():
+        assert (err[exempt] <= bf16_ulp(ref[exempt])).all(), f"{what}: |out|>=1 element beyond 1 ulp"
+    return {"max_abs": float(err.max()), "max_rel": rel, "exempt": int(exempt.sum())}
+
+
+def assert_pools_equal(got_k, got_v, ref_k, ref_v, what=""):
+    assert got_k.shape == ref_k.shape
+    assert got_k.tobytes() == ref_k.tobytes(), f"{what}: K pool differs from the oracle"
+    assert got_v.tobytes() == ref_v.tobytes(), f"{what}: V pool differs from the oracle"
