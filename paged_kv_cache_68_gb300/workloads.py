@@ -77,7 +77,7 @@ class Workload:
         """Algorithmic HBM bytes of one decode: K/V + q + out + tables + lengths."""
         bs = self.block_size
         tbl = int(sum(-(-int(L) // bs) for L in self.seq_lens)) * 4
-        qo = 2 * self.q.size * self.elem_bytes
+        qo = 2 * int(np.prod(tuple(self.q.shape))) * self.elem_bytes
         return self.kv_bytes() + qo + tbl + 4 * self.batch
 
     def append_bytes(self) -> int:
