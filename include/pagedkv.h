@@ -161,6 +161,34 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attention_decode_noalloc -- paged_attention_decode without a
+ * caller-supplied workspace.  (The source pages have no counterpart: this is
+ * an interface convenience of this library.)
+ *
+ * For callers that cannot allocate device memory -- for example a serving
+ * engine that reserves the whole device for its KV pool up front and forbids
+ * allocation inside the decode loop, or a plug-in whose host framework owns
+ * the allocator and passes it only input and output buffers.  The scratch
+ * comes from an 8 MiB array compiled into the library, held on every device
+ * that loads the library until the process exits.  Arguments, layouts and
+ * results are those of paged_attention_decode.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (once, with the device current); make that first call before any stream
+ * capture.  The call allocates nothing.  All calls share the one array: calls
+ * whose work overlaps on the GPU (other streams, other host threads) race on
+ * it and must be serialised by the caller.  Nothing persists in it between
+ * calls.
+ * Errors: those of paged_attention_decode, and KV_ENOWORKSPACE when the call
+ *   would need more than the 8 MiB maximum (paged_attention_workspace_size
+ *   tells the need).
+ */
+kv_status paged_attention_decode_noalloc(kv_pool_t pool, const void* q, void* out,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* seq_lens, int batch, int num_q_heads,
+                                         float scale, int num_kv_heads, void* stream);
+
+/*
  * kv_pool_get_error -- read the pool's device error word (KV_DEVERR_* bits,
  * OR-ed over every call since the last clear).  Synchronises the device.
  * Returns KV_ERANGE when any bit is set, KV_OK when none is.

@@ -216,3 +216,22 @@ class KVPool:
 
     def clear_error(self) -> None:
         kv_pool_clear_error(self.handle)
+
+
+def paged_attention_decode_noalloc(handle, q, out, block_tables, seq_lens, scale: float,
+                                   num_kv_heads: int, dtype, stream=None) -> None:
+    """Decode without a workspace argument, for callers that cannot allocate
+    device memory (an engine that reserved the device for its KV pool, a
+    plug-in whose host framework owns the allocator): the library's built-in
+    8 MiB scratch array is used.  Calls that overlap on the GPU race on that
+    array; the first call on a device should precede any stream capture."""
+    fn = load().paged_attention_decode_noalloc
+    if fn.restype is not ctypes.c_int:
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [P, P, P, P, I, P, I, I, F, I, P]
+        fn.restype = I
+    b, hq, _ = q.shape
+    _check(fn(handle, _dev(q, "q", dtype), _dev(out, "out", dtype),
+              _dev(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+              _dev(seq_lens, "seq_lens", torch.int32), int(b), int(hq), float(scale),
+              int(num_kv_heads), _stream(stream)), "paged_attention_decode_noalloc")
