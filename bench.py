@@ -66,19 +66,22 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--placement", choices=["random", "identity"], default="random")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (profiling a smaller case)")
     return ap.parse_args(argv)
 
 
-def make_workload(name: str, seed: int, device, placement: str = "random"):
+def make_workload(name: str, seed: int, device, placement: str = "random", batch=None):
     from paged_kv_cache_68_gb300 import workloads as wl
+    kw = {} if batch is None else {"batch": batch}
     if name == "llama3_8b_gqa":
-        return wl.llama3_8b_gqa(seed, device=device, placement=placement)
+        return wl.llama3_8b_gqa(seed, device=device, placement=placement, **kw)
     if name == "opt13b_mha":
-        return wl.opt13b_mha(seed, device=device)
+        return wl.opt13b_mha(seed, device=device, **kw)
     if name == "shared_prefix":
-        return wl.shared_prefix(seed, device=device)
+        return wl.shared_prefix(seed, device=device, **({} if batch is None else {"prompts": batch}))
     if name == "long_context":
-        return wl.long_context(seed, device=device)
+        return wl.long_context(seed, device=device, **kw)
     raise ValueError(name)
 
 
@@ -241,7 +244,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pagedkv.load()
-    w = make_workload(args.workload, args.seed, dev, args.placement)
+    w = make_workload(args.workload, args.seed, dev, args.placement, args.batch)
     tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
     k_pool, v_pool = w.k_pool, w.v_pool
     q, k_new, v_new = tv(w.q), tv(w.k_new), tv(w.v_new)
@@ -344,8 +347,9 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(max_step_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
-                   "placement": args.placement, "global_batch": w.batch * world,
+        "config": {"workload": WORKLOAD_TEXT[args.workload]
+                   + ("" if args.batch is None else f" (batch overridden to {args.batch})"),
+                   "seed": args.seed, "placement": args.placement, "global_batch": w.batch * world,
                    "tokens_per_replica": int(w.seq_lens.sum()),
                    "kv_bytes_per_replica": w.kv_bytes(), "step_bytes_per_replica": step_bytes,
                    "l2": "flushed (512 MB write) between timed steps; KV 1.7 GB > 129 MB L2",
@@ -377,7 +381,7 @@ def run_reference(args):
     from paged_kv_cache_68_gb300 import workloads as wl
     c_oracle.build()
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
-    w = wl.on_host(make_workload(args.workload, args.seed, dev, args.placement))
+    w = wl.on_host(make_workload(args.workload, args.seed, dev, args.placement, args.batch))
     threads = os.cpu_count() or 1
     per_step = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     seqs = pick_sample(w, per_step, threads)

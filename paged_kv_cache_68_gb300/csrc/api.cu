@@ -40,8 +40,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The pool viewed as [N*bs rows][Hkv][D]; one box = the bs rows of one block
-// for one KV head: {D, 1, bs}.
-bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p) {
+// for one KV head: {D, 1, bs} unswizzled, or {128 bytes of dims, 1, bs} with
+// the 128-byte swizzle (one box per half row of a head_dim-128 16-bit pool).
+bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p, bool swizzled) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t elt = (cuuint64_t)p.elem_bytes;
@@ -49,55 +50,83 @@ bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p) {
                           (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_size};
     cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * elt,
                              (cuuint64_t)p.num_kv_heads * p.head_dim * elt};
-    cuuint32_t box[3] = {(cuuint32_t)p.head_dim, 1u, (cuuint32_t)p.block_size};
+    const cuuint32_t inner = swizzled ? (cuuint32_t)(128 / elt) : (cuuint32_t)p.head_dim;
+    cuuint32_t box[3] = {inner, 1u, (cuuint32_t)p.block_size};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapDataType dt =
         p.elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
     return enc(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr size_t kRingBytes = 64 * 1024;   // shared-memory ring per CTA (target)
+constexpr size_t kMaxRingBytes = 128 * 1024;   // shared-memory ring per CTA, at most
 constexpr size_t kMaxSmem = 227 * 1024;
 
 }  // namespace
 
 namespace pagedkv {
 
-cudaError_t plan_decode(const kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan) {
+cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan) {
+    {
+        std::lock_guard<std::mutex> lock(pool.plan_mu);
+        if (pool.plan_batch == batch && pool.plan_hq == num_q_heads) {
+            *plan = pool.plan;
+            return cudaSuccess;
+        }
+    }
     const int G = num_q_heads / pool.num_kv_heads;
     const int D = pool.head_dim, bs = pool.block_size, elt = pool.elem_bytes;
     const size_t stage = 2ull * bs * D * elt;
-    int S = (int)(kRingBytes / stage);
-    S = S < 2 ? 2 : (S > 32 ? 32 : S);
-    size_t smem = 0;
-    for (;; --S) {
-        smem = dec::Layout(S, batch, bs, G, D, elt).total + 1024;
-        if (smem <= kMaxSmem || S == 2) break;
+    // Ring depth S is a multiple of the consumer-warp count (each stage has a
+    // fixed consumer).  Pick the S with the most (resident CTAs x stages per
+    // warp, the latter counted up to 2), then the deepest ring.
+    const int ncw = dec::NCW;
+    int best_s = 0, best_occ = 0, best_score = -1;
+    size_t best_smem = 0;
+    for (int S = ncw; S <= 8 * ncw; S += ncw) {
+        if (S > ncw && (size_t)S * stage > kMaxRingBytes) break;
+        // + 1 KB: the kernel rounds its shared-memory base up to 1 KB
+        const size_t smem = dec::Layout(S, batch, bs, G, D, elt).total + 1024;
+        if (smem > kMaxSmem) break;
+        int occ = 0;
+        cudaError_t e = cudaErrorNotSupported;
+        if (pool.dtype == KV_F32) e = decode_attrs_f32(pool, G, smem, &occ);
+        if (pool.dtype == KV_F16) e = decode_attrs_f16(pool, G, smem, &occ);
+        if (pool.dtype == KV_BF16) e = decode_attrs_bf16(pool, G, smem, &occ);
+        if (e != cudaSuccess) return e;
+        const int per_warp = S / ncw > 2 ? 2 : S / ncw;
+        const int score = occ * per_warp;
+        if (occ >= 1 && score >= best_score) {
+            best_s = S;
+            best_occ = occ;
+            best_score = score;
+            best_smem = smem;
+        }
     }
-    if (smem > kMaxSmem) return cudaErrorNotSupported;
-    int occ = 0;
-    cudaError_t e = cudaErrorNotSupported;
-    if (pool.dtype == KV_F32) e = decode_attrs_f32(D, G, smem, &occ);
-    if (pool.dtype == KV_F16) e = decode_attrs_f16(D, G, smem, &occ);
-    if (pool.dtype == KV_BF16) e = decode_attrs_bf16(D, G, smem, &occ);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorNotSupported;
-    plan->group = G;
-    plan->stages = S;
-    plan->smem_bytes = smem;
-    plan->num_ctas = pool.num_sms * occ;
+    if (best_s == 0 || best_occ < 1) return cudaErrorNotSupported;
+    DecodePlan pl;
+    pl.group = G;
+    pl.stages = best_s;
+    pl.smem_bytes = best_smem;
+    pl.num_ctas = pool.num_sms * best_occ;
     size_t off = 0;
-    plan->ws_prefix_off = off;
+    pl.ws_prefix_off = off;
     off = align_up(off + 4ull * (batch + 1), 256);
-    plan->ws_part_o_off = off;
-    off = align_up(off + 4ull * plan->num_ctas * 2 * G * D, 256);
-    plan->ws_part_lse_off = off;
-    off = align_up(off + 4ull * plan->num_ctas * 2 * G, 256);
-    plan->ws_bytes = off;
+    pl.ws_part_o_off = off;
+    off = align_up(off + 4ull * pl.num_ctas * 2 * G * D, 256);
+    pl.ws_part_lse_off = off;
+    off = align_up(off + 4ull * pl.num_ctas * 2 * G, 256);
+    pl.ws_bytes = off;
+    {
+        std::lock_guard<std::mutex> lock(pool.plan_mu);
+        pool.plan = pl;
+        pool.plan_batch = batch;
+        pool.plan_hq = num_q_heads;
+    }
+    *plan = pl;
     return cudaSuccess;
 }
 
@@ -146,7 +175,13 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
         delete p;
         return cuda_fail(e, "kv_pool_create");
     }
-    if (!encode_pool_map(&p->tmap_k, k_pool, *p) || !encode_pool_map(&p->tmap_v, v_pool, *p)) {
+    p->has_swizzled_maps = p->elem_bytes == 2 && head_dim == 128 && block_size <= 256;
+    bool maps_ok = encode_pool_map(&p->tmap_k, k_pool, *p, false) &&
+                   encode_pool_map(&p->tmap_v, v_pool, *p, false);
+    if (maps_ok && p->has_swizzled_maps)
+        maps_ok = encode_pool_map(&p->tmap_k_swz, k_pool, *p, true) &&
+                  encode_pool_map(&p->tmap_v_swz, v_pool, *p, true);
+    if (!maps_ok) {
         cudaFree(p->d_err);
         delete p;
         std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error,

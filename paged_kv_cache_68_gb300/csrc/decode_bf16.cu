@@ -9,8 +9,8 @@ cudaError_t decode_dispatch_bf16(const kv_pool& pool, const DecodeCall& call, co
     return dec::dispatch<__nv_bfloat16>(pool, call, plan, stream);
 }
 
-cudaError_t decode_attrs_bf16(int head_dim, int group, size_t smem, int* ctas_per_sm) {
-    return dec::attrs<__nv_bfloat16>(head_dim, group, smem, ctas_per_sm);
+cudaError_t decode_attrs_bf16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm) {
+    return dec::attrs<__nv_bfloat16>(pool, group, smem, ctas_per_sm);
 }
 
 }  // namespace pagedkv

@@ -9,8 +9,8 @@ cudaError_t decode_dispatch_f16(const kv_pool& pool, const DecodeCall& call, con
     return dec::dispatch<__half>(pool, call, plan, stream);
 }
 
-cudaError_t decode_attrs_f16(int head_dim, int group, size_t smem, int* ctas_per_sm) {
-    return dec::attrs<__half>(head_dim, group, smem, ctas_per_sm);
+cudaError_t decode_attrs_f16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm) {
+    return dec::attrs<__half>(pool, group, smem, ctas_per_sm);
 }
 
 }  // namespace pagedkv

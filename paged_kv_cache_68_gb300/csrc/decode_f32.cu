@@ -9,8 +9,8 @@ cudaError_t decode_dispatch_f32(const kv_pool& pool, const DecodeCall& call, con
     return dec::dispatch<float>(pool, call, plan, stream);
 }
 
-cudaError_t decode_attrs_f32(int head_dim, int group, size_t smem, int* ctas_per_sm) {
-    return dec::attrs<float>(head_dim, group, smem, ctas_per_sm);
+cudaError_t decode_attrs_f32(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm) {
+    return dec::attrs<float>(pool, group, smem, ctas_per_sm);
 }
 
 }  // namespace pagedkv

@@ -23,25 +23,35 @@
 // 1 for its last -- and the combine kernel merges those.
 //
 // One CTA = 1 producer warp + NCW consumer warps.  The producer walks the
-// CTA's units, looks each block id up in the block table, and issues two TMA
-// tile loads per unit (the K and V rows of that block for KV head g: a
-// [block_size, head_dim] box of the pool viewed as [N*bs, Hkv, D]) into a ring
-// of S shared-memory stages guarded by full/empty mbarriers.  Consumer warp w
-// takes units w, w+NCW, ... of each piece (one warp per KV block), so the K/V
-// of a block is loaded once for the whole GQA group of G query heads.
-//   QK: TPT lanes per token, each holding D/TPT dims of all G (pre-scaled)
-//       query rows in registers; the G partial dot products are reduced across
-//       the TPT lanes with a transposing shuffle reduction.
-//   softmax: per block, per head, fp32, base 2 (q carries scale*log2 e).
-//   PV: each lane owns 4 dims of the G output rows; p is broadcast from
-//       shared memory.  Rows past the sequence end are never touched.
-// At the end of a piece the NCW warps' (m, l, o) are merged through shared
-// memory (double-buffered, one named barrier per piece).
+// CTA's units, looks each block id up in the block table, and issues the TMA
+// tile loads of the unit (the K and V rows of that block for KV head g: boxes
+// of the pool viewed as [N*bs, Hkv, D]) into a ring of S shared-memory stages
+// guarded by full/empty mbarriers.  Unit k of the CTA goes to stage k % S and
+// is consumed by warp k % NCW; S is a multiple of NCW, so every stage has one
+// fixed consumer that waits on it in order (the parity of an mbarrier wait is
+// only unambiguous when the waiter is at most one phase ahead).  The K/V of a
+// block is loaded once for the whole GQA group of G query heads.  Two compute
+// policies share this frame:
+//   CorePolicy (CUDA cores; fp32 pools, groups of 1-2, odd block sizes):
+//     QK with TPT lanes per token holding D/TPT dims of all G pre-scaled query
+//     rows, a transposing shuffle reduction, packed fp32x2 FMAs; PV with each
+//     lane owning 4 dims of the G output rows.
+//   TcPolicy (tensor cores, mma.sync m16n8k16; 16-bit pools, groups of 4 or
+//     8, block sizes 16 and 32): S^T[tokens x heads] = K_blk Q^T and
+//     O^T[dims x heads] += V_blk^T P^T, the group's heads filling N = 8.
+//     K/V tiles arrive 128-byte-swizzled so ldmatrix is conflict-free; P^T is
+//     transposed in registers with movmatrix and fed as bf16/f16 hi + lo
+//     halves, so its rounding stays below 2^-17 relative.
+// Softmax state is per block, per head, fp32, base 2.  Rows past the sequence
+// end never contribute.  At the end of a piece the NCW warps' (m, l, o) are
+// merged through shared memory by warp 0 (split arrive/sync named barriers).
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
+
+#include <type_traits>
 
 #include "pagedkv_internal.cuh"
 
@@ -75,7 +85,7 @@ struct Params {
 
 // ---------------------------------------------------------------- layout ---
 struct Layout {
-    uint32_t full, empty, valid, misc, prefix, lens, sbuf, abuf, merge_o, merge_ml, ring;
+    uint32_t full, empty, valid, misc, prefix, pbuf, abuf, merge_o, merge_ml, ring;
     uint32_t stage_bytes, total;
     __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt) {
         uint32_t off = 0;
@@ -84,14 +94,12 @@ struct Layout {
         valid = off;  off += 4u * S;
         misc = off;   off += 4u * 40;            // abort flag + warp totals
         prefix = off; off += 4u * (B + 1);
-        lens = off;   off += 4u * B;
         off = (off + 15u) & ~15u;
-        sbuf = off;   off += 4u * NCW * bs * G;
-        abuf = off;   off += 4u * NCW * G;
-        off = (off + 15u) & ~15u;
-        merge_o = off;  off += 2u * 4u * NCW * G * D;
-        merge_ml = off; off += 2u * 2u * 4u * NCW * G;
-        off = (off + 1023u) & ~1023u;
+        pbuf = off;   off += 8u * NCW * bs * G;
+        abuf = off;   off += 8u * NCW * G;
+        merge_o = off;  off += 4u * (NCW - 1) * G * D;
+        merge_ml = off; off += 2u * 4u * (NCW - 1) * G;
+        off = (off + 1023u) & ~1023u;              // swizzle atoms are 1 KB
         ring = off;
         stage_bytes = 2u * bs * D * elt;         // K tile then V tile, 128-byte multiples
         off += stage_bytes * S;
@@ -145,8 +153,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void consumer_barrier() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+// Named barriers among the NCW consumer warps (id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NCW * 32) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(NCW * 32) : "memory");
 }
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -157,6 +169,64 @@ __device__ __forceinline__ float fast_log2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// -- tensor-core helpers (16-bit operands, fp32 accumulate) --
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+template <typename T> struct Mma;
+template <> struct Mma<__nv_bfloat16> {
+    __device__ static __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // (lo, hi) -> packed pair, element `lo` in the low half
+    __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+    __device__ static __forceinline__ float2 unpack(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+};
+template <> struct Mma<__half> {
+    __device__ static __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+    __device__ static __forceinline__ float2 unpack(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+};
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------ element I/O --
@@ -170,6 +240,14 @@ template <> struct Elt<float> {
     // 4 values starting at p (16 bytes)
     __device__ static __forceinline__ void four(const unsigned char* p, float* f) {
         chunk(*reinterpret_cast<const uint4*>(p), f);
+    }
+    // the same as consecutive pairs (element 2i in .x, 2i+1 in .y)
+    __device__ static __forceinline__ void chunk2(uint4 r, float2* f) {
+        f[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+        f[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
+    __device__ static __forceinline__ void four2(const unsigned char* p, float2* f) {
+        chunk2(*reinterpret_cast<const uint4*>(p), f);
     }
     __device__ static __forceinline__ float store(float x) { return x; }
 };
@@ -185,6 +263,16 @@ template <> struct Elt<__half> {
         const uint2 r = *reinterpret_cast<const uint2*>(p);
         pair(r.x, f); pair(r.y, f + 2);
     }
+    __device__ static __forceinline__ float2 pair2(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+    __device__ static __forceinline__ void chunk2(uint4 r, float2* f) {
+        f[0] = pair2(r.x); f[1] = pair2(r.y); f[2] = pair2(r.z); f[3] = pair2(r.w);
+    }
+    __device__ static __forceinline__ void four2(const unsigned char* p, float2* f) {
+        const uint2 r = *reinterpret_cast<const uint2*>(p);
+        f[0] = pair2(r.x); f[1] = pair2(r.y);
+    }
     __device__ static __forceinline__ __half store(float x) { return __float2half_rn(x); }
 };
 template <> struct Elt<__nv_bfloat16> {
@@ -199,6 +287,16 @@ template <> struct Elt<__nv_bfloat16> {
     __device__ static __forceinline__ void four(const unsigned char* p, float* f) {
         const uint2 r = *reinterpret_cast<const uint2*>(p);
         pair(r.x, f); pair(r.y, f + 2);
+    }
+    __device__ static __forceinline__ float2 pair2(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ static __forceinline__ void chunk2(uint4 r, float2* f) {
+        f[0] = pair2(r.x); f[1] = pair2(r.y); f[2] = pair2(r.z); f[3] = pair2(r.w);
+    }
+    __device__ static __forceinline__ void four2(const unsigned char* p, float2* f) {
+        const uint2 r = *reinterpret_cast<const uint2*>(p);
+        f[0] = pair2(r.x); f[1] = pair2(r.y);
     }
     __device__ static __forceinline__ __nv_bfloat16 store(float x) { return __float2bfloat16_rn(x); }
 };
@@ -264,29 +362,428 @@ __host__ __device__ __forceinline__ int unit_chunk(int U, int num_ctas) {
     return c < kMinChunk ? kMinChunk : c;
 }
 
+// ------------------------------------------------------- compute policies --
+// Both policies keep one warp's running softmax state for one (b, g) piece and
+// expose: begin (load the group's query rows), block (fold one KV block in),
+// fold (finish cross-lane sums), put (leave the state for warp 0) and
+// merge_store (warp 0: merge the other warps' states with its own, write the
+// output or the partial).
+
+// Where warp 0 writes a finished piece.
+struct PieceOut {
+    bool complete;        // whole (b, g): write `out`; else a partial slot
+    void* out;            // &out[b, g*G, 0] (element type of the pool)
+    float* part_o;        // &part_o[slot][0][0]
+    float* part_lse;      // &part_lse[slot][0]
+};
+
+template <typename T, int D, int G, int BSC>
+struct CorePolicy {
+    using C = Cfg<T, D, G>;
+    static constexpr bool kSwizzled = false;
+    static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
+
+    float2* pb;                   // this warp's (score | p, p) [bs][G]
+    float2* ab;                   // this warp's (alpha, alpha) [G]
+    float2 qf[G][C::QE / 2];      // scaled query rows, pairs of consecutive dims
+    float2 o[G][2];               // dims dl*4 .. dl*4+3 of each head
+    float m_run, l_run;           // for head lane % G
+
+    __device__ __forceinline__ CorePolicy(float2* pbuf, float2* abuf) : pb(pbuf), ab(abuf) {}
+
+    __device__ __forceinline__ void begin(const T* qp, float qscale, int lane) {
+        const int jl = lane % C::TPT;
+        const float2 sc2 = make_float2(qscale, qscale);
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int i = 0; i < C::NCH; ++i) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                    qp + (size_t)h * D + (jl + C::TPT * i) * C::VE));
+                float2 f[C::VE / 2];
+                Elt<T>::chunk2(raw, f);
+#pragma unroll
+                for (int e = 0; e < C::VE / 2; ++e) qf[h][i * C::VE / 2 + e] = __fmul2_rn(f[e], sc2);
+            }
+        m_run = -CUDART_INF_F;
+        l_run = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) o[h][0] = o[h][1] = make_float2(0.f, 0.f);
+    }
+
+    __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
+                                          int n_valid, int bs_rt, float, int lane) {
+        const int bs = BSC > 0 ? BSC : bs_rt;
+        const int tg = lane / C::TPT, jl = lane % C::TPT;
+        const int hsel = (jl >> C::HSHIFT) & (G - 1);
+        const bool leader = (jl & ((1 << C::HSHIFT) - 1)) == 0;
+        const int hh = lane % G;
+        const int tv = lane / C::LPV, dl = lane % C::LPV;
+        // -- scores --------------------------------------------------------
+#pragma unroll 1
+        for (int t0 = 0; t0 < bs; t0 += C::TPS) {
+            const int t = t0 + tg;
+            float2 acc2[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc2[h] = make_float2(0.f, 0.f);
+            if (t < n_valid) {
+#pragma unroll
+                for (int i = 0; i < C::NCH; ++i) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(
+                        Ks + (uint32_t)(t * C::CHUNKS + jl + C::TPT * i) * 16u);
+                    float2 kf[C::VE / 2];
+                    Elt<T>::chunk2(raw, kf);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int e = 0; e < C::VE / 2; ++e)
+                            acc2[h] = __ffma2_rn(qf[h][i * C::VE / 2 + e], kf[e], acc2[h]);
+                }
+            }
+            float acc[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] = acc2[h].x + acc2[h].y;
+            TReduce<G, C::TPT / 2>::run(acc, lane);
+            if (leader && t < bs) pb[t * G + hsel].x = (t < n_valid) ? acc[0] : -CUDART_INF_F;
+        }
+        __syncwarp();
+        // -- online softmax, per head ---------------------------------------
+        float mloc = -CUDART_INF_F;
+#pragma unroll
+        for (int t = lane / G; t < bs; t += 32 / G) mloc = fmaxf(mloc, pb[t * G + hh].x);
+#pragma unroll
+        for (int off = 16; off >= G; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(FULL, mloc, off));
+        const float m_new = fmaxf(m_run, mloc);
+        float alpha = 1.f, lsum = 0.f;
+        if (m_new != -CUDART_INF_F) {
+            alpha = fast_exp2(m_run - m_new);
+            for (int t = lane / G; t < bs; t += 32 / G) {
+                const float pe = fast_exp2(pb[t * G + hh].x - m_new);
+                pb[t * G + hh] = make_float2(pe, pe);
+                lsum += pe;
+            }
+        } else {
+            for (int t = lane / G; t < bs; t += 32 / G) pb[t * G + hh] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int off = 16; off >= G; off >>= 1) lsum += __shfl_xor_sync(FULL, lsum, off);
+        l_run = l_run * alpha + lsum;
+        m_run = m_new;
+        if (lane < G) ab[lane] = make_float2(alpha, alpha);
+        __syncwarp();
+        // -- weighted sum of V ------------------------------------------------
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float2 a = ab[h];
+            o[h][0] = __fmul2_rn(o[h][0], a);
+            o[h][1] = __fmul2_rn(o[h][1], a);
+        }
+#pragma unroll 4
+        for (int tt = 0; tt < bs; tt += C::TPSV) {
+            const int t = tt + tv;
+            if (t < n_valid) {
+                float2 vf[2];
+                Elt<T>::four2(Vs + (uint32_t)(t * D + dl * 4) * C::ELT, vf);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float2 pr = pb[t * G + h];
+                    o[h][0] = __ffma2_rn(pr, vf[0], o[h][0]);
+                    o[h][1] = __ffma2_rn(pr, vf[1], o[h][1]);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void fold(int) {
+#pragma unroll
+        for (int off = C::LPV; off < 32; off <<= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    o[h][e].x += __shfl_xor_sync(FULL, o[h][e].x, off);
+                    o[h][e].y += __shfl_xor_sync(FULL, o[h][e].y, off);
+                }
+    }
+
+    // merge area: o [NCW-1][G][D], then m [NCW-1][G], l [NCW-1][G]
+    __device__ __forceinline__ void put(float* mo, float* mm, int w, int lane) const {
+        const int dl = lane % C::LPV;
+        if (lane < C::LPV) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                *reinterpret_cast<float4*>(mo + ((w - 1) * G + h) * D + dl * 4) =
+                    make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+        }
+        if (lane < G) {
+            mm[(w - 1) * G + lane] = m_run;
+            mm[(NCW - 1) * G + (w - 1) * G + lane] = l_run;
+        }
+    }
+
+    __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
+                                                const PieceOut& po) const {
+        const int dl = lane % C::LPV;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float m0 = __shfl_sync(FULL, m_run, h);
+            const float l0 = __shfl_sync(FULL, l_run, h);
+            float M = m0;
+#pragma unroll
+            for (int w2 = 1; w2 < NCW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
+            float den = 0.f;
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -CUDART_INF_F) {
+                const float c0 = fast_exp2(m0 - M);
+                den = c0 * l0;
+                num = make_float4(c0 * o[h][0].x, c0 * o[h][0].y, c0 * o[h][1].x, c0 * o[h][1].y);
+#pragma unroll
+                for (int w2 = 1; w2 < NCW; ++w2) {
+                    const float c = fast_exp2(mm[(w2 - 1) * G + h] - M);
+                    den += c * mm[(NCW - 1) * G + (w2 - 1) * G + h];
+                    const float4 ow =
+                        *reinterpret_cast<const float4*>(mo + ((w2 - 1) * G + h) * D + dl * 4);
+                    num.x += c * ow.x; num.y += c * ow.y; num.z += c * ow.z; num.w += c * ow.w;
+                }
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            if (lane < C::LPV) {
+                if (po.complete) {
+                    T* op = static_cast<T*>(po.out) + h * D + dl * 4;
+                    op[0] = Elt<T>::store(num.x * inv);
+                    op[1] = Elt<T>::store(num.y * inv);
+                    op[2] = Elt<T>::store(num.z * inv);
+                    op[3] = Elt<T>::store(num.w * inv);
+                } else {
+                    *reinterpret_cast<float4*>(po.part_o + h * D + dl * 4) =
+                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+                    if (lane == 0) po.part_lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
+                }
+            }
+        }
+    }
+};
+
+// Tensor-core policy.  Lane roles in the m16n8k16 fragments: gid = lane / 4,
+// tig = lane % 4.  S^T (tokens x heads): the lane holds tokens gid, gid + 8 of
+// each 16-token tile for heads 2 tig, 2 tig + 1.  O^T (dims x heads): the lane
+// holds dims 16 mt + gid, 16 mt + gid + 8 for the same two heads.  Heads >= G
+// are padding (zero query rows) and are never written out.
+template <typename T, int D, int G, int BSC>
+struct TcPolicy {
+    static_assert(sizeof(T) == 2, "tensor-core path takes 16-bit pools");
+    static_assert(BSC % 16 == 0 && BSC > 0, "tensor-core path needs a block size of 16k");
+    static_assert(G == 4 || G == 8, "tensor-core path fills N = 8 with 4 or 8 heads");
+    static constexpr bool kSwizzled = true;
+    static constexpr int kMinBlocks = 3;
+    static constexpr int KS = D / 16;      // QK k-steps (16 dims each)
+    static constexpr int MT = D / 16;      // PV m-tiles (16 dims each)
+    static constexpr int TT = BSC / 16;    // 16-token tiles per block
+
+    uint32_t qb[KS][2];                    // Q^T fragments (raw 16-bit query)
+    float oacc[MT][4];                     // O^T accumulators
+    float m_run[2], l_run[2];              // heads 2 tig, 2 tig + 1
+
+    __device__ __forceinline__ TcPolicy(float2*, float2*) {}
+
+    // Shared address of 16-byte chunk c of row r in a 128-byte-swizzled tile
+    // of `rows` rows (chunks 0-7 in the first 128-byte half, 8-15 in the second).
+    __device__ static __forceinline__ uint32_t swz(uint32_t tile, int r, int c) {
+        return tile + (uint32_t)((c >> 3) * BSC * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
+
+    __device__ __forceinline__ void begin(const T* qp, float, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                qb[ks][j] = gid < G ? __ldg(reinterpret_cast<const uint32_t*>(
+                                          qp + gid * D + ks * 16 + j * 8 + tig * 2))
+                                    : 0u;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+        m_run[0] = m_run[1] = -CUDART_INF_F;
+        l_run[0] = l_run[1] = 0.f;
+    }
+
+    __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
+                                          int n_valid, int, float qscale, int lane) {
+        const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, r8 = lane & 7;
+        const uint32_t kbase = smem_u32(Ks), vbase = smem_u32(Vs);
+        if (n_valid < BSC) {
+            // rows past the sequence end may hold anything; P is 0 there, and
+            // 0 * NaN would still poison the MMA, so clear those V rows
+            unsigned char* V = const_cast<unsigned char*>(Vs);
+            const int nbytes = (BSC - n_valid) * 128;
+            for (int i = lane * 16; i < nbytes; i += 32 * 16)
+#pragma unroll
+                for (int hf = 0; hf < D / 64; ++hf)
+                    *reinterpret_cast<uint4*>(V + hf * BSC * 128 + n_valid * 128 + i) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async();
+            __syncwarp();
+        }
+        // -- S^T = K_blk Q^T, scaled to base 2, masked past the end ----------
+        float s[TT][4];
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(a, swz(kbase, tt * 16 + (mi & 1) * 8 + r8, ks * 2 + (mi >> 1)));
+                Mma<T>::run(acc, a, qb[ks][0], qb[ks][1]);
+            }
+            const bool v0 = tt * 16 + gid < n_valid, v1 = tt * 16 + gid + 8 < n_valid;
+            s[tt][0] = v0 ? acc[0] * qscale : -CUDART_INF_F;
+            s[tt][1] = v0 ? acc[1] * qscale : -CUDART_INF_F;
+            s[tt][2] = v1 ? acc[2] * qscale : -CUDART_INF_F;
+            s[tt][3] = v1 ? acc[3] * qscale : -CUDART_INF_F;
+        }
+        // -- online softmax for heads 2 tig (j = 0) and 2 tig + 1 (j = 1) -----
+        float alpha[2];
+        float mnew[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int tt = 0; tt < TT; ++tt) mx = fmaxf(mx, fmaxf(s[tt][j], s[tt][j + 2]));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+            mnew[j] = fmaxf(m_run[j], mx);
+            alpha[j] = mnew[j] == -CUDART_INF_F ? 1.f : fast_exp2(m_run[j] - mnew[j]);
+        }
+        float lsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = e & 1;
+                const float pe = mnew[j] == -CUDART_INF_F ? 0.f : fast_exp2(s[tt][e] - mnew[j]);
+                s[tt][e] = pe;
+                lsum[j] += pe;
+            }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            lsum[j] += __shfl_xor_sync(FULL, lsum[j], 4);
+            lsum[j] += __shfl_xor_sync(FULL, lsum[j], 8);
+            lsum[j] += __shfl_xor_sync(FULL, lsum[j], 16);
+            l_run[j] = l_run[j] * alpha[j] + lsum[j];
+            m_run[j] = mnew[j];
+        }
+        const float2 a2 = make_float2(alpha[0], alpha[1]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            float2 lo = __fmul2_rn(make_float2(oacc[mt][0], oacc[mt][1]), a2);
+            float2 hi = __fmul2_rn(make_float2(oacc[mt][2], oacc[mt][3]), a2);
+            oacc[mt][0] = lo.x; oacc[mt][1] = lo.y; oacc[mt][2] = hi.x; oacc[mt][3] = hi.y;
+        }
+        // -- O^T += V_blk^T P^T, P as hi + lo 16-bit halves -------------------
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) {
+            const uint32_t h01 = Mma<T>::pack(s[tt][0], s[tt][1]);
+            const uint32_t h23 = Mma<T>::pack(s[tt][2], s[tt][3]);
+            const float2 f01 = Mma<T>::unpack(h01), f23 = Mma<T>::unpack(h23);
+            const uint32_t l01 = Mma<T>::pack(s[tt][0] - f01.x, s[tt][1] - f01.y);
+            const uint32_t l23 = Mma<T>::pack(s[tt][2] - f23.x, s[tt][3] - f23.y);
+            const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
+            const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_t(a, swz(vbase, tt * 16 + (mi >> 1) * 8 + r8, mt * 2 + (mi & 1)));
+                Mma<T>::run(oacc[mt], a, bh0, bh1);
+                Mma<T>::run(oacc[mt], a, bl0, bl1);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void fold(int) {}
+
+    __device__ __forceinline__ void put(float* mo, float* mm, int w, int lane) const {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int h = 2 * tig + j;
+            if (h < G) {
+                float* row = mo + ((w - 1) * G + h) * D;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    row[mt * 16 + gid] = oacc[mt][j];
+                    row[mt * 16 + gid + 8] = oacc[mt][j + 2];
+                }
+                if (gid == 0) {
+                    mm[(w - 1) * G + h] = m_run[j];
+                    mm[(NCW - 1) * G + (w - 1) * G + h] = l_run[j];
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
+                                                const PieceOut& po) const {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int h = 2 * tig + j;
+            if (h >= G) continue;
+            float M = m_run[j];
+#pragma unroll
+            for (int w2 = 1; w2 < NCW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
+            float c[NCW];
+            float den = 0.f;
+            c[0] = M == -CUDART_INF_F ? 0.f : fast_exp2(m_run[j] - M);
+            den = c[0] * l_run[j];
+#pragma unroll
+            for (int w2 = 1; w2 < NCW; ++w2) {
+                c[w2] = M == -CUDART_INF_F ? 0.f : fast_exp2(mm[(w2 - 1) * G + h] - M);
+                den += c[w2] * mm[(NCW - 1) * G + (w2 - 1) * G + h];
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int d = mt * 16 + gid + 8 * hf;
+                    float num = c[0] * oacc[mt][j + 2 * hf];
+#pragma unroll
+                    for (int w2 = 1; w2 < NCW; ++w2) num += c[w2] * mo[((w2 - 1) * G + h) * D + d];
+                    if (po.complete)
+                        static_cast<T*>(po.out)[h * D + d] = Elt<T>::store(num * inv);
+                    else
+                        po.part_o[h * D + d] = num * inv;
+                }
+            if (!po.complete && gid == 0)
+                po.part_lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
+        }
+    }
+};
+
 // ------------------------------------------------------------ split kernel --
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(NTHREADS) paged_decode_split(
+template <typename T, int D, int G, class Pol>
+__global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
-    using C = Cfg<T, D, G>;
+    constexpr int ELT = sizeof(T);
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int B = p.batch, bs = p.bs, S = p.stages, H = p.num_kv_heads;
-    const Layout lay(S, B, bs, G, D, C::ELT);
+    const int B = p.batch, S = p.stages, H = p.num_kv_heads, bs = p.bs;
+    const Layout lay(S, B, bs, G, D, ELT);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc);
     int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
     int* prefix = reinterpret_cast<int*>(smem + lay.prefix);
-    int* lens = reinterpret_cast<int*>(smem + lay.lens);
     unsigned char* ring = smem + lay.ring;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cap = p.max_blocks * bs;              // longest context a table can hold
 
-    // -- 1. clamped lengths and the blocks-per-sequence prefix --------------
+    // -- 1. the blocks-per-sequence prefix of the clamped lengths -----------
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -296,17 +793,14 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {
-        const int cap = p.max_blocks * bs;
         const int per = (B + NTHREADS - 1) / NTHREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int local = 0;
         bool over = false;
         for (int b = b0; b < b1; ++b) {
-            int L = p.seq_lens[b];
-            L = L < 0 ? 0 : L;
-            if (L > cap) { over = true; L = cap; }
-            lens[b] = L;
-            local += (L + bs - 1) / bs;
+            const int L = p.seq_lens[b];
+            over |= L > cap;
+            local += (min(max(L, 0), cap) + bs - 1) / bs;
         }
         if (over && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_SEQ_RANGE);
         int x = local;
@@ -322,7 +816,7 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
         int run = woff + x - local;
         for (int b = b0; b < b1; ++b) {
             prefix[b] = run;
-            run += (lens[b] + bs - 1) / bs;
+            run += (min(max(p.seq_lens[b], 0), cap) + bs - 1) / bs;
         }
         if (tid == NTHREADS - 1) prefix[B] = woff + x;
     }
@@ -339,7 +833,10 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
     if (warp == NCW) {
         // ---------------------------------------------------- producer warp --
         // Lanes look up the block ids of the next 32 units in parallel; lane 0
-        // then issues the TMA loads one unit at a time.
+        // issues the TMA loads one unit at a time: one box per tile, or one
+        // per 128-byte half of the row for the swizzled layout.
+        constexpr int kBoxes = Pol::kSwizzled ? D * ELT / 128 : 1;
+        const uint32_t box_bytes = (uint32_t)bs * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
         auto fetch = [&](int uu, int& id, int& gg) {
             id = -1;
             gg = 0;
@@ -373,8 +870,13 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
                         valid[s] = 1;
                         mbar_arrive_tx(fb, lay.stage_bytes);
                         const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
-                        tma_load_3d(dst, &tmap_k, 0, gg, id * bs, fb);
-                        tma_load_3d(dst + lay.stage_bytes / 2, &tmap_v, 0, gg, id * bs, fb);
+#pragma unroll
+                        for (int x = 0; x < kBoxes; ++x) {
+                            const int col = x * (int)(128 / ELT);
+                            tma_load_3d(dst + x * box_bytes, &tmap_k, col, gg, id * bs, fb);
+                            tma_load_3d(dst + lay.stage_bytes / 2 + x * box_bytes, &tmap_v, col, gg,
+                                        id * bs, fb);
+                        }
                     } else {
                         valid[s] = 0;
                         if (ok) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
@@ -396,17 +898,16 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
 
     // ---------------------------------------------------- consumer warps ----
     const int w = warp;
-    const int tg = lane / C::TPT, jl = lane % C::TPT;
-    const int hsel = (jl >> C::HSHIFT) & (G - 1);
-    const bool leader = (jl & ((1 << C::HSHIFT) - 1)) == 0;
-    const int hh = lane % G;                       // head this lane tracks in softmax
-    const int tv = lane / C::LPV, dl = lane % C::LPV;
-    float* sb = reinterpret_cast<float*>(smem + lay.sbuf) + w * bs * G;   // [bs][G]
-    float* ab = reinterpret_cast<float*>(smem + lay.abuf) + w * G;
+    float2* pb = reinterpret_cast<float2*>(smem + lay.pbuf) + w * bs * G;
+    float2* ab = reinterpret_cast<float2*>(smem + lay.abuf) + w * G;
+    // merge area: warps 1..NCW-1 leave (o [G][D], m [G], l [G]) for warp 0
+    float* mo = reinterpret_cast<float*>(smem + lay.merge_o);
+    float* mm = reinterpret_cast<float*>(smem + lay.merge_ml);
     const T* qbase = static_cast<const T*>(p.q);
     T* obase = static_cast<T*>(p.out);
+    Pol pol(pb, ab);
 
-    int sel = 0;
+    bool first_piece = true;
     for (int u = start; u < end;) {
         const int b = find_seq(prefix, B, u, H);
         const int nb = prefix[b + 1] - prefix[b];
@@ -415,32 +916,14 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
         const int j0 = r - g * nb;
         const int seg_start = prefix[b] * H + g * nb;
         const int piece_end = min(end, seg_start + nb);
-        const int Lb = lens[b];
+        const int Lb = min(max(p.seq_lens[b], 0), cap);
+        const size_t head0 = (size_t)b * p.num_q_heads + (size_t)g * G;
 
-        // query rows of the group, scaled by scale * log2(e), in registers
-        float qf[G][C::QE];
-        {
-            const T* qp = qbase + ((size_t)b * p.num_q_heads + (size_t)g * G) * D;
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int i = 0; i < C::NCH; ++i) {
-                    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                        qp + (size_t)h * D + (jl + C::TPT * i) * C::VE));
-                    float f[C::VE];
-                    Elt<T>::chunk(raw, f);
-#pragma unroll
-                    for (int e = 0; e < C::VE; ++e) qf[h][i * C::VE + e] = f[e] * p.qscale;
-                }
-        }
-        float m_run = -CUDART_INF_F, l_run = 0.f;
-        float o[G][4];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
+        pol.begin(qbase + head0 * D, p.qscale, lane);
 
-        for (int uu = u + w; uu < piece_end; uu += NCW) {
+        // this warp's units of the piece: those with (uu - start) % NCW == w
+        const int first = u + ((w - (u - start) % NCW) + NCW) % NCW;
+        for (int uu = first; uu < piece_end; uu += NCW) {
             const int k = uu - start, s = k % S;
             bool ok = *abort_flag == 0;
             if (ok && !mbar_wait(smem_u32(&full[s]), (k / S) & 1)) {
@@ -451,128 +934,38 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_split(
             ok = __all_sync(FULL, ok);
             if (ok && valid[s]) {
                 const int j = j0 + (uu - u);
-                const int n_valid = min(bs, Lb - j * bs);
                 const unsigned char* Ks = ring + (size_t)s * lay.stage_bytes;
-                const unsigned char* Vs = Ks + lay.stage_bytes / 2;
-                // -- scores --------------------------------------------------
-                for (int t0 = 0; t0 < bs; t0 += C::TPS) {
-                    const int t = t0 + tg;
-                    float acc[G];
-#pragma unroll
-                    for (int h = 0; h < G; ++h) acc[h] = 0.f;
-                    if (t < n_valid) {
-#pragma unroll
-                        for (int i = 0; i < C::NCH; ++i) {
-                            const uint4 raw = *reinterpret_cast<const uint4*>(
-                                Ks + ((size_t)t * C::CHUNKS + jl + C::TPT * i) * 16);
-                            float kf[C::VE];
-                            Elt<T>::chunk(raw, kf);
-#pragma unroll
-                            for (int h = 0; h < G; ++h)
-#pragma unroll
-                                for (int e = 0; e < C::VE; ++e)
-                                    acc[h] = fmaf(qf[h][i * C::VE + e], kf[e], acc[h]);
-                        }
-                    }
-                    TReduce<G, C::TPT / 2>::run(acc, lane);
-                    if (leader && t < bs) sb[t * G + hsel] = (t < n_valid) ? acc[0] : -CUDART_INF_F;
-                }
-                __syncwarp();
-                // -- online softmax, per head -----------------------------------
-                float mloc = -CUDART_INF_F;
-                for (int t = lane / G; t < bs; t += 32 / G) mloc = fmaxf(mloc, sb[t * G + hh]);
-#pragma unroll
-                for (int off = 16; off >= G; off >>= 1)
-                    mloc = fmaxf(mloc, __shfl_xor_sync(FULL, mloc, off));
-                const float m_new = fmaxf(m_run, mloc);
-                float alpha = 1.f, lsum = 0.f;
-                if (m_new != -CUDART_INF_F) {
-                    alpha = fast_exp2(m_run - m_new);
-                    for (int t = lane / G; t < bs; t += 32 / G) {
-                        const float pe = fast_exp2(sb[t * G + hh] - m_new);
-                        sb[t * G + hh] = pe;
-                        lsum += pe;
-                    }
-                } else {
-                    for (int t = lane / G; t < bs; t += 32 / G) sb[t * G + hh] = 0.f;
-                }
-#pragma unroll
-                for (int off = 16; off >= G; off >>= 1) lsum += __shfl_xor_sync(FULL, lsum, off);
-                l_run = l_run * alpha + lsum;
-                m_run = m_new;
-                if (lane < G) ab[lane] = alpha;
-                __syncwarp();
-                // -- weighted sum of V -------------------------------------------
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float a = ab[h];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[h][e] *= a;
-                }
-                for (int t = tv; t < n_valid; t += C::TPSV) {
-                    float vf[4];
-                    Elt<T>::four(Vs + ((size_t)t * D + dl * 4) * C::ELT, vf);
-                    float pr[G];
-#pragma unroll
-                    for (int h = 0; h < G; ++h) pr[h] = sb[t * G + h];
-#pragma unroll
-                    for (int h = 0; h < G; ++h)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) o[h][e] = fmaf(pr[h], vf[e], o[h][e]);
-                }
+                pol.block(Ks, Ks + lay.stage_bytes / 2, min(bs, Lb - j * bs), bs, p.qscale, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
 
         // -- merge the NCW warps' partial softmaxes of this piece -------------
-        float* mo = reinterpret_cast<float*>(smem + lay.merge_o) + sel * NCW * G * D;
-        float* mm = reinterpret_cast<float*>(smem + lay.merge_ml) + sel * 2 * NCW * G;
-#pragma unroll
-        for (int off = C::LPV; off < 32; off <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[h][e] += __shfl_xor_sync(FULL, o[h][e], off);
-        if (lane < C::LPV) {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-                *reinterpret_cast<float4*>(mo + (w * G + h) * D + dl * 4) =
-                    make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        // Warps 1..NCW-1 leave their state in shared memory and move on
+        // (bar.arrive); warp 0 waits for it (bar.sync), merges it with its own
+        // registers and writes the result; before a warp overwrites the area
+        // for its next piece it waits (bar.sync) for warp 0 to have read it.
+        pol.fold(lane);
+        if (w != 0) {
+            if (!first_piece) named_sync(2);
+            pol.put(mo, mm, w, lane);
+            named_arrive(1);
+        } else {
+            named_sync(1);
+            const size_t ps = (size_t)blockIdx.x * 2 + ((u == start) ? 0 : 1);
+            PieceOut po;
+            po.complete = seg_start >= start && seg_start + nb <= end;
+            po.out = obase + head0 * D;
+            po.part_o = p.part_o + ps * G * D;
+            po.part_lse = p.part_lse + ps * G;
+            pol.merge_store(mo, mm, lane, po);
+            named_arrive(2);
         }
-        if (lane < G) {
-            mm[w * G + lane] = m_run;
-            mm[NCW * G + w * G + lane] = l_run;
-        }
-        consumer_barrier();
-        const bool complete = seg_start >= start && seg_start + nb <= end;
-        const int slot = (u == start) ? 0 : 1;
-        for (int idx = tid; idx < G * D; idx += NCW * 32) {
-            const int h = idx / D, d = idx % D;
-            float M = -CUDART_INF_F;
-#pragma unroll
-            for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, mm[w2 * G + h]);
-            float den = 0.f, num = 0.f;
-            if (M != -CUDART_INF_F) {
-#pragma unroll
-                for (int w2 = 0; w2 < NCW; ++w2) {
-                    const float sc = fast_exp2(mm[w2 * G + h] - M);
-                    den += sc * mm[NCW * G + w2 * G + h];
-                    num += sc * mo[(w2 * G + h) * D + d];
-                }
-            }
-            const float val = den > 0.f ? num / den : 0.f;
-            if (complete) {
-                obase[((size_t)b * p.num_q_heads + (size_t)g * G + h) * D + d] = Elt<T>::store(val);
-            } else {
-                const size_t ps = (size_t)blockIdx.x * 2 + slot;
-                p.part_o[(ps * G + h) * D + d] = val;
-                if (d == 0) p.part_lse[ps * G + h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
-            }
-        }
-        sel ^= 1;
+        first_piece = false;
         u = piece_end;
     }
+    if (w != 0 && !first_piece) named_sync(2);   // match warp 0's last arrive
 }
 
 // ---------------------------------------------------------- combine kernel --
@@ -617,10 +1010,10 @@ __global__ void __launch_bounds__(128) paged_decode_combine(const Params p) {
 }
 
 // ------------------------------------------------------------- host side --
-template <typename T, int D, int G>
+template <typename T, int D, int G, class Pol>
 cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
                          cudaStream_t stream) {
-    auto split = paged_decode_split<T, D, G>;
+    auto split = paged_decode_split<T, D, G, Pol>;
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -643,26 +1036,73 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.stages = plan.stages;
     p.num_ctas = plan.num_ctas;
     p.qscale = call.scale * 1.4426950408889634f;
-    split<<<plan.num_ctas, NTHREADS, plan.smem_bytes, stream>>>(pool.tmap_k, pool.tmap_v, p);
+    if (Pol::kSwizzled)
+        split<<<plan.num_ctas, NTHREADS, plan.smem_bytes, stream>>>(pool.tmap_k_swz, pool.tmap_v_swz, p);
+    else
+        split<<<plan.num_ctas, NTHREADS, plan.smem_bytes, stream>>>(pool.tmap_k, pool.tmap_v, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     paged_decode_combine<T, D, G><<<call.batch * pool.num_kv_heads, 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, class Pol>
 cudaError_t attrs_typed(size_t smem, int* ctas_per_sm) {
-    auto split = paged_decode_split<T, D, G>;
+    auto split = paged_decode_split<T, D, G, Pol>;
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split, NTHREADS, smem);
 }
 
+// Which compute policy runs a shape.  Tensor cores: 16-bit pools, head_dim
+// 128, groups of 4 or 8, block size 16 or 32, a pool with swizzled
+// descriptors.  CUDA cores otherwise, with the token loops unrolled for block
+// size 16 (and 8 / 32 on bf16 head_dim 128); other block sizes take the
+// generic instance.
+template <typename T, int D>
+constexpr bool kExtraBlockSizes = std::is_same<T, __nv_bfloat16>::value && D == 128;
+template <typename T, int D, int G>
+constexpr bool kTensorCores = sizeof(T) == 2 && D == 128 && (G == 4 || G == 8);
+
+inline bool use_tensor_cores(const kv_pool& pool, int G) {
+    return pool.elem_bytes == 2 && pool.head_dim == 128 && (G == 4 || G == 8) &&
+           (pool.block_size == 16 || pool.block_size == 32) && pool.has_swizzled_maps;
+}
+
+template <typename T, int D, int G, template <typename, int, int, class> class Fn, typename... A>
+cudaError_t with_policy(int bs, bool tc, A... args) {
+    if constexpr (kTensorCores<T, D, G>) {
+        if (tc && bs == 16) return Fn<T, D, G, TcPolicy<T, D, G, 16>>::run(args...);
+        if (tc && bs == 32) return Fn<T, D, G, TcPolicy<T, D, G, 32>>::run(args...);
+    }
+    if (bs == 16) return Fn<T, D, G, CorePolicy<T, D, G, 16>>::run(args...);
+    if constexpr (kExtraBlockSizes<T, D>) {
+        if (bs == 8) return Fn<T, D, G, CorePolicy<T, D, G, 8>>::run(args...);
+        if (bs == 32) return Fn<T, D, G, CorePolicy<T, D, G, 32>>::run(args...);
+    }
+    return Fn<T, D, G, CorePolicy<T, D, G, 0>>::run(args...);
+}
+
+template <typename T, int D, int G, class Pol> struct LaunchFn {
+    static cudaError_t run(const kv_pool* pool, const DecodeCall* call, const DecodePlan* plan,
+                           cudaStream_t stream) {
+        return launch_typed<T, D, G, Pol>(*pool, *call, *plan, stream);
+    }
+};
+template <typename T, int D, int G, class Pol> struct AttrsFn {
+    static cudaError_t run(size_t smem, int* ctas_per_sm) {
+        return attrs_typed<T, D, G, Pol>(smem, ctas_per_sm);
+    }
+};
+
 template <typename T>
 cudaError_t dispatch(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
                      cudaStream_t stream) {
-#define PKV_CASE(DD, GG) \
-    if (pool.head_dim == DD && plan.group == GG) return launch_typed<T, DD, GG>(pool, call, plan, stream);
+    const bool tc = use_tensor_cores(pool, plan.group);
+#define PKV_CASE(DD, GG)                                                                 \
+    if (pool.head_dim == DD && plan.group == GG)                                         \
+        return with_policy<T, DD, GG, LaunchFn>(pool.block_size, tc, &pool, &call, &plan, \
+                                                stream);
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
 #undef PKV_CASE
@@ -670,9 +1110,11 @@ cudaError_t dispatch(const kv_pool& pool, const DecodeCall& call, const DecodePl
 }
 
 template <typename T>
-cudaError_t attrs(int head_dim, int group, size_t smem, int* ctas_per_sm) {
-#define PKV_CASE(DD, GG) \
-    if (head_dim == DD && group == GG) return attrs_typed<T, DD, GG>(smem, ctas_per_sm);
+cudaError_t attrs(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm) {
+    const bool tc = use_tensor_cores(pool, group);
+#define PKV_CASE(DD, GG)                                                                        \
+    if (pool.head_dim == DD && group == GG)                                                     \
+        return with_policy<T, DD, GG, AttrsFn>(pool.block_size, tc, smem, ctas_per_sm);
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
 #undef PKV_CASE

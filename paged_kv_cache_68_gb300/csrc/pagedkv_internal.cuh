@@ -5,7 +5,21 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pagedkv.h"
+
+namespace pagedkv {
+// Launch plan of one decode: grid size, ring depth, shared memory, workspace.
+struct DecodePlan {
+    int group;
+    int stages;
+    int num_ctas;
+    size_t smem_bytes;
+    size_t ws_bytes;
+    size_t ws_prefix_off, ws_part_o_off, ws_part_lse_off;
+};
+}  // namespace pagedkv
 
 struct kv_pool {
     int num_blocks;
@@ -17,10 +31,18 @@ struct kv_pool {
     void* k;
     void* v;
     int* d_err;             // device error word (KV_DEVERR_* bits)
-    CUtensorMap tmap_k;     // 3-D {head_dim, num_kv_heads, num_blocks*block_size}
-    CUtensorMap tmap_v;
+    CUtensorMap tmap_k;     // 3-D {head_dim, num_kv_heads, num_blocks*block_size},
+    CUtensorMap tmap_v;     //   box {head_dim, 1, block_size}, no swizzle
+    CUtensorMap tmap_k_swz; // same view, box {128 bytes of dims, 1, block_size},
+    CUtensorMap tmap_v_swz; //   128-byte swizzle (16-bit pools, head_dim 128)
+    bool has_swizzled_maps;
     int device;
     int num_sms;
+    // last decode plan, keyed by (batch, num_q_heads)
+    std::mutex plan_mu;
+    int plan_batch = -1;
+    int plan_hq = -1;
+    pagedkv::DecodePlan plan;
 };
 
 namespace pagedkv {
@@ -50,19 +72,10 @@ struct DecodeCall {
     size_t workspace_bytes;
 };
 
-// Launch plan of one decode: grid size, ring depth, shared memory, workspace.
-struct DecodePlan {
-    int group;
-    int stages;
-    int num_ctas;
-    size_t smem_bytes;
-    size_t ws_bytes;
-    size_t ws_prefix_off, ws_part_o_off, ws_part_lse_off;
-};
-
-// Fill `plan` for this pool / batch / head count on the current device.
-// Returns cudaErrorNotSupported for shapes with no compiled kernel.
-cudaError_t plan_decode(const kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan);
+// Fill `plan` for this pool / batch / head count on the current device
+// (cached per pool).  Returns cudaErrorNotSupported for shapes with no
+// compiled kernel.
+cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan);
 
 cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
                           cudaStream_t stream);
@@ -71,8 +84,8 @@ cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const Dec
 cudaError_t decode_dispatch_f32(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
 cudaError_t decode_dispatch_f16(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
 cudaError_t decode_dispatch_bf16(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
-cudaError_t decode_attrs_f32(int head_dim, int group, size_t smem, int* ctas_per_sm);
-cudaError_t decode_attrs_f16(int head_dim, int group, size_t smem, int* ctas_per_sm);
-cudaError_t decode_attrs_bf16(int head_dim, int group, size_t smem, int* ctas_per_sm);
+cudaError_t decode_attrs_f32(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
+cudaError_t decode_attrs_f16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
+cudaError_t decode_attrs_bf16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
 
 }  // namespace pagedkv
