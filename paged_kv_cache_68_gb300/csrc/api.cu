@@ -3,6 +3,7 @@
 // the caller's stream and returns; see pagedkv.h for the contract.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -113,8 +114,8 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* p
     pl.smem_bytes = best_smem;
     pl.num_ctas = pool.num_sms * best_occ;
     size_t off = 0;
-    pl.ws_prefix_off = off;
-    off = align_up(off + 4ull * (batch + 1), 256);
+    pl.ws_counter_off = off;
+    off = align_up(off + 8ull * batch * pool.num_kv_heads, 256);
     pl.ws_part_o_off = off;
     off = align_up(off + 4ull * pl.num_ctas * 2 * G * D, 256);
     pl.ws_part_lse_off = off;
@@ -264,8 +265,12 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
     if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode(plan)");
     if (workspace_bytes < plan.ws_bytes) return KV_ENOWORKSPACE;
-    pagedkv::DecodeCall call{q, out, block_tables, max_blocks_per_seq, seq_lens,
-                             batch, num_q_heads, scale, workspace, workspace_bytes};
+    // a process-wide call tag for the workspace's piece counters (never 0)
+    static std::atomic<unsigned> next_epoch{1};
+    unsigned epoch = next_epoch.fetch_add(1);
+    if (epoch == 0) epoch = next_epoch.fetch_add(1);
+    pagedkv::DecodeCall call{q,     out,   block_tables, max_blocks_per_seq, seq_lens, batch,
+                             num_q_heads, scale, workspace, workspace_bytes, epoch};
     e = pagedkv::launch_decode(*pool, call, plan, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KV_OK : cuda_fail(e, "paged_attention_decode");
 }

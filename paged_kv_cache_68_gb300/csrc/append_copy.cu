@@ -19,6 +19,13 @@ __device__ __forceinline__ uint4 ldg_nc16(const void* p) {
     return r;
 }
 
+// Programmatic dependent launch (no-ops without a programmatic dependency):
+// let the next kernel start launching, and wait for the previous one.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void stg16(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
@@ -29,6 +36,8 @@ __global__ void __launch_bounds__(256) append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int64_t* __restrict__ slots, int num_tokens, uint4* __restrict__ k_pool,
     uint4* __restrict__ v_pool, long long num_rows, int row16, int* __restrict__ err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= 2 * num_tokens) return;
@@ -49,6 +58,8 @@ __global__ void __launch_bounds__(256) append_kernel(
 __global__ void __launch_bounds__(256) copy_blocks_kernel(
     const int32_t* __restrict__ pairs, int num_pairs, uint4* __restrict__ k_pool,
     uint4* __restrict__ v_pool, int num_blocks, int blk16, int* __restrict__ err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int pair = blockIdx.x >> 1;
     const bool is_v = blockIdx.x & 1;
     if (pair >= num_pairs) return;
@@ -72,6 +83,24 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(
     for (; i < blk16; i += 256) stg16(d + i, s[i]);
 }
 
+cudaLaunchConfig_t pdl_config(int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    return cfg;
+}
+
+// The launch may overlap the previous kernel of the stream (each kernel waits
+// with griddepcontrol.wait before touching memory).
+void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute& attr) {
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+}
+
 }  // namespace
 
 cudaError_t launch_append(const kv_pool& pool, const void* k_new, const void* v_new,
@@ -80,21 +109,25 @@ cudaError_t launch_append(const kv_pool& pool, const void* k_new, const void* v_
     const int row16 = pool.num_kv_heads * pool.head_dim * pool.elem_bytes / 16;
     const long long warps = 2ll * num_tokens;
     const int grid = (int)((warps * 32 + 255) / 256);
-    append_kernel<<<grid, 256, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, num_tokens,
-        static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
-        (long long)pool.num_blocks * pool.block_size, row16, pool.d_err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = pdl_config(grid, stream);
+    cudaLaunchAttribute attr;
+    pdl_attr(cfg, attr);
+    return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<const uint4*>(k_new),
+                              static_cast<const uint4*>(v_new), slots, num_tokens,
+                              static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
+                              (long long)pool.num_blocks * pool.block_size, row16, pool.d_err);
 }
 
 cudaError_t launch_copy_blocks(const kv_pool& pool, const int32_t* pairs, int num_pairs,
                                cudaStream_t stream) {
     if (num_pairs <= 0) return cudaSuccess;
     const int blk16 = pool.block_size * pool.num_kv_heads * pool.head_dim * pool.elem_bytes / 16;
-    copy_blocks_kernel<<<2 * num_pairs, 256, 0, stream>>>(
-        pairs, num_pairs, static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
-        pool.num_blocks, blk16, pool.d_err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = pdl_config(2 * num_pairs, stream);
+    cudaLaunchAttribute attr;
+    pdl_attr(cfg, attr);
+    return cudaLaunchKernelEx(&cfg, copy_blocks_kernel, pairs, num_pairs,
+                              static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
+                              pool.num_blocks, blk16, pool.d_err);
 }
 
 }  // namespace pagedkv

@@ -1,5 +1,5 @@
-// PagedAttention decode for sm_103a: a persistent, token-balanced split kernel
-// fed by TMA, and a log-sum-exp combine kernel.
+// PagedAttention decode for sm_103a: one persistent, token-balanced kernel fed
+// by TMA, with a log-sum-exp merge of the pieces cut across CTAs.
 //
 // What is computed ("Lecture 3", semidirectx.com CS349D notes, sec. 3.2; S06
 // "Implementation", llminference.xinbetween.com): for each sequence b and
@@ -8,7 +8,7 @@
 // softmaxes are merged with a running maximum and sum ("Lecture 24",
 // semidirectx.com CMU 11-868 notes, sec. 3.2 -- the FlashAttention /
 // Flash-Decoding trick); partial results of one sequence computed on
-// different CTAs are merged by log-sum-exp in the combine kernel.
+// different CTAs are merged by log-sum-exp.
 //
 // Work decomposition.  A unit is one (sequence b, KV head g, logical block j).
 // Units are ordered b-major, then g, then j, and the U units are cut into
@@ -20,7 +20,9 @@
 // whole (b, g) is finished in the CTA and written to `out`; a piece cut by a
 // range boundary is written as a partial (normalised o, log2-sum-exp) to one
 // of two workspace slots of its CTA -- slot 0 for the CTA's first piece, slot
-// 1 for its last -- and the combine kernel merges those.
+// 1 for its last -- and counted in an epoch-tagged per-(b, g) counter; the CTA
+// that completes the count merges the partials by log-sum-exp (no second
+// kernel).
 //
 // One CTA = 1 producer warp + NCW consumer warps.  The producer walks the
 // CTA's units, looks each block id up in the block table, and issues the TMA
@@ -69,7 +71,7 @@ struct Params {
     const int32_t* block_tables;
     const int32_t* seq_lens;
     int* err;
-    int* ws_prefix;        // [batch + 1]: blocks-per-sequence prefix (CTA 0 writes)
+    unsigned long long* counters;  // [batch][num_kv_heads]: (epoch << 32) | pieces done
     float* part_o;         // [num_ctas][2][G][D]
     float* part_lse;       // [num_ctas][2][G]
     int max_blocks;
@@ -81,6 +83,7 @@ struct Params {
     int stages;
     int num_ctas;
     float qscale;          // scale * log2(e)
+    unsigned epoch;        // nonzero tag of this call (stale counters read as zero)
 };
 
 // ---------------------------------------------------------------- layout ---
@@ -223,6 +226,14 @@ template <> struct Mma<__half> {
         return __half22float2(*reinterpret_cast<const __half2*>(&w));
     }
 };
+// Programmatic dependent launch: let the next kernel in the stream start its
+// launch now / wait until the previous kernel's results are visible.  Both
+// are no-ops when the launch carries no programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async() {
@@ -761,6 +772,56 @@ struct TcPolicy {
     }
 };
 
+// ------------------------------------------------- cross-CTA partial merge --
+// Pieces of one (b, g) cut across CTAs: CTA c holds its piece in slot
+// (c, 0) when the piece is its first, else (c, 1).  The piece counter is
+// tagged with the call's epoch, so a value left by an earlier call (or never
+// written) counts as zero; the CTA that completes the count resets it.
+__device__ __forceinline__ int count_piece(unsigned long long* ctr, unsigned epoch, int pieces) {
+    const unsigned long long tag = (unsigned long long)epoch << 32;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
+    while (true) {
+        next = ((old >> 32) == epoch ? old : tag) + 1;
+        const unsigned long long seen = atomicCAS(ctr, old, next);
+        if (seen == old) break;
+        old = seen;
+    }
+    const int done = (int)(next & 0xffffffffu);
+    if (done == pieces) atomicExch(ctr, tag);          // ready for a replay of this call
+    return done == pieces;
+}
+
+// One warp: out[h, d] = sum_c 2^(lse_c[h] - M) o_c[h, d] / sum_c 2^(lse_c[h] - M).
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_partials(const Params& p, int seg_start, int chunk, int c0,
+                                               int c1, T* out, int lane) {
+    const int slot0 = (seg_start == c0 * chunk) ? 0 : 1;
+#pragma unroll 1
+    for (int h = 0; h < G; ++h) {
+        float M = -CUDART_INF_F;
+        for (int c = c0; c <= c1; ++c) {
+            const size_t ps = (size_t)c * 2 + (c == c0 ? slot0 : 0);
+            M = fmaxf(M, __ldcg(p.part_lse + ps * G + h));
+        }
+        float den = 0.f, num[D / 32];
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) num[k] = 0.f;
+        if (M != -CUDART_INF_F) {
+            for (int c = c0; c <= c1; ++c) {
+                const size_t ps = (size_t)c * 2 + (c == c0 ? slot0 : 0);
+                const float wgt = fast_exp2(__ldcg(p.part_lse + ps * G + h) - M);
+                den += wgt;
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k)
+                    num[k] += wgt * __ldcg(p.part_o + (ps * G + h) * D + lane + 32 * k);
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) out[h * D + lane + 32 * k] = Elt<T>::store(num[k] * inv);
+    }
+}
+
 // ------------------------------------------------------------ split kernel --
 template <typename T, int D, int G, class Pol>
 __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
@@ -792,6 +853,8 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    pdl_launch_dependents();
+    pdl_wait();                                    // inputs of earlier kernels are visible
     {
         const int per = (B + NTHREADS - 1) / NTHREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
@@ -821,8 +884,12 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         if (tid == NTHREADS - 1) prefix[B] = woff + x;
     }
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int i = tid; i <= B; i += NTHREADS) p.ws_prefix[i] = prefix[i];
+    // sequences with no context get zeros (no unit covers them)
+    for (int b = blockIdx.x; b < B; b += gridDim.x)
+        if (prefix[b + 1] == prefix[b]) {
+            T* ob = static_cast<T*>(p.out) + (size_t)b * p.num_q_heads * D;
+            for (int i = tid; i < p.num_q_heads * D; i += NTHREADS) ob[i] = Elt<T>::store(0.f);
+        }
 
     const int U = prefix[B] * H;
     const int chunk = unit_chunk(U, p.num_ctas);
@@ -960,53 +1027,26 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
             po.part_o = p.part_o + ps * G * D;
             po.part_lse = p.part_lse + ps * G;
             pol.merge_store(mo, mm, lane, po);
+            if (!po.complete) {
+                // Count the finished pieces of (b, g); the CTA that finishes
+                // the last one merges all their partials into `out`.
+                __threadfence();
+                __syncwarp();
+                const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
+                int last = 0;
+                if (lane == 0)
+                    last = count_piece(p.counters + (size_t)b * H + g, p.epoch, c1 - c0 + 1);
+                if (__shfl_sync(FULL, last, 0)) {
+                    __threadfence();
+                    merge_partials<T, D, G>(p, seg_start, chunk, c0, c1, obase + head0 * D, lane);
+                }
+            }
             named_arrive(2);
         }
         first_piece = false;
         u = piece_end;
     }
     if (w != 0 && !first_piece) named_sync(2);   // match warp 0's last arrive
-}
-
-// ---------------------------------------------------------- combine kernel --
-// One CTA per (sequence, KV head): merge the partials of a (b, g) that was cut
-// across CTAs (weights 2^(lse_p - max)), write zeros for empty sequences, and
-// leave whole pieces (already written by the split kernel) alone.
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) paged_decode_combine(const Params p) {
-    const int H = p.num_kv_heads;
-    const int b = blockIdx.x / H, g = blockIdx.x % H;
-    const int* prefix = p.ws_prefix;
-    const int nb = prefix[b + 1] - prefix[b];
-    T* o = static_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)g * G) * D;
-    if (nb == 0) {
-        for (int idx = threadIdx.x; idx < G * D; idx += 128) o[idx] = Elt<T>::store(0.f);
-        return;
-    }
-    const int U = prefix[p.batch] * H;
-    const int chunk = unit_chunk(U, p.num_ctas);
-    const int S0 = prefix[b] * H + g * nb;
-    const int c0 = S0 / chunk, c1 = (S0 + nb - 1) / chunk;
-    if (c0 == c1) return;
-    const int slot0 = (S0 == c0 * chunk) ? 0 : 1;
-    for (int idx = threadIdx.x; idx < G * D; idx += 128) {
-        const int h = idx / D, d = idx % D;
-        float M = -CUDART_INF_F;
-        for (int c = c0; c <= c1; ++c) {
-            const size_t ps = (size_t)c * 2 + (c == c0 ? slot0 : 0);
-            M = fmaxf(M, p.part_lse[ps * G + h]);
-        }
-        float den = 0.f, num = 0.f;
-        if (M != -CUDART_INF_F) {
-            for (int c = c0; c <= c1; ++c) {
-                const size_t ps = (size_t)c * 2 + (c == c0 ? slot0 : 0);
-                const float wgt = fast_exp2(p.part_lse[ps * G + h] - M);
-                den += wgt;
-                num += wgt * p.part_o[(ps * G + h) * D + d];
-            }
-        }
-        o[idx] = Elt<T>::store(den > 0.f ? num / den : 0.f);
-    }
 }
 
 // ------------------------------------------------------------- host side --
@@ -1024,7 +1064,7 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.seq_lens = call.seq_lens;
     p.err = pool.d_err;
     unsigned char* ws = static_cast<unsigned char*>(call.workspace);
-    p.ws_prefix = reinterpret_cast<int*>(ws + plan.ws_prefix_off);
+    p.counters = reinterpret_cast<unsigned long long*>(ws + plan.ws_counter_off);
     p.part_o = reinterpret_cast<float*>(ws + plan.ws_part_o_off);
     p.part_lse = reinterpret_cast<float*>(ws + plan.ws_part_lse_off);
     p.max_blocks = call.max_blocks;
@@ -1036,14 +1076,20 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.stages = plan.stages;
     p.num_ctas = plan.num_ctas;
     p.qscale = call.scale * 1.4426950408889634f;
+    p.epoch = call.epoch;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.num_ctas);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (Pol::kSwizzled)
-        split<<<plan.num_ctas, NTHREADS, plan.smem_bytes, stream>>>(pool.tmap_k_swz, pool.tmap_v_swz, p);
-    else
-        split<<<plan.num_ctas, NTHREADS, plan.smem_bytes, stream>>>(pool.tmap_k, pool.tmap_v, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    paged_decode_combine<T, D, G><<<call.batch * pool.num_kv_heads, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, split, pool.tmap_k_swz, pool.tmap_v_swz, p);
+    return cudaLaunchKernelEx(&cfg, split, pool.tmap_k, pool.tmap_v, p);
 }
 
 template <typename T, int D, int G, class Pol>

@@ -17,7 +17,7 @@ struct DecodePlan {
     int num_ctas;
     size_t smem_bytes;
     size_t ws_bytes;
-    size_t ws_prefix_off, ws_part_o_off, ws_part_lse_off;
+    size_t ws_counter_off, ws_part_o_off, ws_part_lse_off;
 };
 }  // namespace pagedkv
 
@@ -70,6 +70,7 @@ struct DecodeCall {
     float scale;
     void* workspace;
     size_t workspace_bytes;
+    unsigned epoch;        // nonzero, distinct for consecutive calls
 };
 
 // Fill `plan` for this pool / batch / head count on the current device
