@@ -83,8 +83,9 @@ typedef struct kv_pool* kv_pool_t;
  * Limits: 1 <= block_size <= 256; head_dim in {64, 128}; num_kv_heads >= 1;
  *   num_blocks >= 1 and num_blocks * block_size < 2^31.
  * On success *out receives a handle.  The handle owns no pool memory: it holds
- *   the geometry, two TMA descriptors built from k_pool / v_pool, and a 4-byte
- *   device error word that this call allocates (freed by kv_pool_destroy).
+ *   the geometry, the TMA descriptors built from k_pool / v_pool (plain, and
+ *   128-byte-swizzled for 16-bit head_dim-128 pools), and a 4-byte device
+ *   error word that this call allocates (freed by kv_pool_destroy).
  * Errors: KV_EINVAL (null or misaligned pointer, size out of range),
  *   KV_EUNSUPPORTED (head_dim, dtype), KV_ECUDA.
  */
@@ -139,7 +140,8 @@ kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_he
  *     s_t = scale * dot(q[b,h,:], K[block_tables[b, t / bs], t % bs, g, :])
  *     out[b,h,:] = sum_t softmax(s)_t * V[block_tables[b, t / bs], t % bs, g, :]
  * over t = 0 .. L-1.  L = 0 gives zeros.  Only table entries
- * 0 .. ceil(L / bs) - 1 and only the first L rows are read.
+ * 0 .. ceil(L / bs) - 1 are read; the last block is loaded whole, but only its
+ * rows below L contribute (the rest may hold anything, NaN included).
  *
  * q, out: device [batch, num_q_heads, head_dim] of the pool dtype.
  * block_tables: device int32 [batch, max_blocks_per_seq] (row-major).
@@ -150,8 +152,10 @@ kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_he
  * num_kv_heads must equal the pool's; num_q_heads / num_kv_heads in {1,2,4,8};
  *   1 <= batch <= 4096.
  * workspace: device scratch of at least paged_attention_workspace_size bytes,
- *   16-byte aligned, owned by the caller; it holds no state between calls.
- *   Calls that use the same workspace must not overlap in time.
+ *   16-byte aligned, owned by the caller.  Its contents need no initialisation
+ *   and carry nothing the caller must manage between calls (it holds per-call
+ *   partial results and self-resetting piece counters tagged with a call
+ *   number).  Calls that use the same workspace must not overlap in time.
  * Errors: KV_EINVAL, KV_EUNSUPPORTED, KV_ENOWORKSPACE, KV_ECUDA.
  */
 kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
