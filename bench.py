@@ -68,10 +68,15 @@ def parse_args(argv=None):
     ap.add_argument("--placement", choices=["random", "identity"], default="random")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (profiling a smaller case)")
+    ap.add_argument("--block-size", type=int, default=None,
+                    help="block size of the long-context workload (8, 16 or 32)")
+    ap.add_argument("--prompt-len", type=int, default=None,
+                    help="prompt length of the shared-prefix workload (2000 or 2008)")
     return ap.parse_args(argv)
 
 
-def make_workload(name: str, seed: int, device, placement: str = "random", batch=None):
+def make_workload(name: str, seed: int, device, placement: str = "random", batch=None,
+                  block_size=None, prompt_len=None):
     from paged_kv_cache_68_gb300 import workloads as wl
     kw = {} if batch is None else {"batch": batch}
     if name == "llama3_8b_gqa":
@@ -79,8 +84,14 @@ def make_workload(name: str, seed: int, device, placement: str = "random", batch
     if name == "opt13b_mha":
         return wl.opt13b_mha(seed, device=device, **kw)
     if name == "shared_prefix":
-        return wl.shared_prefix(seed, device=device, **({} if batch is None else {"prompts": batch}))
+        if batch is not None:
+            kw = {"prompts": batch}
+        if prompt_len is not None:
+            kw["prompt_len"] = prompt_len
+        return wl.shared_prefix(seed, device=device, **kw)
     if name == "long_context":
+        if block_size is not None:
+            kw["block_size"] = block_size
         return wl.long_context(seed, device=device, **kw)
     raise ValueError(name)
 
@@ -197,6 +208,18 @@ def reduce_max_sum(local_ms: float, local_units: float):
     return float(t.item()), float(u.item())
 
 
+def unique_bytes_fields(w, world, dec_ms):
+    """Shared-prefix steps: decode GB/s against the K/V bytes stored once (the
+    prefix counted once per prompt) beside the logical bytes."""
+    if "unique_tokens" not in w.info:
+        return {}
+    row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2
+    ub = int(w.info["unique_tokens"]) * row
+    return {"unique_kv_bytes_per_replica": ub,
+            "attention_gbs_unique": round(ub * world / (dec_ms * 1e-3) / 1e9, 2),
+            "cow_pairs_per_step": int(w.pairs.shape[0])}
+
+
 # ----------------------------------------------------------- CPU baseline --
 
 def oracle_sample_step(host_w, seqs, threads):
@@ -244,7 +267,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pagedkv.load()
-    w = make_workload(args.workload, args.seed, dev, args.placement, args.batch)
+    w = make_workload(args.workload, args.seed, dev, args.placement, args.batch,
+                      args.block_size, args.prompt_len)
     tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
     k_pool, v_pool = w.k_pool, w.v_pool
     # the step's inputs live back to back in one device buffer (256-byte
@@ -359,13 +383,16 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(max_step_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload]
-                   + ("" if args.batch is None else f" (batch overridden to {args.batch})"),
+                   + ("" if args.batch is None else f" (batch overridden to {args.batch})")
+                   + ("" if args.block_size is None else f" (block_size {args.block_size})")
+                   + ("" if args.prompt_len is None else f" (prompt_len {args.prompt_len})"),
                    "seed": args.seed, "placement": args.placement, "global_batch": w.batch * world,
                    "tokens_per_replica": int(w.seq_lens.sum()),
                    "kv_bytes_per_replica": w.kv_bytes(), "step_bytes_per_replica": step_bytes,
                    "l2": "flushed (512 MB write) between timed steps; KV 1.7 GB > 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "seq_steps_per_s": round(total_seqs / (max_step_ms * 1e-3), 1),
+        **unique_bytes_fields(w, world, max_dec_ms),
         "attention_gbs": round(att_bytes * world / (max_dec_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm",
                      "kernel": "paged_decode_split (the whole decode call: one kernel, merges included)",
@@ -393,7 +420,8 @@ def run_reference(args):
     from paged_kv_cache_68_gb300 import workloads as wl
     c_oracle.build()
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
-    w = wl.on_host(make_workload(args.workload, args.seed, dev, args.placement, args.batch))
+    w = wl.on_host(make_workload(args.workload, args.seed, dev, args.placement, args.batch,
+                                 args.block_size, args.prompt_len))
     threads = os.cpu_count() or 1
     per_step = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     seqs = pick_sample(w, per_step, threads)
