@@ -72,6 +72,8 @@ def parse_args(argv=None):
                     help="block size of the long-context workload (8, 16 or 32)")
     ap.add_argument("--prompt-len", type=int, default=None,
                     help="prompt length of the shared-prefix workload (2000 or 2008)")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix workload: decode with the cascade entry point")
     return ap.parse_args(argv)
 
 
@@ -293,15 +295,31 @@ def run_ours(args):
     host_in = dev_in.cpu().pin_memory()
     pool = pagedkv.KVPool(k_pool, v_pool)
     out = torch.empty_like(q)
-    ws = pool.workspace(w.batch, w.num_q_heads)
+    cascade = args.cascade and w.groups is not None
+    if cascade:
+        groups = torch.from_numpy(np.ascontiguousarray(w.groups)).to(dev)
+        gcols = [groups[:, i].contiguous() for i in range(3)]
+        ws = torch.empty(pagedkv.paged_attention_cascade_workspace_size(
+            pool.handle, w.batch, w.num_q_heads, int(groups.shape[0])), dtype=torch.uint8, device=dev)
+    else:
+        ws = pool.workspace(w.batch, w.num_q_heads)
+
+    def decode():
+        if cascade:
+            pagedkv.paged_attention_decode_cascade(pool.handle, q, out, tables, lens, w.scale,
+                                                   w.num_kv_heads, gcols[0], gcols[1], gcols[2],
+                                                   ws, pool.dtype)
+        else:
+            pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     n_pairs = int(w.pairs.shape[0])
-    launches_per_step = (1 if n_pairs else 0) + 1 + 1     # copy (if pairs), append, decode
+    # copy (if pairs), append, decode (two kernels for a cascade decode)
+    launches_per_step = (1 if n_pairs else 0) + 1 + (2 if cascade else 1)
 
     def step():
         pool.copy_blocks(pairs)
         pool.append(k_new, v_new, slots)
-        pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
+        decode()
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -321,7 +339,7 @@ def run_ours(args):
         pool.copy_blocks(pairs)
         pool.append(k_new, v_new, slots)
         e[1].record()
-        pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
+        decode()
         e[2].record()
         e[3].record()
     torch.cuda.synchronize()
@@ -360,7 +378,13 @@ def run_ours(args):
     total_seqs = w.batch * world
     value = total_bytes / (max_step_ms * 1e-3) / 1e9
     peak, peak_kind = measured_hbm_peak()
-    achieved = att_bytes / (dec_ms * 1e-3) / 1e9
+    # A cascade decode reads each shared block once per group: its algorithmic
+    # bytes count the stored (unique) K/V, not the logical per-sequence K/V.
+    roof_bytes = att_bytes
+    if cascade and "unique_tokens" in w.info:
+        row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2
+        roof_bytes = att_bytes - w.kv_bytes() + int(w.info["unique_tokens"]) * row
+    achieved = roof_bytes / (dec_ms * 1e-3) / 1e9
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -395,10 +419,13 @@ def run_ours(args):
         **unique_bytes_fields(w, world, max_dec_ms),
         "attention_gbs": round(att_bytes * world / (max_dec_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm",
-                     "kernel": "paged_decode_split (the whole decode call: one kernel, merges included)",
+                     "kernel": ("paged_decode_prefix + paged_decode_split (the whole cascade decode call)"
+                                if cascade else
+                                "paged_decode_split (the whole decode call: one kernel, merges included)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": profiled_traffic(), "algorithmic_bytes": att_bytes},
+                     "traffic": None if cascade else profiled_traffic(),
+                     "algorithmic_bytes": roof_bytes},
         "e2e": {"value": round(total_bytes / (max_e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(max_e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

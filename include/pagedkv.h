@@ -72,6 +72,8 @@ typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype;
 #define KV_DEVERR_PAIR_RANGE   0x4  /* copy_blocks: src or dst outside the pool     */
 #define KV_DEVERR_SEQ_RANGE    0x8  /* decode: seq_len > max_blocks_per_seq*bs      */
 #define KV_DEVERR_TIMEOUT      0x10 /* a pipeline wait gave up (work was skipped)    */
+#define KV_DEVERR_GROUP_RANGE  0x20 /* cascade: a group outside the batch, overlapping
+                                       or out of order (its sharing is ignored)       */
 
 typedef struct kv_pool* kv_pool_t;
 
@@ -163,6 +165,48 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
                                  const int32_t* seq_lens, int batch, int num_q_heads,
                                  float scale, int num_kv_heads, void* workspace,
                                  size_t workspace_bytes, void* stream);
+
+/*
+ * paged_attention_cascade_workspace_size -- bytes of workspace that
+ * paged_attention_decode_cascade needs (>= paged_attention_workspace_size).
+ */
+kv_status paged_attention_cascade_workspace_size(kv_pool_t pool, int batch, int num_q_heads,
+                                                 int num_groups, size_t* bytes);
+
+/*
+ * paged_attention_decode_cascade -- paged_attention_decode for batches whose
+ * sequences share prefix blocks ("Lecture 3", sec. 4.1: parallel samples and
+ * beams point their tables at the same physical blocks; S06 "In production":
+ * the cascade path batches the shared prefix apart from the diverging
+ * suffixes).  The result is that of paged_attention_decode on the same
+ * arguments (up to fp32 rounding); the grouping only lets each shared block be
+ * read once per group instead of once per sequence.
+ *
+ * group_first, group_size, group_shared_blocks: device int32 [num_groups].
+ *   Group k is sequences group_first[k] .. group_first[k] + group_size[k] - 1;
+ *   its members' tables hold the same physical block ids in their first
+ *   group_shared_blocks[k] entries.  Groups are disjoint and sorted by their
+ *   first member; sequences outside every group are decoded plainly.
+ *   Preconditions the kernel cannot check: the shared entries are identical
+ *   across members (otherwise the first member's blocks are used for all).
+ *   A group outside the batch, overlapping its predecessor or out of order is
+ *   ignored (its members are decoded plainly) and sets KV_DEVERR_GROUP_RANGE;
+ *   the shared-block count is clamped to every member's own block count.
+ * num_groups <= 1024.  Pools that are not 16-bit head_dim-128, query/KV head
+ *   ratios other than 4 and 8, block sizes other than 16 and 32, and
+ *   num_groups = 0 are decoded by paged_attention_decode (same result).
+ * workspace: at least paged_attention_cascade_workspace_size bytes.
+ * Two kernels are enqueued (the shared-prefix pass, then the per-sequence
+ * pass); the other arguments, errors and device error bits are those of
+ * paged_attention_decode.
+ */
+kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* out,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* seq_lens, int batch, int num_q_heads,
+                                         float scale, int num_kv_heads, const int32_t* group_first,
+                                         const int32_t* group_size,
+                                         const int32_t* group_shared_blocks, int num_groups,
+                                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * paged_attention_decode_noalloc -- paged_attention_decode without a

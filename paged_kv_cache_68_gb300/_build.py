@@ -52,7 +52,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     nvcc = _nvcc()
     obj_dir = os.path.join(LIB_DIR, "obj")
     os.makedirs(obj_dir, exist_ok=True)
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC",
                     "-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
     if verbose:
         flags += ["-Xptxas", "-v"]

@@ -148,6 +148,17 @@ class BlockManager:
     def table(self, seq_id: int) -> List[int]:
         return list(self.tables[seq_id])
 
+    def shared_prefix_blocks(self, seq_ids) -> int:
+        """Leading table entries that every sequence of ``seq_ids`` holds in
+        common (the same physical block ids), counting only blocks whose
+        reference count covers them all."""
+        tables = [self.tables[s] for s in seq_ids]
+        n = 0
+        while all(len(t) > n for t in tables) and len({t[n] for t in tables}) == 1 \
+                and self.ref[tables[0][n]] >= len(tables):
+            n += 1
+        return n
+
     def check_invariant(self) -> None:
         """Tables holding each block == its reference count; free <=> count 0."""
         holders = Counter(blk for t in self.tables.values() for blk in t)

@@ -16,12 +16,6 @@ namespace {
 
 thread_local char g_last_cuda_error[256] = "";
 
-kv_status cuda_fail(cudaError_t e, const char* where) {
-    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where,
-                  cudaGetErrorString(e));
-    return KV_ECUDA;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int elem_bytes(kv_dtype d) { return d == KV_F32 ? 4 : 2; }
@@ -70,10 +64,18 @@ constexpr size_t kMaxSmem = 227 * 1024;
 
 namespace pagedkv {
 
-cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan) {
+kv_status cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where,
+                  cudaGetErrorString(e));
+    return KV_ECUDA;
+}
+
+cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_groups,
+                        DecodePlan* plan) {
     {
         std::lock_guard<std::mutex> lock(pool.plan_mu);
-        if (pool.plan_batch == batch && pool.plan_hq == num_q_heads) {
+        if (pool.plan_batch == batch && pool.plan_hq == num_q_heads &&
+            pool.plan_groups == num_groups) {
             *plan = pool.plan;
             return cudaSuccess;
         }
@@ -90,7 +92,7 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* p
     for (int S = ncw; S <= 8 * ncw; S += ncw) {
         if (S > ncw && (size_t)S * stage > kMaxRingBytes) break;
         // + 1 KB: the kernel rounds its shared-memory base up to 1 KB
-        const size_t smem = dec::Layout(S, batch, bs, G, D, elt).total + 1024;
+        const size_t smem = dec::Layout(S, batch, bs, G, D, elt, num_groups).total + 1024;
         if (smem > kMaxSmem) break;
         int occ = 0;
         cudaError_t e = cudaErrorNotSupported;
@@ -126,6 +128,7 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* p
         pool.plan = pl;
         pool.plan_batch = batch;
         pool.plan_hq = num_q_heads;
+        pool.plan_groups = num_groups;
     }
     *plan = pl;
     return cudaSuccess;
@@ -174,7 +177,7 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
     if (e != cudaSuccess) {
         if (p->d_err) cudaFree(p->d_err);
         delete p;
-        return cuda_fail(e, "kv_pool_create");
+        return pagedkv::cuda_fail(e, "kv_pool_create");
     }
     p->has_swizzled_maps = p->elem_bytes == 2 && head_dim == 128 && block_size <= 256;
     bool maps_ok = encode_pool_map(&p->tmap_k, k_pool, *p, false) &&
@@ -197,7 +200,7 @@ kv_status kv_pool_destroy(kv_pool_t pool) {
     if (!pool) return KV_OK;
     cudaError_t e = cudaFree(pool->d_err);
     delete pool;
-    return e == cudaSuccess ? KV_OK : cuda_fail(e, "kv_pool_destroy");
+    return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "kv_pool_destroy");
 }
 
 kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
@@ -209,7 +212,7 @@ kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
         return KV_EINVAL;
     cudaError_t e = pagedkv::launch_append(*pool, k_new, v_new, slot_mapping, num_tokens,
                                            static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? KV_OK : cuda_fail(e, "kv_append");
+    return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "kv_append");
 }
 
 kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void* stream) {
@@ -218,7 +221,7 @@ kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void*
     if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 7u)) return KV_EINVAL;
     cudaError_t e = pagedkv::launch_copy_blocks(*pool, pairs, num_pairs,
                                                 static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? KV_OK : cuda_fail(e, "copy_blocks");
+    return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "copy_blocks");
 }
 
 static kv_status check_decode_shape(kv_pool_t pool, int batch, int num_q_heads) {
@@ -236,18 +239,20 @@ kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_he
     kv_status st = check_decode_shape(pool, batch, num_q_heads);
     if (st != KV_OK) return st;
     pagedkv::DecodePlan plan;
-    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, &plan);
+    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, 0, &plan);
     if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
-    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_workspace_size");
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_workspace_size");
     *bytes = plan.ws_bytes;
     return KV_OK;
 }
 
-kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
-                                 const int32_t* block_tables, int max_blocks_per_seq,
-                                 const int32_t* seq_lens, int batch, int num_q_heads, float scale,
-                                 int num_kv_heads, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
+static kv_status decode_impl(kv_pool_t pool, const void* q, void* out,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                             int num_kv_heads, void* workspace, size_t workspace_bytes,
+                             const int32_t* g_first, const int32_t* g_size,
+                             const int32_t* g_blocks, int num_groups, const float* pst_o,
+                             const float* pst_lse, void* stream) {
     kv_status st = check_decode_shape(pool, batch, num_q_heads);
     if (st != KV_OK) return st;
     if (num_kv_heads != pool->num_kv_heads) return KV_EINVAL;
@@ -261,9 +266,9 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
         return KV_EUNSUPPORTED;
     if (!(scale == scale)) return KV_EINVAL;
     pagedkv::DecodePlan plan;
-    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, &plan);
+    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, num_groups, &plan);
     if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
-    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode(plan)");
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode(plan)");
     if (workspace_bytes < plan.ws_bytes) return KV_ENOWORKSPACE;
     // a process-wide call tag for the workspace's piece counters (never 0)
     static std::atomic<unsigned> next_epoch{1};
@@ -271,8 +276,24 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
     if (epoch == 0) epoch = next_epoch.fetch_add(1);
     pagedkv::DecodeCall call{q,     out,   block_tables, max_blocks_per_seq, seq_lens, batch,
                              num_q_heads, scale, workspace, workspace_bytes, epoch};
+    call.g_first = g_first;
+    call.g_size = g_size;
+    call.g_blocks = g_blocks;
+    call.num_groups = num_groups;
+    call.pst_o = pst_o;
+    call.pst_lse = pst_lse;
     e = pagedkv::launch_decode(*pool, call, plan, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? KV_OK : cuda_fail(e, "paged_attention_decode");
+    return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "paged_attention_decode");
+}
+
+kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                                 int num_kv_heads, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    return decode_impl(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                       num_q_heads, scale, num_kv_heads, workspace, workspace_bytes, nullptr,
+                       nullptr, nullptr, 0, nullptr, nullptr, stream);
 }
 
 kv_status kv_pool_get_error(kv_pool_t pool, int* device_error_bits) {
@@ -280,7 +301,7 @@ kv_status kv_pool_get_error(kv_pool_t pool, int* device_error_bits) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess)
         e = cudaMemcpy(device_error_bits, pool->d_err, sizeof(int), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "kv_pool_get_error");
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "kv_pool_get_error");
     return *device_error_bits ? KV_ERANGE : KV_OK;
 }
 
@@ -289,7 +310,7 @@ kv_status kv_pool_clear_error(kv_pool_t pool) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemset(pool->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    return e == cudaSuccess ? KV_OK : cuda_fail(e, "kv_pool_clear_error");
+    return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "kv_pool_clear_error");
 }
 
 const char* kv_strerror(kv_status status) {
@@ -307,3 +328,18 @@ const char* kv_strerror(kv_status status) {
 const char* kv_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"
+
+namespace pagedkv {
+
+kv_status decode_after_prefix(kv_pool* pool, const void* q, void* out, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                              int num_q_heads, float scale, void* workspace,
+                              size_t plain_ws_bytes, const int32_t* g_first, const int32_t* g_size,
+                              const int32_t* g_blocks, int num_groups, const float* pst_o,
+                              const float* pst_lse, cudaStream_t stream) {
+    return decode_impl(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                       num_q_heads, scale, pool->num_kv_heads, workspace, plain_ws_bytes, g_first,
+                       g_size, g_blocks, num_groups, pst_o, pst_lse, stream);
+}
+
+}  // namespace pagedkv

@@ -1,0 +1,223 @@
+// Cascade (shared-prefix) decode: planning, launch and the C-ABI entry points.
+//
+// Two launches on the caller's stream: the shared-prefix pass
+// (paged_decode_prefix) leaves per-(sequence, head) prefix states in the
+// workspace, then the split kernel attends each sequence's remaining blocks
+// and folds the prefix state into its log-sum-exp merge.  Shapes without a
+// prefix kernel (fp32 pools, head_dim 64, groups of 1 or 2, block sizes other
+// than 16 and 32) and calls with no groups run the plain decode, which gives
+// the same result.
+#include <atomic>
+#include <cstdio>
+#include <mutex>
+
+#include "decode_prefix.cuh"
+#include "pagedkv_internal.cuh"
+
+namespace pagedkv {
+namespace {
+
+constexpr size_t kMaxSmemP = 227 * 1024;
+constexpr size_t kMaxRingBytesP = 128 * 1024;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct PrefixPlan {
+    int stages;
+    int num_ctas;
+    size_t smem_bytes;
+    // workspace, after the plain decode's part
+    size_t off_pst_o, off_pst_lse, off_ctr, off_part_o, off_part_lse, end;
+};
+
+bool cascade_shape(const kv_pool& pool, int group) {
+    return pool.elem_bytes == 2 && pool.head_dim == 128 && (group == 4 || group == 8) &&
+           (pool.block_size == 16 || pool.block_size == 32) && pool.has_swizzled_maps;
+}
+
+template <typename T, int G, int BSC>
+cudaError_t prefix_attrs(size_t smem, int* occ) {
+    auto k = dec::paged_decode_prefix<T, 128, G, BSC>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, dec::NTHREADS, smem);
+}
+
+template <typename T, int G, int BSC>
+cudaError_t prefix_launch(const kv_pool& pool, const dec::PParams& p, size_t smem, int grid,
+                          cudaStream_t stream) {
+    auto k = dec::paged_decode_prefix<T, 128, G, BSC>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(dec::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, pool.tmap_k_swz, pool.tmap_v_swz, p);
+}
+
+// Dispatch on (dtype, group, block size) for one of the two functions above.
+template <class F>
+cudaError_t by_shape(const kv_pool& pool, int group, F&& f) {
+    const bool bf = pool.dtype == KV_BF16;
+    const int bs = pool.block_size;
+#define PKV_P(TT, GG, BB) \
+    if (group == GG && bs == BB) return f.template operator()<TT, GG, BB>();
+    if (bf) { PKV_P(__nv_bfloat16, 4, 16) PKV_P(__nv_bfloat16, 4, 32) PKV_P(__nv_bfloat16, 8, 16) PKV_P(__nv_bfloat16, 8, 32) }
+    else    { PKV_P(__half, 4, 16) PKV_P(__half, 4, 32) PKV_P(__half, 8, 16) PKV_P(__half, 8, 32) }
+#undef PKV_P
+    return cudaErrorNotSupported;
+}
+
+cudaError_t plan_prefix(const kv_pool& pool, int batch, int num_q_heads, int num_groups,
+                        size_t base, PrefixPlan* pp) {
+    const int G = num_q_heads / pool.num_kv_heads;
+    const int bs = pool.block_size, D = pool.head_dim, elt = pool.elem_bytes;
+    const size_t stage = 2ull * bs * D * elt;
+    int best_s = 0, best_occ = 0, best_score = -1;
+    size_t best_smem = 0;
+    for (int S = dec::NCW; S <= 8 * dec::NCW; S += dec::NCW) {
+        if (S > dec::NCW && (size_t)S * stage > kMaxRingBytesP) break;
+        const size_t smem = dec::PLayout(S, num_groups, bs, D, elt).total + 1024;
+        if (smem > kMaxSmemP) break;
+        int occ = 0;
+        cudaError_t e = by_shape(pool, G, [&]<typename T, int GG, int BB>() {
+            return prefix_attrs<T, GG, BB>(smem, &occ);
+        });
+        if (e != cudaSuccess) return e;
+        const int per_warp = S / dec::NCW > 2 ? 2 : S / dec::NCW;
+        if (occ >= 1 && occ * per_warp >= best_score) {
+            best_s = S;
+            best_occ = occ;
+            best_score = occ * per_warp;
+            best_smem = smem;
+        }
+    }
+    if (best_s == 0) return cudaErrorNotSupported;
+    pp->stages = best_s;
+    pp->smem_bytes = best_smem;
+    pp->num_ctas = pool.num_sms * best_occ;
+    size_t off = align_up(base, 256);
+    pp->off_pst_o = off;     off = align_up(off + 4ull * batch * num_q_heads * D, 256);
+    pp->off_pst_lse = off;   off = align_up(off + 4ull * batch * num_q_heads, 256);
+    pp->off_ctr = off;       off = align_up(off + 8ull * batch * pool.num_kv_heads, 256);
+    pp->off_part_o = off;    off = align_up(off + 4ull * pp->num_ctas * 2 * dec::kRows * D, 256);
+    pp->off_part_lse = off;  off = align_up(off + 4ull * pp->num_ctas * 2 * dec::kRows, 256);
+    pp->end = off;
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+extern "C" {
+
+kv_status paged_attention_cascade_workspace_size(kv_pool_t pool, int batch, int num_q_heads,
+                                                 int num_groups, size_t* bytes) {
+    if (!bytes || num_groups < 0 || num_groups > pagedkv::kMaxGroups) return KV_EINVAL;
+    size_t plain = 0;
+    kv_status st = paged_attention_workspace_size(pool, batch, num_q_heads, &plain);
+    if (st != KV_OK) return st;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if (num_groups == 0 || !pagedkv::cascade_shape(*pool, G)) {
+        *bytes = plain;
+        return KV_OK;
+    }
+    pagedkv::PrefixPlan pp;
+    cudaError_t e = pagedkv::plan_prefix(*pool, batch, num_q_heads, num_groups, plain, &pp);
+    if (e == cudaErrorNotSupported) {
+        *bytes = plain;
+        return KV_OK;
+    }
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_cascade_workspace_size");
+    *bytes = pp.end;
+    return KV_OK;
+}
+
+kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* out,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* seq_lens, int batch, int num_q_heads,
+                                         float scale, int num_kv_heads, const int32_t* group_first,
+                                         const int32_t* group_size,
+                                         const int32_t* group_shared_blocks, int num_groups,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_groups < 0 || num_groups > pagedkv::kMaxGroups) return KV_EINVAL;
+    if (num_groups > 0 && (!group_first || !group_size || !group_shared_blocks ||
+                           (reinterpret_cast<uintptr_t>(group_first) & 3u) ||
+                           (reinterpret_cast<uintptr_t>(group_size) & 3u) ||
+                           (reinterpret_cast<uintptr_t>(group_shared_blocks) & 3u)))
+        return KV_EINVAL;
+    if (!pool || num_kv_heads != pool->num_kv_heads || num_q_heads < 1 ||
+        num_q_heads % num_kv_heads)
+        return KV_EINVAL;
+    const int G = num_q_heads / num_kv_heads;
+    if (num_groups == 0 || !pagedkv::cascade_shape(*pool, G))
+        return paged_attention_decode(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
+                                      batch, num_q_heads, scale, num_kv_heads, workspace,
+                                      workspace_bytes, stream);
+    size_t plain = 0;
+    kv_status st = paged_attention_workspace_size(pool, batch, num_q_heads, &plain);
+    if (st != KV_OK) return st;
+    pagedkv::PrefixPlan pp;
+    cudaError_t e = pagedkv::plan_prefix(*pool, batch, num_q_heads, num_groups, plain, &pp);
+    if (e == cudaErrorNotSupported)
+        return paged_attention_decode(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
+                                      batch, num_q_heads, scale, num_kv_heads, workspace,
+                                      workspace_bytes, stream);
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_cascade(plan)");
+    if (!workspace || workspace_bytes < pp.end) return KV_ENOWORKSPACE;
+    // the plain decode checks the remaining arguments before anything is enqueued
+    if (!q || !out || !block_tables || !seq_lens) return KV_EINVAL;
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    static std::atomic<unsigned> next_epoch{1u << 31};
+    unsigned epoch = next_epoch.fetch_add(1);
+    if (epoch == 0) epoch = next_epoch.fetch_add(1);
+    pagedkv::dec::PParams p;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.g_first = group_first;
+    p.g_size = group_size;
+    p.g_blocks = group_shared_blocks;
+    p.err = pool->d_err;
+    p.pst_o = reinterpret_cast<float*>(ws + pp.off_pst_o);
+    p.pst_lse = reinterpret_cast<float*>(ws + pp.off_pst_lse);
+    p.counters = reinterpret_cast<unsigned long long*>(ws + pp.off_ctr);
+    p.part_o = reinterpret_cast<float*>(ws + pp.off_part_o);
+    p.part_lse = reinterpret_cast<float*>(ws + pp.off_part_lse);
+    p.num_groups = num_groups;
+    p.max_blocks = max_blocks_per_seq;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = pool->num_blocks;
+    p.bs = pool->block_size;
+    p.stages = pp.stages;
+    p.num_ctas = pp.num_ctas;
+    p.qscale = scale * 1.4426950408889634f;
+    p.epoch = epoch;
+    // argument checks of the second pass first, so nothing is enqueued on error
+    if (batch < 1 || batch > pagedkv::kMaxBatch || max_blocks_per_seq < 1 ||
+        (long long)batch * max_blocks_per_seq * num_kv_heads >= (1ll << 31) ||
+        (reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15u) || !(scale == scale))
+        return KV_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = pagedkv::by_shape(*pool, G, [&]<typename T, int GG, int BB>() {
+        return pagedkv::prefix_launch<T, GG, BB>(*pool, p, pp.smem_bytes, pp.num_ctas, s);
+    });
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_cascade(prefix)");
+    return pagedkv::decode_after_prefix(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
+                                        batch, num_q_heads, scale, workspace, plain,
+                                        group_first, group_size, group_shared_blocks, num_groups,
+                                        p.pst_o, p.pst_lse, s);
+}
+
+}  // extern "C"

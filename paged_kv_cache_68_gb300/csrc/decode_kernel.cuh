@@ -84,20 +84,33 @@ struct Params {
     int num_ctas;
     float qscale;          // scale * log2(e)
     unsigned epoch;        // nonzero tag of this call (stale counters read as zero)
+    // Cascade decode (num_groups > 0): the groups of sequences sharing leading
+    // blocks, and the shared-prefix pass's states for their members; this pass
+    // then covers only each member's remaining blocks.
+    const int32_t* g_first;
+    const int32_t* g_size;
+    const int32_t* g_blocks;
+    int num_groups;
+    const float* pst_o;    // [batch][num_q_heads][D], normalised
+    const float* pst_lse;  // [batch][num_q_heads], log2-sum-exp
 };
 
 // ---------------------------------------------------------------- layout ---
 struct Layout {
-    uint32_t full, empty, valid, misc, prefix, pbuf, abuf, merge_o, merge_ml, ring;
+    uint32_t full, empty, valid, misc, prefix, groups, skip, pst, pbuf, abuf, merge_o, merge_ml, ring;
     uint32_t stage_bytes, total;
-    __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt) {
+    // K: cascade groups (0 for plain decode)
+    __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt, int K = 0) {
         uint32_t off = 0;
         full = off;   off += 8u * S;
         empty = off;  off += 8u * S;
         valid = off;  off += 4u * S;
         misc = off;   off += 4u * 40;            // abort flag + warp totals
         prefix = off; off += 4u * (B + 1);
+        groups = off; off += K > 0 ? 4u * 3u * K : 0u;   // used groups: first, size, blocks
+        skip = off;   off += K > 0 ? 4u * B : 0u;        // leading blocks each sequence skips
         off = (off + 15u) & ~15u;
+        pst = off;    off += K > 0 ? (4u * G * D + 4u * G + 15u) & ~15u : 0u;  // prefix state
         pbuf = off;   off += 8u * NCW * bs * G;
         abuf = off;   off += 8u * NCW * G;
         merge_o = off;  off += 4u * (NCW - 1) * G * D;
@@ -238,6 +251,20 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // async-proxy (TMA) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Asynchronous global -> shared copies (LDGSTS): 16 bytes through L2 only,
+// or 4 bytes; wait_all blocks until this thread's copies have landed.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ------------------------------------------------------------ element I/O --
@@ -386,7 +413,19 @@ struct PieceOut {
     void* out;            // &out[b, g*G, 0] (element type of the pool)
     float* part_o;        // &part_o[slot][0][0]
     float* part_lse;      // &part_lse[slot][0]
+    const float* pst_o;   // cascade: &pst_o[b, g*G, 0] to fold into a complete piece, or null
+    const float* pst_lse; // cascade: &pst_lse[b, g*G]
 };
+
+// Fold a normalised state (o_p, lse_p) into an unnormalised one (num, den at
+// base M): returns the new base and rescales num/den in place.
+__device__ __forceinline__ float fold_state(float M, float& den, float lse_p, float& cs, float& cp) {
+    const float M2 = fmaxf(M, lse_p);
+    cs = (M2 == -CUDART_INF_F || M == -CUDART_INF_F) ? 0.f : fast_exp2(M - M2);
+    cp = (M2 == -CUDART_INF_F || lse_p == -CUDART_INF_F) ? 0.f : fast_exp2(lse_p - M2);
+    den = den * cs + cp;
+    return M2;
+}
 
 template <typename T, int D, int G, int BSC>
 struct CorePolicy {
@@ -535,6 +574,10 @@ struct CorePolicy {
     __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
                                                 const PieceOut& po) const {
         const int dl = lane % C::LPV;
+        // every load of the merge before the first store: the compiler
+        // cannot move a load above a store it might alias
+        float4 res[G];
+        float lse[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float m0 = __shfl_sync(FULL, m_run, h);
@@ -557,18 +600,29 @@ struct CorePolicy {
                     num.x += c * ow.x; num.y += c * ow.y; num.z += c * ow.z; num.w += c * ow.w;
                 }
             }
+            if (po.complete && po.pst_lse != nullptr) {
+                float cs, cp;
+                M = fold_state(M, den, po.pst_lse[h], cs, cp);
+                const float4 op4 = *reinterpret_cast<const float4*>(po.pst_o + h * D + dl * 4);
+                num.x = num.x * cs + op4.x * cp; num.y = num.y * cs + op4.y * cp;
+                num.z = num.z * cs + op4.z * cp; num.w = num.w * cs + op4.w * cp;
+            }
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            if (lane < C::LPV) {
+            res[h] = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+            lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
+        }
+        if (lane < C::LPV) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
                 if (po.complete) {
                     T* op = static_cast<T*>(po.out) + h * D + dl * 4;
-                    op[0] = Elt<T>::store(num.x * inv);
-                    op[1] = Elt<T>::store(num.y * inv);
-                    op[2] = Elt<T>::store(num.z * inv);
-                    op[3] = Elt<T>::store(num.w * inv);
+                    op[0] = Elt<T>::store(res[h].x);
+                    op[1] = Elt<T>::store(res[h].y);
+                    op[2] = Elt<T>::store(res[h].z);
+                    op[3] = Elt<T>::store(res[h].w);
                 } else {
-                    *reinterpret_cast<float4*>(po.part_o + h * D + dl * 4) =
-                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-                    if (lane == 0) po.part_lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
+                    *reinterpret_cast<float4*>(po.part_o + h * D + dl * 4) = res[h];
+                    if (lane == 0) po.part_lse[h] = lse[h];
                 }
             }
         }
@@ -752,7 +806,12 @@ struct TcPolicy {
                 c[w2] = M == -CUDART_INF_F ? 0.f : fast_exp2(mm[(w2 - 1) * G + h] - M);
                 den += c[w2] * mm[(NCW - 1) * G + (w2 - 1) * G + h];
             }
+            float fs = 1.f, fp = 0.f;                 // cascade: fold the prefix state
+            if (po.complete && po.pst_lse != nullptr) M = fold_state(M, den, po.pst_lse[h], fs, fp);
             const float inv = den > 0.f ? 1.f / den : 0.f;
+            // every load of the merge before the first store: the compiler
+            // cannot move a load above a store it might alias
+            float v[MT][2];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -761,10 +820,18 @@ struct TcPolicy {
                     float num = c[0] * oacc[mt][j + 2 * hf];
 #pragma unroll
                     for (int w2 = 1; w2 < NCW; ++w2) num += c[w2] * mo[((w2 - 1) * G + h) * D + d];
+                    if (po.complete && po.pst_lse != nullptr) num = num * fs + po.pst_o[h * D + d] * fp;
+                    v[mt][hf] = num * inv;
+                }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int d = mt * 16 + gid + 8 * hf;
                     if (po.complete)
-                        static_cast<T*>(po.out)[h * D + d] = Elt<T>::store(num * inv);
+                        static_cast<T*>(po.out)[h * D + d] = Elt<T>::store(v[mt][hf]);
                     else
-                        po.part_o[h * D + d] = num * inv;
+                        po.part_o[h * D + d] = v[mt][hf];
                 }
             if (!po.complete && gid == 0)
                 po.part_lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
@@ -791,35 +858,198 @@ __device__ __forceinline__ int count_piece(unsigned long long* ctr, unsigned epo
     return done == pieces;
 }
 
-// One warp: out[h, d] = sum_c 2^(lse_c[h] - M) o_c[h, d] / sum_c 2^(lse_c[h] - M).
-template <typename T, int D, int G>
-__device__ __forceinline__ void merge_partials(const Params& p, int seg_start, int chunk, int c0,
-                                               int c1, T* out, int lane) {
-    const int slot0 = (seg_start == c0 * chunk) ? 0 : 1;
-#pragma unroll 1
-    for (int h = 0; h < G; ++h) {
-        float M = -CUDART_INF_F;
-        for (int c = c0; c <= c1; ++c) {
-            const size_t ps = (size_t)c * 2 + (c == c0 ? slot0 : 0);
-            M = fmaxf(M, __ldcg(p.part_lse + ps * G + h));
+// Fold one normalised state (log2-sum-exp l, output o[0..N)) into a running
+// (base M, denominator den, numerator acc).
+template <int N>
+__device__ __forceinline__ void lse_add(float& M, float& den, float* acc, float l, const float* o) {
+    const float M2 = fmaxf(M, l);
+    if (M2 == -CUDART_INF_F) return;
+    const float a = M == -CUDART_INF_F ? 0.f : fast_exp2(M - M2);
+    const float w = l == -CUDART_INF_F ? 0.f : fast_exp2(l - M2);
+    den = den * a + w;
+#pragma unroll
+    for (int k = 0; k < N; ++k) acc[k] = acc[k] * a + w * o[k];
+    M = M2;
+}
+
+template <int N>
+__device__ __forceinline__ void load_row(float* v, const float* src, bool cached_l2_only) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < N; k += 4) {
+            const float4 x = cached_l2_only ? __ldcg(reinterpret_cast<const float4*>(src + k))
+                                            : *reinterpret_cast<const float4*>(src + k);
+            v[k] = x.x; v[k + 1] = x.y; v[k + 2] = x.z; v[k + 3] = x.w;
         }
-        float den = 0.f, num[D / 32];
+    } else {
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) num[k] = 0.f;
-        if (M != -CUDART_INF_F) {
-            for (int c = c0; c <= c1; ++c) {
-                const size_t ps = (size_t)c * 2 + (c == c0 ? slot0 : 0);
-                const float wgt = fast_exp2(__ldcg(p.part_lse + ps * G + h) - M);
-                den += wgt;
+        for (int k = 0; k < N; ++k) v[k] = cached_l2_only ? __ldcg(src + k) : src[k];
+    }
+}
+
+// One warp merges the partial states that a segment cut across CTAs c0..c1
+// left in their slots (CTA c0's piece in slot slot0 of c0, every later CTA's
+// in slot 0), plus an optional extra state (x_o, x_lse; null for none).  Each
+// is a normalised output [R][D] with its log2-sum-exp [R]:
+//   out[r, d] = sum_i 2^(lse_i[r] - M) o_i[r, d] / sum_i 2^(lse_i[r] - M).
+// A lane owns EPL consecutive dims of one row; the slots are read
+// kMergeBatch at a time so that their loads are in flight together.  store(r, d0, vals, lse)
+// takes row r's merge_epl<R, D>() results from dim d0 and the row's merged
+// log2-sum-exp.
+constexpr int kMergeBatch = 2;   // slots whose loads merge_cut issues together
+
+template <int R, int D>
+__host__ __device__ constexpr int merge_epl() {
+    return ((R * D) % 256 == 0 && D % 8 == 0) ? 8 : ((R * D) % 128 == 0 && D % 4 == 0) ? 4
+         : ((R * D) % 64 == 0 && D % 2 == 0) ? 2 : 1;
+}
+
+template <int R, int D, class Store>
+__device__ __forceinline__ void merge_cut(const float* part_o, const float* part_lse, int c0,
+                                          int c1, int slot0, const float* x_o, const float* x_lse,
+                                          int lane, Store&& store) {
+    constexpr int E = R * D;
+    constexpr int EPL = merge_epl<R, D>();
+    static_assert(E % (32 * EPL) == 0, "rows x dims must be whole warps of lanes");
+#pragma unroll 1
+    for (int pass = 0; pass < E / (32 * EPL); ++pass) {
+        const int e0 = (pass * 32 + lane) * EPL;
+        const int r = e0 / D, d0 = e0 % D;
+        float M = -CUDART_INF_F, den = 0.f, acc[EPL];
 #pragma unroll
-                for (int k = 0; k < D / 32; ++k)
-                    num[k] += wgt * __ldcg(p.part_o + (ps * G + h) * D + lane + 32 * k);
+        for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
+        for (int c = c0; c <= c1; c += kMergeBatch) {
+            float ls[kMergeBatch], ov[kMergeBatch][EPL];
+#pragma unroll
+            for (int t = 0; t < kMergeBatch; ++t) {
+                const int cc = c + t;
+                const size_t slot = (size_t)cc * 2 + (cc == c0 ? slot0 : 0);
+                ls[t] = -CUDART_INF_F;
+                if (cc <= c1) {
+                    ls[t] = __ldcg(part_lse + slot * R + r);
+                    load_row<EPL>(ov[t], part_o + (slot * R + r) * D + d0, true);
+                }
             }
+#pragma unroll
+            for (int t = 0; t < kMergeBatch; ++t)
+                if (c + t <= c1) lse_add<EPL>(M, den, acc, ls[t], ov[t]);
+        }
+        if (x_lse != nullptr) {
+            float xv[EPL];
+            load_row<EPL>(xv, x_o + r * D + d0, false);
+            lse_add<EPL>(M, den, acc, x_lse[r], xv);
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) out[h * D + lane + 32 * k] = Elt<T>::store(num[k] * inv);
+        for (int k = 0; k < EPL; ++k) acc[k] *= inv;
+        store(r, d0, acc, den > 0.f ? M + fast_log2(den) : -CUDART_INF_F);
     }
+}
+
+// ------------------------------------------------- block-wide scans --
+// One int per thread, every thread of the CTA calls; `scratch` holds a word
+// per warp.  Exclusive sum (and the total), exclusive max of non-negatives.
+__device__ __forceinline__ int block_excl_sum(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    int off = 0, tot = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        if (w < warp) off += scratch[w];
+        tot += scratch[w];
+    }
+    __syncthreads();
+    if (total) *total = tot;
+    return off + x - v;
+}
+__device__ __forceinline__ int block_excl_max(int v, int* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x = max(x, y);
+    }
+    const int up = __shfl_up_sync(FULL, x, 1);
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    int off = lane > 0 ? up : 0;
+    for (int w = 0; w < warp; ++w) off = max(off, scratch[w]);
+    __syncthreads();
+    return off;
+}
+
+// ------------------------------------------- cascade groups (both passes) --
+// A group (first member, members, shared leading blocks) is used when it lies
+// inside the batch, starts at or after the end of every earlier group, and at
+// least one block is shared (the count is clamped to each member's own block
+// count).  Both passes compact the used groups, in order, into shared memory
+// (vg: first[n], size[n], blocks[n]) and return n; unused groups set
+// KV_DEVERR_GROUP_RANGE when malformed.  Every thread of the CTA calls.
+__device__ __forceinline__ int load_groups(const int32_t* g_first, const int32_t* g_size,
+                                           const int32_t* g_blocks, int K, const int32_t* seq_lens,
+                                           int B, int bs, int cap, int* vg, int* scratch, int* err) {
+    const int per = (K + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int k0 = min(K, (int)threadIdx.x * per), k1 = min(K, k0 + per);
+    auto raw_end = [&](int k) {
+        const long long e = (long long)g_first[k] + (long long)max(g_size[k], 0);
+        return (int)min(max(e, 0ll), 2147483647ll);
+    };
+    auto shared_blocks = [&](int k, int before, bool& ok) {
+        const int first = g_first[k], size = g_size[k];
+        int blocks = g_blocks[k];
+        ok = first >= 0 && size >= 1 && (long long)first + size <= B && blocks >= 0 &&
+             first >= before;
+        if (!ok) return 0;
+        for (int m = 0; m < size; ++m)
+            blocks = min(blocks, (min(max(seq_lens[first + m], 0), cap) + bs - 1) / bs);
+        return blocks;
+    };
+    int cmax = 0;
+    for (int k = k0; k < k1; ++k) cmax = max(cmax, raw_end(k));
+    const int before0 = block_excl_max(cmax, scratch);
+    int before = before0, keep = 0;
+    bool bad = false;
+    for (int k = k0; k < k1; ++k) {
+        bool ok;
+        keep += shared_blocks(k, before, ok) > 0;
+        bad |= !ok;
+        before = max(before, raw_end(k));
+    }
+    if (bad && blockIdx.x == 0) atomicOr(err, KV_DEVERR_GROUP_RANGE);
+    int n = 0;
+    int idx = block_excl_sum(keep, scratch, &n);
+    before = before0;
+    for (int k = k0; k < k1; ++k) {
+        bool ok;
+        const int blocks = shared_blocks(k, before, ok);
+        before = max(before, raw_end(k));
+        if (blocks > 0) {
+            vg[idx] = g_first[k];
+            vg[K + idx] = g_size[k];
+            vg[2 * K + idx] = blocks;
+            ++idx;
+        }
+    }
+    __syncthreads();
+    return n;
+}
+
+// Shared leading blocks of sequence b (0 outside every used group).
+__device__ __forceinline__ int group_skip(const int* vg, int K, int n, int b) {
+    if (n == 0 || b < vg[0]) return 0;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (vg[mid] <= b) lo = mid; else hi = mid;
+    }
+    return b < vg[lo] + vg[K + lo] ? vg[2 * K + lo] : 0;
 }
 
 // ------------------------------------------------------------ split kernel --
@@ -832,17 +1062,19 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int B = p.batch, S = p.stages, H = p.num_kv_heads, bs = p.bs;
-    const Layout lay(S, B, bs, G, D, ELT);
+    const Layout lay(S, B, bs, G, D, ELT, p.num_groups);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc);
     int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
     int* prefix = reinterpret_cast<int*>(smem + lay.prefix);
+    int* skip_s = reinterpret_cast<int*>(smem + lay.skip);
     unsigned char* ring = smem + lay.ring;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cap = p.max_blocks * bs;              // longest context a table can hold
+    const bool cascade = p.num_groups > 0;
 
     // -- 1. the blocks-per-sequence prefix of the clamped lengths -----------
     if (tid == 0) {
@@ -856,6 +1088,11 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     pdl_launch_dependents();
     pdl_wait();                                    // inputs of earlier kernels are visible
     {
+        // cascade: the leading blocks the shared-prefix pass attended
+        int* vg = reinterpret_cast<int*>(smem + lay.groups);
+        const int nvg = cascade ? load_groups(p.g_first, p.g_size, p.g_blocks, p.num_groups,
+                                              p.seq_lens, B, bs, cap, vg, warp_tot, p.err)
+                                : 0;
         const int per = (B + NTHREADS - 1) / NTHREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int local = 0;
@@ -863,32 +1100,31 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         for (int b = b0; b < b1; ++b) {
             const int L = p.seq_lens[b];
             over |= L > cap;
-            local += (min(max(L, 0), cap) + bs - 1) / bs;
+            const int nb = (min(max(L, 0), cap) + bs - 1) / bs;
+            const int skip = cascade ? min(group_skip(vg, p.num_groups, nvg, b), nb) : 0;
+            if (cascade) skip_s[b] = skip;
+            local += nb - skip;
         }
         if (over && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_SEQ_RANGE);
-        int x = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(FULL, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) warp_tot[warp] = x;
-        __syncthreads();
-        int woff = 0;
-        for (int w = 0; w < warp; ++w) woff += warp_tot[w];
-        int run = woff + x - local;
+        int total = 0;
+        int run = block_excl_sum(local, warp_tot, &total);
         for (int b = b0; b < b1; ++b) {
             prefix[b] = run;
-            run += (min(max(p.seq_lens[b], 0), cap) + bs - 1) / bs;
+            const int nb = (min(max(p.seq_lens[b], 0), cap) + bs - 1) / bs;
+            run += nb - (cascade ? skip_s[b] : 0);
         }
-        if (tid == NTHREADS - 1) prefix[B] = woff + x;
+        if (tid == 0) prefix[B] = total;
     }
     __syncthreads();
-    // sequences with no context get zeros (no unit covers them)
+    // sequences no unit covers: zeros, or (cascade) the prefix state alone
     for (int b = blockIdx.x; b < B; b += gridDim.x)
         if (prefix[b + 1] == prefix[b]) {
             T* ob = static_cast<T*>(p.out) + (size_t)b * p.num_q_heads * D;
-            for (int i = tid; i < p.num_q_heads * D; i += NTHREADS) ob[i] = Elt<T>::store(0.f);
+            const bool has = cascade && skip_s[b] > 0;
+            for (int i = tid; i < p.num_q_heads * D; i += NTHREADS) {
+                const size_t row = (size_t)b * p.num_q_heads + i / D;
+                ob[i] = Elt<T>::store(has ? p.pst_o[row * D + i % D] : 0.f);
+            }
         }
 
     const int U = prefix[B] * H;
@@ -912,7 +1148,8 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                 const int nb = prefix[b + 1] - prefix[b];
                 const int r = uu - prefix[b] * H;
                 gg = r / nb;
-                id = __ldg(p.block_tables + (size_t)b * p.max_blocks + (r - gg * nb));
+                id = __ldg(p.block_tables + (size_t)b * p.max_blocks +
+                           (cascade ? skip_s[b] : 0) + (r - gg * nb));
             }
         };
         int id_cur, g_cur, id_nxt, g_nxt;
@@ -970,6 +1207,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     // merge area: warps 1..NCW-1 leave (o [G][D], m [G], l [G]) for warp 0
     float* mo = reinterpret_cast<float*>(smem + lay.merge_o);
     float* mm = reinterpret_cast<float*>(smem + lay.merge_ml);
+    float* pst_s = reinterpret_cast<float*>(smem + lay.pst);   // cascade: [G][D] then [G]
     const T* qbase = static_cast<const T*>(p.q);
     T* obase = static_cast<T*>(p.out);
     Pol pol(pb, ab);
@@ -984,7 +1222,16 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         const int seg_start = prefix[b] * H + g * nb;
         const int piece_end = min(end, seg_start + nb);
         const int Lb = min(max(p.seq_lens[b], 0), cap);
+        const int skip = cascade ? skip_s[b] : 0;
         const size_t head0 = (size_t)b * p.num_q_heads + (size_t)g * G;
+        // cascade: warp 0, which merges, stages this (b, g)'s prefix state in
+        // shared memory while the piece's blocks are attended
+        if (w == 0 && skip > 0) {
+            __syncwarp();                          // the last piece's reads are done
+            for (int i = lane; i < G * D / 4; i += 32)
+                cp_async16(pst_s + 4 * i, p.pst_o + head0 * D + 4 * i);
+            if (lane < G) cp_async4(pst_s + G * D + lane, p.pst_lse + head0 + lane);
+        }
 
         pol.begin(qbase + head0 * D, p.qscale, lane);
 
@@ -1000,7 +1247,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
             }
             ok = __all_sync(FULL, ok);
             if (ok && valid[s]) {
-                const int j = j0 + (uu - u);
+                const int j = skip + j0 + (uu - u);
                 const unsigned char* Ks = ring + (size_t)s * lay.stage_bytes;
                 pol.block(Ks, Ks + lay.stage_bytes / 2, min(bs, Lb - j * bs), bs, p.qscale, lane);
             }
@@ -1026,6 +1273,12 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
             po.out = obase + head0 * D;
             po.part_o = p.part_o + ps * G * D;
             po.part_lse = p.part_lse + ps * G;
+            po.pst_o = skip > 0 ? pst_s : nullptr;
+            po.pst_lse = skip > 0 ? pst_s + G * D : nullptr;
+            if (skip > 0) {
+                cp_async_wait_all();
+                __syncwarp();
+            }
             pol.merge_store(mo, mm, lane, po);
             if (!po.complete) {
                 // Count the finished pieces of (b, g); the CTA that finishes
@@ -1038,7 +1291,14 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                     last = count_piece(p.counters + (size_t)b * H + g, p.epoch, c1 - c0 + 1);
                 if (__shfl_sync(FULL, last, 0)) {
                     __threadfence();
-                    merge_partials<T, D, G>(p, seg_start, chunk, c0, c1, obase + head0 * D, lane);
+                    T* ob = obase + head0 * D;
+                    merge_cut<G, D>(p.part_o, p.part_lse, c0, c1,
+                                    seg_start == c0 * chunk ? 0 : 1, po.pst_o, po.pst_lse, lane,
+                                    [&](int r, int d0, const float* v, float) {
+#pragma unroll
+                                        for (int k = 0; k < merge_epl<G, D>(); ++k)
+                                            ob[r * D + d0 + k] = Elt<T>::store(v[k]);
+                                    });
                 }
             }
             named_arrive(2);
@@ -1077,6 +1337,12 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.num_ctas = plan.num_ctas;
     p.qscale = call.scale * 1.4426950408889634f;
     p.epoch = call.epoch;
+    p.g_first = call.g_first;
+    p.g_size = call.g_size;
+    p.g_blocks = call.g_blocks;
+    p.num_groups = call.num_groups;
+    p.pst_o = call.pst_o;
+    p.pst_lse = call.pst_lse;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.num_ctas);
     cfg.blockDim = dim3(NTHREADS);

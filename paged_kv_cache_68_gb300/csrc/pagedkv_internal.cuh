@@ -42,12 +42,27 @@ struct kv_pool {
     std::mutex plan_mu;
     int plan_batch = -1;
     int plan_hq = -1;
+    int plan_groups = -1;
     pagedkv::DecodePlan plan;
 };
 
 namespace pagedkv {
 
 constexpr int kMaxBatch = 4096;
+constexpr int kMaxGroups = 1024;   // cascade decode: groups per call
+
+// Record the text of a failed CUDA call for kv_last_cuda_error; returns KV_ECUDA.
+kv_status cuda_fail(cudaError_t e, const char* where);
+
+// The split decode after a cascade prefix pass: the groups, and that pass's
+// states in the workspace; `plain_ws_bytes` is the part of the workspace the
+// split kernel itself uses (at its start).
+kv_status decode_after_prefix(kv_pool* pool, const void* q, void* out, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                              int num_q_heads, float scale, void* workspace,
+                              size_t plain_ws_bytes, const int32_t* g_first, const int32_t* g_size,
+                              const int32_t* g_blocks, int num_groups, const float* pst_o,
+                              const float* pst_lse, cudaStream_t stream);
 
 // Bounded waits: a pipeline wait gives up after this many nanoseconds, sets
 // KV_DEVERR_TIMEOUT and lets the kernel finish without the missing data.
@@ -71,12 +86,20 @@ struct DecodeCall {
     void* workspace;
     size_t workspace_bytes;
     unsigned epoch;        // nonzero, distinct for consecutive calls
+    // cascade decode: the groups and the shared-prefix pass's states
+    const int32_t* g_first = nullptr;
+    const int32_t* g_size = nullptr;
+    const int32_t* g_blocks = nullptr;
+    int num_groups = 0;
+    const float* pst_o = nullptr;
+    const float* pst_lse = nullptr;
 };
 
 // Fill `plan` for this pool / batch / head count on the current device
 // (cached per pool).  Returns cudaErrorNotSupported for shapes with no
 // compiled kernel.
-cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, DecodePlan* plan);
+cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_groups,
+                        DecodePlan* plan);
 
 cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
                           cudaStream_t stream);

@@ -7,8 +7,10 @@ fails, an exception is raised.
 
 The module-level functions carry the C names (``kv_pool_create``,
 ``kv_append``, ``copy_blocks``, ``paged_attention_workspace_size``,
-``paged_attention_decode``, ``kv_pool_get_error``, ``kv_pool_clear_error``,
-``kv_pool_destroy``); ``KVPool`` bundles them for convenience.
+``paged_attention_decode``, ``paged_attention_cascade_workspace_size``,
+``paged_attention_decode_cascade``, ``paged_attention_decode_noalloc``,
+``kv_pool_get_error``, ``kv_pool_clear_error``, ``kv_pool_destroy``);
+``KVPool`` bundles them for convenience.
 """
 
 from __future__ import annotations
@@ -28,6 +30,7 @@ KV_DEVERR_BLOCK_RANGE = 0x2
 KV_DEVERR_PAIR_RANGE = 0x4
 KV_DEVERR_SEQ_RANGE = 0x8
 KV_DEVERR_TIMEOUT = 0x10
+KV_DEVERR_GROUP_RANGE = 0x20
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
@@ -67,6 +70,8 @@ def load(build: bool = True) -> ctypes.CDLL:
             "copy_blocks": ([P, P, I, P], I),
             "paged_attention_workspace_size": ([P, I, I, ctypes.POINTER(S)], I),
             "paged_attention_decode": ([P, P, P, P, I, P, I, I, F, I, P, S, P], I),
+            "paged_attention_cascade_workspace_size": ([P, I, I, I, ctypes.POINTER(S)], I),
+            "paged_attention_decode_cascade": ([P, P, P, P, I, P, I, I, F, I, P, P, P, I, P, S, P], I),
             "kv_pool_get_error": ([P, ctypes.POINTER(I)], I),
             "kv_pool_clear_error": ([P], I),
             "kv_strerror": ([I], ctypes.c_char_p),
@@ -153,6 +158,31 @@ def paged_attention_decode(handle, q, out, block_tables, seq_lens, scale: float,
         _stream(stream)), "paged_attention_decode")
 
 
+def paged_attention_cascade_workspace_size(handle, batch: int, num_q_heads: int,
+                                           num_groups: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().paged_attention_cascade_workspace_size(handle, batch, num_q_heads, num_groups,
+                                                         ctypes.byref(out)),
+           "paged_attention_cascade_workspace_size")
+    return int(out.value)
+
+
+def paged_attention_decode_cascade(handle, q, out, block_tables, seq_lens, scale: float,
+                                   num_kv_heads: int, group_first, group_size,
+                                   group_shared_blocks, workspace, dtype, stream=None) -> None:
+    b, hq, _ = q.shape
+    k = int(group_first.numel())
+    gp = lambda t, n: _dev(t, n, torch.int32) if k else None
+    _check(load().paged_attention_decode_cascade(
+        handle, _dev(q, "q", dtype), _dev(out, "out", dtype),
+        _dev(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), int(b), int(hq), float(scale), int(num_kv_heads),
+        gp(group_first, "group_first"), gp(group_size, "group_size"),
+        gp(group_shared_blocks, "group_shared_blocks"), k,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "paged_attention_decode_cascade")
+
+
 def kv_pool_get_error(handle) -> int:
     bits = ctypes.c_int()
     st = load().kv_pool_get_error(handle, ctypes.byref(bits))
@@ -209,6 +239,25 @@ class KVPool:
             workspace = self.workspace(q.shape[0], q.shape[1])
         paged_attention_decode(self.handle, q, out, block_tables, seq_lens, scale,
                                self.num_kv_heads, workspace, self.dtype, stream)
+        return out
+
+    def decode_cascade(self, q, block_tables, seq_lens, scale: float, groups, out=None,
+                       workspace=None, stream=None) -> torch.Tensor:
+        """Decode with shared-prefix groups: ``groups`` int32 [K, 3] on the
+        device, rows (first member, members, shared leading blocks)."""
+        if out is None:
+            out = torch.empty_like(q)
+        groups = groups.reshape(-1, 3)
+        k = int(groups.shape[0])
+        if workspace is None:
+            need = paged_attention_cascade_workspace_size(self.handle, q.shape[0], q.shape[1], k)
+            if self._ws is None or self._ws.numel() < need:
+                self._ws = torch.empty(need, dtype=torch.uint8, device=self.k_pool.device)
+            workspace = self._ws
+        cols = [groups[:, i].contiguous() for i in range(3)]
+        paged_attention_decode_cascade(self.handle, q, out, block_tables, seq_lens, scale,
+                                       self.num_kv_heads, cols[0], cols[1], cols[2], workspace,
+                                       self.dtype, stream)
         return out
 
     def get_error(self) -> int:

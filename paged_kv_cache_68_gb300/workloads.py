@@ -59,6 +59,9 @@ class Workload:
     seq_lens: np.ndarray        # int32 [B], after the append
     pairs: np.ndarray           # int32 [P, 2] (src, dst), this step's copies
     info: Dict[str, float] = field(default_factory=dict)
+    # sequences sharing prefix blocks: int32 [K, 3] (first member, members,
+    # shared leading blocks), or None
+    groups: Optional[np.ndarray] = None
 
     @property
     def batch(self) -> int:
@@ -398,6 +401,9 @@ def shared_prefix(seed: int = 0, prompts: int = 32, prompt_len: int = 2000, n: i
                  slot_mapping=np.asarray(slots, dtype=np.int64),
                  block_tables=_tables_array(bm, list(range(S)), None), seq_lens=seq_lens,
                  pairs=np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    groups = np.asarray([[p * n, n, bm.shared_prefix_blocks(range(p * n, p * n + n))]
+                         for p in range(prompts)], dtype=np.int32).reshape(-1, 3)
+    w.groups = groups
     unique_tokens = prompts * prompt_len + int(seq_lens.sum()) - S * prompt_len
     w.info = {"seed": seed, "tokens": int(seq_lens.sum()), "unique_tokens": unique_tokens,
               "history_copies": history_copies, "step_copies": len(pairs),
