@@ -739,6 +739,8 @@ struct TcPolicy {
             m_run[j] = mnew[j];
         }
         const float2 a2 = make_float2(alpha[0], alpha[1]);
+        // rescale the accumulators only when some running maximum moved
+        if (!__all_sync(FULL, alpha[0] == 1.f && alpha[1] == 1.f))
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             float2 lo = __fmul2_rn(make_float2(oacc[mt][0], oacc[mt][1]), a2);

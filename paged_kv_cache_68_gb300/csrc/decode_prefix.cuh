@@ -167,23 +167,28 @@ struct TcRows {
         float s[TT][NT][4];
 #pragma unroll
         for (int tt = 0; tt < TT; ++tt) {
-            float acc[NT][4];
+            // even and odd k-steps accumulate apart: two independent MMA chains
+            float acc[2][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    acc[h2][nt][0] = acc[h2][nt][1] = acc[h2][nt][2] = acc[h2][nt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a[4];
                 ldsm_x4(a, swz(kbase, tt * 16 + (mi & 1) * 8 + r8, ks * 2 + (mi >> 1)));
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) Mma<T>::run(acc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+                for (int nt = 0; nt < NT; ++nt)
+                    Mma<T>::run(acc[ks & 1][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
             }
             const int t0 = tt * 16 + gid, t1 = t0 + 8;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                s[tt][nt][0] = t0 < nv[nt][0] ? acc[nt][0] * qscale : -CUDART_INF_F;
-                s[tt][nt][1] = t0 < nv[nt][1] ? acc[nt][1] * qscale : -CUDART_INF_F;
-                s[tt][nt][2] = t1 < nv[nt][0] ? acc[nt][2] * qscale : -CUDART_INF_F;
-                s[tt][nt][3] = t1 < nv[nt][1] ? acc[nt][3] * qscale : -CUDART_INF_F;
+                s[tt][nt][0] = t0 < nv[nt][0] ? (acc[0][nt][0] + acc[1][nt][0]) * qscale : -CUDART_INF_F;
+                s[tt][nt][1] = t0 < nv[nt][1] ? (acc[0][nt][1] + acc[1][nt][1]) * qscale : -CUDART_INF_F;
+                s[tt][nt][2] = t1 < nv[nt][0] ? (acc[0][nt][2] + acc[1][nt][2]) * qscale : -CUDART_INF_F;
+                s[tt][nt][3] = t1 < nv[nt][1] ? (acc[0][nt][3] + acc[1][nt][3]) * qscale : -CUDART_INF_F;
             }
         }
         // -- online softmax per column ----------------------------------------
@@ -223,6 +228,11 @@ struct TcRows {
                 l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + lsum[nt][j];
                 m_run[nt][j] = mnew[nt][j];
             }
+        // rescale the accumulators only when some running maximum moved
+        bool same = true;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) same = same && alpha[nt][0] == 1.f && alpha[nt][1] == 1.f;
+        if (!__all_sync(FULL, same))
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
