@@ -30,6 +30,8 @@
  *
  * Element types: 0 = IEEE binary32, 1 = IEEE binary16, 2 = bfloat16 (the top
  * 16 bits of a binary32).  Decoding is written from the formats' definitions.
+ * 8-bit pools (FP8 E4M3 with a per-pool scale, INT8 with per-token scales)
+ * are described at their section below.
  */
 #include <math.h>
 #include <pthread.h>
@@ -132,11 +134,162 @@ long oracle_copy_blocks(void* k_pool, void* v_pool, long num_blocks,
     return bad;
 }
 
+/* ------------------------------------------------------- 8-bit KV cache --
+ *
+ * [RL-Part3] ch. 10 (KV cache quantisation): a new token's K and V are scaled
+ * and rounded to 8 bits before they are stored, and turned back into wider
+ * numbers when the attention reads them (sec. 1); INT8 is a scale plus a
+ * rounding to integers, with a fine-grained (per-token) scale (sec. 3); FP8 is
+ * a shorter float (sec. 3).  Readings where the chapter is silent:
+ *   OR_E4M3: E4M3 (bias 7, 3 mantissa bits, S.1111.111 = NaN, max 448), one
+ *     scale per pool: code = E4M3(x / scale) with the division in fp32,
+ *     nearest-even rounding, saturation to +-448 (infinities too), NaN -> 0x7F;
+ *     value = decode(code) * scale.
+ *   OR_INT8: one scale per (token, KV head): amax = max |x| over the row,
+ *     inv = 127 / amax and scale = amax / 127 in fp32, code = rint(x * inv)
+ *     (fp32 product, ties to even) clipped to [-127, 127]; all-zero row:
+ *     scale 0, codes 0; a row holding NaN or an infinity: scale NaN, codes 0.
+ *     value = code * scale.
+ *   Codes use the pool layout [num_blocks, block_size, Hkv, D], one byte each;
+ *   INT8 scales are fp32 [num_blocks, Hkv, block_size].
+ */
+enum { OR_E4M3 = 3, OR_INT8 = 4 };
+
+static double e4m3_decode(uint8_t c) {
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);                 /* m/8 * 2^-6 */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+static uint8_t e4m3_encode(float t) {
+    if (isnan(t)) return 0x7F;
+    uint8_t sign = signbit(t) ? 0x80 : 0;
+    double a = fabs((double)t);
+    if (a > 448.0) a = 448.0;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                          /* a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    if (E < -6) E = -6;                    /* below 2^-6 the grid is 2^-9 */
+    double step = ldexp(1.0, E - 3);
+    double v = nearbyint(a / step) * step; /* exact quotient; ties to even */
+    if (v == 0.0) return sign;
+    frexp(v, &e);
+    E = e - 1;
+    if (E < -6) return (uint8_t)(sign | (int)(v / ldexp(1.0, -9)));
+    return (uint8_t)(sign | ((E + 7) << 3) | ((int)(v / ldexp(1.0, E - 3)) - 8));
+}
+
+static void int8_quantize_row(const float* x, long n, int8_t* codes, float* scale) {
+    float amax = 0.0f;
+    int finite = 1;
+    for (long i = 0; i < n; ++i) {
+        if (!isfinite(x[i])) finite = 0;
+        else if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+    }
+    for (long i = 0; i < n; ++i) codes[i] = 0;
+    if (!finite) { *scale = NAN; return; }
+    if (amax == 0.0f) { *scale = 0.0f; return; }
+    float inv = 127.0f / amax;
+    for (long i = 0; i < n; ++i) {
+        float t = x[i] * inv;
+        float r = nearbyintf(t);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        codes[i] = (int8_t)r;
+    }
+    *scale = amax / 127.0f;
+}
+
+static double dequant(const void* codes, size_t idx, int fmt, float row_scale,
+                      double pool_scale) {
+    uint8_t c = ((const uint8_t*)codes)[idx];
+    if (fmt == OR_E4M3) return e4m3_decode(c) * pool_scale;
+    return (double)(int8_t)c * (double)row_scale;
+}
+
+/* Exposed for the tests. */
+double oracle_e4m3_decode(int code) { return e4m3_decode((uint8_t)code); }
+int oracle_e4m3_encode(float t) { return e4m3_encode(t); }
+void oracle_int8_quantize_row(const float* x, long n, int8_t* codes, float* scale) {
+    int8_quantize_row(x, n, codes, scale);
+}
+
+/*
+ * Quantising append: kv_append's slot rule, with each (token, KV head) row of
+ * the new K and V (elements of `dtype`, read as fp32) quantised to `fmt`.
+ * Returns the number of out-of-range slots.
+ */
+long oracle_append_q8(uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales,
+                      long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                      int fmt, int dtype, const void* k_new, const void* v_new,
+                      const int64_t* slot_mapping, long num_tokens,
+                      float fp8_k_scale, float fp8_v_scale) {
+    long nrows = num_blocks * block_size, D = head_dim, Hkv = num_kv_heads;
+    long bad = 0;
+    float* x = (float*)malloc(sizeof(float) * (size_t)D);
+    int8_t* c8 = (int8_t*)malloc((size_t)D);
+    if (!x || !c8) { free(x); free(c8); return -1; }
+    for (long i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= nrows) { ++bad; continue; }
+        long blk = (long)(slot / block_size), off = (long)(slot % block_size);
+        for (int kv = 0; kv < 2; ++kv) {
+            const void* src = kv ? v_new : k_new;
+            uint8_t* codes = kv ? v_codes : k_codes;
+            float* scales = kv ? v_scales : k_scales;
+            float s8 = kv ? fp8_v_scale : fp8_k_scale;
+            for (long g = 0; g < Hkv; ++g) {
+                size_t in = ((size_t)i * Hkv + g) * D;
+                size_t dst = (((size_t)blk * block_size + off) * Hkv + g) * D;
+                for (long d = 0; d < D; ++d) x[d] = (float)load_elem(src, in + d, dtype);
+                if (fmt == OR_E4M3) {
+                    for (long d = 0; d < D; ++d) codes[dst + d] = e4m3_encode(x[d] / s8);
+                } else {
+                    float sc;
+                    int8_quantize_row(x, D, c8, &sc);
+                    memcpy(codes + dst, c8, (size_t)D);
+                    scales[((size_t)blk * Hkv + g) * block_size + off] = sc;
+                }
+            }
+        }
+    }
+    free(x);
+    free(c8);
+    return bad;
+}
+
+/* copy_blocks for an 8-bit pool: codes, and INT8 scales when given. */
+long oracle_copy_blocks_q8(uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales,
+                           long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                           const int32_t* pairs, long num_pairs) {
+    size_t blk = (size_t)block_size * num_kv_heads * head_dim;
+    size_t sblk = (size_t)num_kv_heads * block_size;
+    long bad = 0;
+    for (long p = 0; p < num_pairs; ++p) {
+        long src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) { ++bad; continue; }
+        memmove(k_codes + dst * blk, k_codes + src * blk, blk);
+        memmove(v_codes + dst * blk, v_codes + src * blk, blk);
+        if (k_scales) memmove(k_scales + dst * sblk, k_scales + src * sblk, sblk * 4);
+        if (v_scales) memmove(v_scales + dst * sblk, v_scales + src * sblk, sblk * 4);
+    }
+    return bad;
+}
+
+
 typedef struct {
     const void* q;
     const void* k_pool;
     const void* v_pool;
-    int dtype;
+    int dtype;          /* element type of q and out, and of the pool if fmt < 0 */
+    int fmt;            /* -1: pool holds `dtype` elements; OR_E4M3 / OR_INT8: 8-bit codes */
+    const float* k_scales, *v_scales;   /* OR_INT8: [num_blocks, Hkv, block_size] */
+    double fp8_k_scale, fp8_v_scale;    /* OR_E4M3: one scale per pool */
     long num_blocks, block_size, num_kv_heads, head_dim;
     const int32_t* block_tables;
     long max_blocks_per_seq;
@@ -189,9 +342,21 @@ static void decode_one_seq(decode_job* J, long b, double* kbuf, double* vbuf,
                 continue;
             }
             size_t row = (((size_t)phys * bs + t % bs) * Hkv + g) * D;
-            for (long d = 0; d < D; ++d) {
-                kbuf[n * D + d] = load_elem(J->k_pool, row + d, J->dtype);
-                vbuf[n * D + d] = load_elem(J->v_pool, row + d, J->dtype);
+            if (J->fmt < 0) {
+                for (long d = 0; d < D; ++d) {
+                    kbuf[n * D + d] = load_elem(J->k_pool, row + d, J->dtype);
+                    vbuf[n * D + d] = load_elem(J->v_pool, row + d, J->dtype);
+                }
+            } else {
+                size_t srow = ((size_t)phys * Hkv + g) * bs + t % bs;
+                for (long d = 0; d < D; ++d) {
+                    kbuf[n * D + d] = dequant(J->k_pool, row + d, J->fmt,
+                                              J->k_scales ? J->k_scales[srow] : 0.0f,
+                                              J->fp8_k_scale);
+                    vbuf[n * D + d] = dequant(J->v_pool, row + d, J->fmt,
+                                              J->v_scales ? J->v_scales[srow] : 0.0f,
+                                              J->fp8_v_scale);
+                }
             }
             ++n;
         }
@@ -244,11 +409,13 @@ static void* decode_worker(void* arg) {
  * positive count of such problems otherwise (the offending positions are
  * skipped), or -1 on bad arguments / no memory.
  */
-long oracle_decode(const void* q, const void* k_pool, const void* v_pool, int dtype,
-                   long num_blocks, long block_size, long num_kv_heads, long head_dim,
-                   const int32_t* block_tables, long max_blocks_per_seq,
-                   const int32_t* seq_lens, long batch, long num_q_heads,
-                   double scale, double* out, int num_threads) {
+static long run_decode(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                       int fmt, const float* k_scales, const float* v_scales,
+                       double fp8_k_scale, double fp8_v_scale,
+                       long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                       const int32_t* block_tables, long max_blocks_per_seq,
+                       const int32_t* seq_lens, long batch, long num_q_heads,
+                       double scale, double* out, int num_threads) {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 ||
         head_dim <= 0 || batch < 0)
         return -1;
@@ -260,6 +427,8 @@ long oracle_decode(const void* q, const void* k_pool, const void* v_pool, int dt
     for (int i = 0; i < num_threads; ++i) {
         decode_job* J = &jobs[i];
         J->q = q; J->k_pool = k_pool; J->v_pool = v_pool; J->dtype = dtype;
+        J->fmt = fmt; J->k_scales = k_scales; J->v_scales = v_scales;
+        J->fp8_k_scale = fp8_k_scale; J->fp8_v_scale = fp8_v_scale;
         J->num_blocks = num_blocks; J->block_size = block_size;
         J->num_kv_heads = num_kv_heads; J->head_dim = head_dim;
         J->block_tables = block_tables; J->max_blocks_per_seq = max_blocks_per_seq;
@@ -283,4 +452,34 @@ long oracle_decode(const void* q, const void* k_pool, const void* v_pool, int dt
     free(jobs);
     free(tids);
     return bad;
+}
+
+long oracle_decode(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                   long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                   const int32_t* block_tables, long max_blocks_per_seq,
+                   const int32_t* seq_lens, long batch, long num_q_heads,
+                   double scale, double* out, int num_threads) {
+    return run_decode(q, k_pool, v_pool, dtype, -1, NULL, NULL, 1.0, 1.0, num_blocks,
+                      block_size, num_kv_heads, head_dim, block_tables, max_blocks_per_seq,
+                      seq_lens, batch, num_q_heads, scale, out, num_threads);
+}
+
+/*
+ * The same decode over an 8-bit pool: every K/V element read is the
+ * dequantised value of its code (fmt OR_E4M3 or OR_INT8, see above); q and
+ * out are `dtype` elements.
+ */
+long oracle_decode_q8(const void* q, int dtype, const uint8_t* k_codes, const uint8_t* v_codes,
+                      const float* k_scales, const float* v_scales, int fmt,
+                      double fp8_k_scale, double fp8_v_scale,
+                      long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                      const int32_t* block_tables, long max_blocks_per_seq,
+                      const int32_t* seq_lens, long batch, long num_q_heads,
+                      double scale, double* out, int num_threads) {
+    if (fmt != OR_E4M3 && fmt != OR_INT8) return -1;
+    if (fmt == OR_INT8 && (!k_scales || !v_scales)) return -1;
+    return run_decode(q, k_codes, v_codes, dtype, fmt, k_scales, v_scales, fp8_k_scale,
+                      fp8_v_scale, num_blocks, block_size, num_kv_heads, head_dim,
+                      block_tables, max_blocks_per_seq, seq_lens, batch, num_q_heads, scale,
+                      out, num_threads);
 }
