@@ -41,7 +41,9 @@
  *     set in the pool's device error word, and kv_pool_get_error reports it.
  *   - Element types: q, out, new K/V rows and the pools all use the pool's
  *     kv_dtype.  Arithmetic in attention is fp32; one rounding to the output
- *     type at the end (round to nearest even).
+ *     type at the end (round to nearest even).  An 8-bit pool
+ *     (kv_pool_create_quantized) stores K and V as FP8 or INT8 codes while q,
+ *     out and the new K/V rows keep a 16-bit type.
  *   - Devices: a pool belongs to the device that was current when it was
  *     created; every call on it must be made with that device current.
  */
@@ -64,7 +66,13 @@ typedef enum {
     KV_ENOWORKSPACE = 5   /* workspace too small (see the size query)          */
 } kv_status;
 
-typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype;
+typedef enum {
+    KV_F32 = 0,
+    KV_F16 = 1,
+    KV_BF16 = 2,
+    KV_FP8_E4M3 = 3,  /* 8-bit pools only (kv_pool_create_quantized)            */
+    KV_INT8 = 4       /* 8-bit pools only (kv_pool_create_quantized)            */
+} kv_dtype;
 
 /* Bits of the device error word (kv_pool_get_error). */
 #define KV_DEVERR_SLOT_RANGE   0x1  /* kv_append: slot >= num_blocks*block_size     */
@@ -94,6 +102,39 @@ typedef struct kv_pool* kv_pool_t;
 kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
                          kv_dtype dtype, void* k_pool, void* v_pool, kv_pool_t* out);
 
+/*
+ * kv_pool_create_quantized -- describe an 8-bit KV block pool ("Part 3: single
+ * node", random-liu.github.io, ch. 10: K and V are scaled and rounded to 8
+ * bits when a token is written and turned back into wider numbers when the
+ * attention reads them; INT8 with a fine-grained per-token scale, FP8 as a
+ * shorter float).
+ *
+ * cache_dtype: KV_FP8_E4M3 or KV_INT8.  dtype: KV_F16 or KV_BF16, the type of
+ *   q, out and of the new K/V rows given to kv_append.
+ * k_pool, v_pool: device uint8 [num_blocks, block_size, num_kv_heads,
+ *   head_dim] (one code per element), 16-byte aligned.
+ * KV_FP8_E4M3: code = E4M3(x / scale) with the division in fp32, rounded to
+ *   nearest (ties to even) and saturated to +-448 (infinities included; NaN
+ *   stays NaN); value = E4M3 value of the code * scale.  k_scale / v_scale are
+ *   the pool's K and V scales (finite, > 0); k_scales, v_scales must be NULL.
+ * KV_INT8: one scale per (block, KV head, token row), decided when the row is
+ *   written: amax = max |x| over its head_dim elements, inv = 127 / amax and
+ *   scale = amax / 127 in fp32, code = x * inv rounded to nearest even and
+ *   clipped to [-127, 127]; value = code * scale.  An all-zero row has scale 0;
+ *   a row holding NaN or an infinity gets scale NaN and codes 0.  k_scales,
+ *   v_scales: device fp32 [num_blocks, num_kv_heads, block_size], 16-byte
+ *   aligned, owned by the caller; k_scale and v_scale are ignored.
+ * Limits: head_dim 128; block_size a multiple of 16, at most 256; the rest as
+ *   kv_pool_create.  copy_blocks moves codes and INT8 scales together; decode
+ *   computes with the dequantised values (fp32 scores and softmax, as for
+ *   16-bit pools).  paged_attention_decode_cascade decodes 8-bit pools plainly.
+ * Errors: KV_EINVAL, KV_EUNSUPPORTED, KV_ECUDA.
+ */
+kv_status kv_pool_create_quantized(int num_blocks, int block_size, int num_kv_heads,
+                                   int head_dim, kv_dtype cache_dtype, kv_dtype dtype,
+                                   void* k_pool, void* v_pool, float* k_scales, float* v_scales,
+                                   float k_scale, float v_scale, kv_pool_t* out);
+
 /* kv_pool_destroy -- free the handle and its error word (not the pools).
  * Work already queued with the handle must have finished.  NULL is a no-op. */
 kv_status kv_pool_destroy(kv_pool_t pool);
@@ -102,7 +143,9 @@ kv_status kv_pool_destroy(kv_pool_t pool);
  * kv_append -- write each new token's K and V row into its slot
  * ("Part 3: single node", ch. 13 sec. 1: kv_cache[slot_mapping[i]] = new_kv).
  *
- * k_new, v_new: device [num_tokens, num_kv_heads, head_dim] of the pool dtype.
+ * k_new, v_new: device [num_tokens, num_kv_heads, head_dim] of the pool dtype
+ *   (of the pool's 16-bit type for an 8-bit pool, whose rows are quantised as
+ *   kv_pool_create_quantized describes).
  * slot_mapping: device int64 [num_tokens]; slot = block * block_size + offset.
  *   A negative slot is padding and is skipped.  A slot >= num_blocks *
  *   block_size is skipped and sets KV_DEVERR_SLOT_RANGE.

@@ -48,8 +48,9 @@ bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p, bool swizzl
     const cuuint32_t inner = swizzled ? (cuuint32_t)(128 / elt) : (cuuint32_t)p.head_dim;
     cuuint32_t box[3] = {inner, 1u, (cuuint32_t)p.block_size};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUtensorMapDataType dt =
-        p.elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const CUtensorMapDataType dt = p.elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : p.elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     return enc(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -82,7 +83,10 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     }
     const int G = num_q_heads / pool.num_kv_heads;
     const int D = pool.head_dim, bs = pool.block_size, elt = pool.elem_bytes;
-    const size_t stage = 2ull * bs * D * elt;
+    const bool q8 = is_q8(pool);
+    const int sb = pool.cache_dtype == KV_INT8 ? 4 : 0;     // scale bytes per tile row
+    const int cvt = q8 ? 16 * D * 2 : 0;                    // f16 tile per consumer warp
+    const size_t stage = 2ull * bs * D * elt + 2ull * bs * sb;
     // Ring depth S is a multiple of the consumer-warp count (each stage has a
     // fixed consumer).  Pick the S with the most (resident CTAs x stages per
     // warp, the latter counted up to 2), then the deepest ring.
@@ -92,13 +96,18 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     for (int S = ncw; S <= 8 * ncw; S += ncw) {
         if (S > ncw && (size_t)S * stage > kMaxRingBytes) break;
         // + 1 KB: the kernel rounds its shared-memory base up to 1 KB
-        const size_t smem = dec::Layout(S, batch, bs, G, D, elt, num_groups).total + 1024;
+        const size_t smem = dec::Layout(S, batch, bs, G, D, elt, num_groups, sb, cvt).total + 1024;
         if (smem > kMaxSmem) break;
         int occ = 0;
         cudaError_t e = cudaErrorNotSupported;
-        if (pool.dtype == KV_F32) e = decode_attrs_f32(pool, G, smem, &occ);
-        if (pool.dtype == KV_F16) e = decode_attrs_f16(pool, G, smem, &occ);
-        if (pool.dtype == KV_BF16) e = decode_attrs_bf16(pool, G, smem, &occ);
+        if (q8) {
+            if (pool.dtype == KV_F16) e = decode_attrs_q8_f16(pool, G, smem, &occ);
+            if (pool.dtype == KV_BF16) e = decode_attrs_q8_bf16(pool, G, smem, &occ);
+        } else {
+            if (pool.dtype == KV_F32) e = decode_attrs_f32(pool, G, smem, &occ);
+            if (pool.dtype == KV_F16) e = decode_attrs_f16(pool, G, smem, &occ);
+            if (pool.dtype == KV_BF16) e = decode_attrs_bf16(pool, G, smem, &occ);
+        }
         if (e != cudaSuccess) return e;
         const int per_warp = S / ncw > 2 ? 2 : S / ncw;
         const int score = occ * per_warp;
@@ -136,6 +145,11 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
 
 cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
                           cudaStream_t stream) {
+    if (is_q8(pool)) {
+        if (pool.dtype == KV_F16) return decode_dispatch_q8_f16(pool, call, plan, stream);
+        if (pool.dtype == KV_BF16) return decode_dispatch_q8_bf16(pool, call, plan, stream);
+        return cudaErrorNotSupported;
+    }
     switch (pool.dtype) {
         case KV_F32: return decode_dispatch_f32(pool, call, plan, stream);
         case KV_F16: return decode_dispatch_f16(pool, call, plan, stream);
@@ -148,17 +162,27 @@ cudaError_t launch_decode(const kv_pool& pool, const DecodeCall& call, const Dec
 
 extern "C" {
 
+// Geometry checks shared by both pool constructors.
+static kv_status check_geometry(int num_blocks, int block_size, int num_kv_heads, void* k_pool,
+                                void* v_pool) {
+    if (num_blocks < 1 || block_size < 1 || block_size > 256 || num_kv_heads < 1 ||
+        num_kv_heads > 1024)
+        return KV_EINVAL;
+    if ((long long)num_blocks * block_size >= (1ll << 31)) return KV_EINVAL;
+    if (!k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool)) return KV_EINVAL;
+    return KV_OK;
+}
+
+static kv_status finish_pool(kv_pool* p, kv_pool_t* out);
+
 kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
                          kv_dtype dtype, void* k_pool, void* v_pool, kv_pool_t* out) {
     if (!out) return KV_EINVAL;
     *out = nullptr;
     if (dtype != KV_F32 && dtype != KV_F16 && dtype != KV_BF16) return KV_EUNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return KV_EUNSUPPORTED;
-    if (num_blocks < 1 || block_size < 1 || block_size > 256 || num_kv_heads < 1 ||
-        num_kv_heads > 1024)
-        return KV_EINVAL;
-    if ((long long)num_blocks * block_size >= (1ll << 31)) return KV_EINVAL;
-    if (!k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool)) return KV_EINVAL;
+    kv_status st = check_geometry(num_blocks, block_size, num_kv_heads, k_pool, v_pool);
+    if (st != KV_OK) return st;
     kv_pool* p = new (std::nothrow) kv_pool();
     if (!p) return KV_EINVAL;
     p->num_blocks = num_blocks;
@@ -166,9 +190,58 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
     p->num_kv_heads = num_kv_heads;
     p->head_dim = head_dim;
     p->dtype = dtype;
+    p->cache_dtype = dtype;
     p->elem_bytes = elem_bytes(dtype);
     p->k = k_pool;
     p->v = v_pool;
+    return finish_pool(p, out);
+}
+
+kv_status kv_pool_create_quantized(int num_blocks, int block_size, int num_kv_heads,
+                                   int head_dim, kv_dtype cache_dtype, kv_dtype dtype,
+                                   void* k_pool, void* v_pool, float* k_scales, float* v_scales,
+                                   float k_scale, float v_scale, kv_pool_t* out) {
+    if (!out) return KV_EINVAL;
+    *out = nullptr;
+    if (cache_dtype != KV_FP8_E4M3 && cache_dtype != KV_INT8) return KV_EUNSUPPORTED;
+    if (dtype != KV_F16 && dtype != KV_BF16) return KV_EUNSUPPORTED;
+    if (head_dim != 128 || block_size % 16 != 0) return KV_EUNSUPPORTED;
+    kv_status st = check_geometry(num_blocks, block_size, num_kv_heads, k_pool, v_pool);
+    if (st != KV_OK) return st;
+    if (cache_dtype == KV_INT8) {
+        if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
+            return KV_EINVAL;
+    } else {
+        if (k_scales || v_scales) return KV_EINVAL;
+        if (!(k_scale > 0.f && k_scale <= 3.4e38f) || !(v_scale > 0.f && v_scale <= 3.4e38f))
+            return KV_EINVAL;
+    }
+    kv_pool* p = new (std::nothrow) kv_pool();
+    if (!p) return KV_EINVAL;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->num_kv_heads = num_kv_heads;
+    p->head_dim = head_dim;
+    p->dtype = dtype;
+    p->cache_dtype = cache_dtype;
+    p->elem_bytes = 1;
+    p->k = k_pool;
+    p->v = v_pool;
+    if (cache_dtype == KV_INT8) {
+        p->k_scales = k_scales;
+        p->v_scales = v_scales;
+    } else {
+        p->fp8_k_scale = k_scale;
+        p->fp8_v_scale = v_scale;
+    }
+    return finish_pool(p, out);
+}
+
+// Device, error word and tensor maps of a filled-in pool; frees it on failure.
+static kv_status finish_pool(kv_pool* p, kv_pool_t* out) {
+    const int head_dim = p->head_dim, block_size = p->block_size;
+    void* k_pool = p->k;
+    void* v_pool = p->v;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);

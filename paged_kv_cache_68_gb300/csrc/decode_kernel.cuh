@@ -51,6 +51,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 #include <type_traits>
@@ -93,14 +94,22 @@ struct Params {
     int num_groups;
     const float* pst_o;    // [batch][num_q_heads][D], normalised
     const float* pst_lse;  // [batch][num_q_heads], log2-sum-exp
+    // 8-bit pools: INT8 scales per (block, KV head, token), FP8 scales per pool
+    const float* k_scales; // [num_blocks][num_kv_heads][bs]
+    const float* v_scales;
+    float fp8_k_scale, fp8_v_scale;
 };
 
 // ---------------------------------------------------------------- layout ---
 struct Layout {
-    uint32_t full, empty, valid, misc, prefix, groups, skip, pst, pbuf, abuf, merge_o, merge_ml, ring;
-    uint32_t stage_bytes, total;
-    // K: cascade groups (0 for plain decode)
-    __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt, int K = 0) {
+    uint32_t full, empty, valid, misc, prefix, groups, skip, pst, pbuf, abuf, merge_o, merge_ml, cvt,
+        ring;
+    uint32_t tx_bytes, stage_bytes, total;
+    // elt: bytes per pool element; K: cascade groups (0 for plain decode);
+    // sb: scale bytes per token row of a tile (INT8 pools: 4); cvt_warp: bytes
+    // of each consumer warp's conversion tile (8-bit pools)
+    __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt, int K = 0, int sb = 0,
+                               int cvt_warp = 0) {
         uint32_t off = 0;
         full = off;   off += 8u * S;
         empty = off;  off += 8u * S;
@@ -116,8 +125,11 @@ struct Layout {
         merge_o = off;  off += 4u * (NCW - 1) * G * D;
         merge_ml = off; off += 2u * 4u * (NCW - 1) * G;
         off = (off + 1023u) & ~1023u;              // swizzle atoms are 1 KB
+        cvt = off;    off += (uint32_t)NCW * (((uint32_t)cvt_warp + 1023u) & ~1023u);
         ring = off;
-        stage_bytes = 2u * bs * D * elt;         // K tile then V tile, 128-byte multiples
+        // K tile, V tile, then (INT8) the K and V scales of the tile's rows
+        tx_bytes = 2u * bs * D * elt + 2u * bs * sb;
+        stage_bytes = (tx_bytes + 127u) & ~127u;
         off += stage_bytes * S;
         total = off;
     }
@@ -167,6 +179,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing on the mbarrier like a tile load.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 // Named barriers among the NCW consumer warps (id 0 is __syncthreads).
@@ -432,6 +453,9 @@ struct CorePolicy {
     using C = Cfg<T, D, G>;
     static constexpr bool kSwizzled = false;
     static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
+    static constexpr int kKvBytes = sizeof(T);   // pool element
+    static constexpr int kScaleBytes = 0;
+    static constexpr int kCvtBytes = 0;
 
     float2* pb;                   // this warp's (score | p, p) [bs][G]
     float2* ab;                   // this warp's (alpha, alpha) [G]
@@ -440,6 +464,7 @@ struct CorePolicy {
     float m_run, l_run;           // for head lane % G
 
     __device__ __forceinline__ CorePolicy(float2* pbuf, float2* abuf) : pb(pbuf), ab(abuf) {}
+    __device__ __forceinline__ void setup(const Params&, unsigned char*) {}
 
     __device__ __forceinline__ void begin(const T* qp, float qscale, int lane) {
         const int jl = lane % C::TPT;
@@ -638,9 +663,12 @@ template <typename T, int D, int G, int BSC>
 struct TcPolicy {
     static_assert(sizeof(T) == 2, "tensor-core path takes 16-bit pools");
     static_assert(BSC % 16 == 0 && BSC > 0, "tensor-core path needs a block size of 16k");
-    static_assert(G == 4 || G == 8, "tensor-core path fills N = 8 with 4 or 8 heads");
+    static_assert(G >= 1 && G <= 8, "the group's heads fill N = 8");
     static constexpr bool kSwizzled = true;
     static constexpr int kMinBlocks = 3;
+    static constexpr int kKvBytes = sizeof(T);
+    static constexpr int kScaleBytes = 0;
+    static constexpr int kCvtBytes = 0;
     static constexpr int KS = D / 16;      // QK k-steps (16 dims each)
     static constexpr int MT = D / 16;      // PV m-tiles (16 dims each)
     static constexpr int TT = BSC / 16;    // 16-token tiles per block
@@ -650,6 +678,7 @@ struct TcPolicy {
     float m_run[2], l_run[2];              // heads 2 tig, 2 tig + 1
 
     __device__ __forceinline__ TcPolicy(float2*, float2*) {}
+    __device__ __forceinline__ void setup(const Params&, unsigned char*) {}
 
     // Shared address of 16-byte chunk c of row r in a 128-byte-swizzled tile
     // of `rows` rows (chunks 0-7 in the first 128-byte half, 8-15 in the second).
@@ -838,6 +867,254 @@ struct TcPolicy {
             if (!po.complete && gid == 0)
                 po.part_lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
         }
+    }
+};
+
+// ---------------------------------------------------- 8-bit pools on MMA --
+// K/V stored as 8-bit codes ("Part 3: single node", random-liu.github.io,
+// ch. 10: a token's K and V are scaled and rounded to 8 bits when written and
+// turned back into wider numbers when read): FP8 E4M3 with one scale per pool,
+// or INT8 with one fp32 scale per (block, KV head, token row).  The tiles
+// arrive unswizzled, one byte per element (INT8: the tile's K and V scales
+// follow them in the stage).  Each consumer warp converts a 16-token tile of
+// codes to f16 -- exactly: every E4M3 value and every integer in [-128, 127]
+// is an f16 -- into its own 128-byte-swizzled shared tile and runs the
+// tensor-core policy's MMAs on it (f16 x f16 -> fp32).  The scales never pass
+// through f16:
+//   * Q is held as f16 * 2^e (a power of two per piece keeps the group's
+//     largest |q| below 2^15; bf16 and f16 queries convert exactly), and the
+//     score of token t is acc * scale * log2(e) * 2^-e * kscale_t in fp32;
+//   * P is multiplied by vscale_t / vref before its hi + lo f16 split, vref
+//     the tile's largest V scale, and the accumulator is kept as O / R with R
+//     the last tile's vref (a change of R rescales it with the softmax alpha).
+// The MMA type is f16 whatever the query type; outputs use the query type.
+constexpr int kFmtE4M3 = 0;
+constexpr int kFmtInt8 = 1;
+
+template <int FMT>
+__device__ __forceinline__ void codes16_to_f16(uint4 w, uint4& lo, uint4& hi) {
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[8];
+    if constexpr (FMT == kFmtE4M3) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(
+                (__nv_fp8x2_storage_t)(in[i] & 0xffffu), __NV_E4M3);
+            const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(
+                (__nv_fp8x2_storage_t)(in[i] >> 16), __NV_E4M3);
+            o[2 * i] = (uint32_t)a.x | ((uint32_t)a.y << 16);
+            o[2 * i + 1] = (uint32_t)b.x | ((uint32_t)b.y << 16);
+        }
+    } else {
+        // two's complement byte b -> f16 (1024 + (b ^ 0x80)) - 1152 = b, exactly
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t x = in[i] ^ 0x80808080u;
+            const uint32_t l = __byte_perm(x, 0x64646464u, 0x7150);
+            const uint32_t h = __byte_perm(x, 0x64646464u, 0x7352);
+            const __half2 lh = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
+            const __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+            o[2 * i] = *reinterpret_cast<const uint32_t*>(&lh);
+            o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <typename T, int D, int G, int FMT>
+struct Tc8Policy : TcPolicy<T, D, G, 16> {
+    using Base = TcPolicy<T, D, G, 16>;
+    static constexpr int KS = Base::KS;
+    static constexpr int MT = Base::MT;
+    static constexpr bool kSwizzled = false;
+    static constexpr int kMinBlocks = 3;
+    static constexpr int kKvBytes = 1;
+    static constexpr int kScaleBytes = FMT == kFmtInt8 ? 4 : 0;
+    static constexpr int kCvtBytes = 16 * D * 2;   // one 16-token f16 tile per warp
+
+    unsigned char* cvt;   // this warp's f16 tile [16][D], 128-byte swizzled halves
+    float qs;             // scale * log2(e) * 2^-e (* the FP8 K scale)
+    float vq;             // FP8: the V scale; INT8: 1
+    float kq;             // FP8: the K scale; INT8: 1
+    float R;              // the accumulators hold O / R
+
+    __device__ __forceinline__ Tc8Policy(float2* a, float2* b) : Base(a, b) {}
+
+    __device__ __forceinline__ void setup(const Params& p, unsigned char* buf) {
+        cvt = buf;
+        kq = FMT == kFmtE4M3 ? p.fp8_k_scale : 1.f;
+        vq = FMT == kFmtE4M3 ? p.fp8_v_scale : 1.f;
+    }
+
+    __device__ static __forceinline__ uint32_t swz16(uint32_t tile, int r, int c) {
+        return tile + (uint32_t)((c >> 3) * 16 * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
+
+    __device__ __forceinline__ void begin(const T* qp, float qscale, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+        float2 qf[KS][2];
+        float amax = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t raw = gid < G ? __ldg(reinterpret_cast<const uint32_t*>(
+                                                   qp + gid * D + ks * 16 + j * 8 + tig * 2))
+                                             : 0u;
+                qf[ks][j] = Mma<T>::unpack(raw);
+                amax = fmaxf(amax, fmaxf(fabsf(qf[ks][j].x), fabsf(qf[ks][j].y)));
+            }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, off));
+        // 2^e with amax * 2^e in [2^14, 2^15): exponent field of amax, clamped
+        int e = 0;
+        if (amax > 0.f && amax <= 3.0e38f) {
+            const int ex = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 126;   // amax < 2^ex
+            e = min(max(15 - ex, -120), 120);
+        }
+        const float up = __uint_as_float((uint32_t)(e + 127) << 23);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const __half2 h = __floats2half2_rn(qf[ks][j].x * up, qf[ks][j].y * up);
+                this->qb[ks][j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+        qs = qscale * kq * __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            this->oacc[mt][0] = this->oacc[mt][1] = this->oacc[mt][2] = this->oacc[mt][3] = 0.f;
+        this->m_run[0] = this->m_run[1] = -CUDART_INF_F;
+        this->l_run[0] = this->l_run[1] = 0.f;
+        R = vq;
+    }
+
+    // Rows r < keep of the 16-row code tile at `src` -> f16 in cvt; rows >= keep -> 0.
+    __device__ __forceinline__ void convert(const unsigned char* src, int keep, int lane) const {
+        constexpr int CPR = D / 16;                 // 16-byte code chunks per row
+#pragma unroll 1
+        for (int i = lane; i < 16 * CPR; i += 32) {
+            const int r = i / CPR, c = i % CPR;
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (r < keep) codes16_to_f16<FMT>(*reinterpret_cast<const uint4*>(src + r * D + c * 16), lo, hi);
+            const int c0 = 2 * c, c1 = 2 * c + 1;
+            *reinterpret_cast<uint4*>(cvt + (c0 >> 3) * 2048 + r * 128 + (((c0 & 7) ^ (r & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(cvt + (c1 >> 3) * 2048 + r * 128 + (((c1 & 7) ^ (r & 7)) << 4)) = hi;
+        }
+    }
+
+    __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
+                                          int n_valid, int bs, float, int lane) {
+        const int gid = lane >> 2, mi = lane >> 3, r8 = lane & 7;
+        const uint32_t cb = smem_u32(cvt);
+        const float* ksc = reinterpret_cast<const float*>(Vs + bs * D);   // INT8 only
+        const float* vsc = ksc + bs;
+        for (int t0 = 0; t0 < n_valid; t0 += 16) {
+            // -- S^T of the tile: 16 tokens x the group's heads ---------------
+            convert(Ks + t0 * D, 16, lane);
+            __syncwarp();
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(a, swz16(cb, (mi & 1) * 8 + r8, ks * 2 + (mi >> 1)));
+                Mma<__half>::run(acc[ks & 1], a, this->qb[ks][0], this->qb[ks][1]);
+            }
+            __syncwarp();                             // the tile is read; V may overwrite it
+            const int ta = t0 + gid, tb = ta + 8;
+            const bool v0 = ta < n_valid, v1 = tb < n_valid;
+            float fa = qs, fb = qs;
+            if constexpr (FMT == kFmtInt8) {
+                fa *= v0 ? ksc[ta] : 0.f;
+                fb *= v1 ? ksc[tb] : 0.f;
+            }
+            float s[4];
+            s[0] = v0 ? (acc[0][0] + acc[1][0]) * fa : -CUDART_INF_F;
+            s[1] = v0 ? (acc[0][1] + acc[1][1]) * fa : -CUDART_INF_F;
+            s[2] = v1 ? (acc[0][2] + acc[1][2]) * fb : -CUDART_INF_F;
+            s[3] = v1 ? (acc[0][3] + acc[1][3]) * fb : -CUDART_INF_F;
+            // -- online softmax, heads 2 tig (j = 0) and 2 tig + 1 (j = 1) -----
+            float alpha[2], mnew[2], lsum[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mx = fmaxf(s[j], s[j + 2]);
+                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+                mnew[j] = fmaxf(this->m_run[j], mx);
+                alpha[j] = mnew[j] == -CUDART_INF_F ? 1.f : fast_exp2(this->m_run[j] - mnew[j]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = e & 1;
+                const float pe = mnew[j] == -CUDART_INF_F ? 0.f : fast_exp2(s[e] - mnew[j]);
+                s[e] = pe;
+                lsum[j] += pe;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                lsum[j] += __shfl_xor_sync(FULL, lsum[j], 4);
+                lsum[j] += __shfl_xor_sync(FULL, lsum[j], 8);
+                lsum[j] += __shfl_xor_sync(FULL, lsum[j], 16);
+                this->l_run[j] = this->l_run[j] * alpha[j] + lsum[j];
+                this->m_run[j] = mnew[j];
+            }
+            // -- V scales: P' = P * vscale_t / vref, accumulators kept as O / vref --
+            float vref = R, wa = 1.f, wb = 1.f;
+            if constexpr (FMT == kFmtInt8) {
+                const float sa = v0 ? vsc[ta] : 0.f, sb = v1 ? vsc[tb] : 0.f;
+                float mx = fmaxf(sa, sb);
+#pragma unroll
+                for (int off = 16; off >= 4; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+                if (mx > 0.f) {
+                    vref = mx;
+                    wa = sa / mx;
+                    wb = sb / mx;
+                } else {
+                    wa = wb = 0.f;                    // the tile's V rows are all zero
+                }
+            }
+            const float rf = R / vref;
+            R = vref;
+            const float2 a2 = make_float2(alpha[0] * rf, alpha[1] * rf);
+            if (!__all_sync(FULL, a2.x == 1.f && a2.y == 1.f))
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const float2 lo = __fmul2_rn(make_float2(this->oacc[mt][0], this->oacc[mt][1]), a2);
+                const float2 hi = __fmul2_rn(make_float2(this->oacc[mt][2], this->oacc[mt][3]), a2);
+                this->oacc[mt][0] = lo.x; this->oacc[mt][1] = lo.y;
+                this->oacc[mt][2] = hi.x; this->oacc[mt][3] = hi.y;
+            }
+            s[0] *= wa; s[1] *= wa; s[2] *= wb; s[3] *= wb;
+            // -- O^T += V_tile^T P'^T, P' as hi + lo f16 halves -----------------
+            convert(Vs + t0 * D, n_valid - t0, lane);
+            __syncwarp();
+            const uint32_t h01 = Mma<__half>::pack(s[0], s[1]), h23 = Mma<__half>::pack(s[2], s[3]);
+            const float2 f01 = Mma<__half>::unpack(h01), f23 = Mma<__half>::unpack(h23);
+            const uint32_t l01 = Mma<__half>::pack(s[0] - f01.x, s[1] - f01.y);
+            const uint32_t l23 = Mma<__half>::pack(s[2] - f23.x, s[3] - f23.y);
+            const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
+            const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_t(a, swz16(cb, (mi >> 1) * 8 + r8, mt * 2 + (mi & 1)));
+                Mma<__half>::run(this->oacc[mt], a, bh0, bh1);
+                Mma<__half>::run(this->oacc[mt], a, bl0, bl1);
+            }
+            __syncwarp();                             // before the next tile's K overwrites it
+        }
+    }
+
+    // Before the warp merge: the accumulators become O itself.
+    __device__ __forceinline__ void fold(int) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) this->oacc[mt][i] *= R;
+        R = 1.f;
     }
 };
 
@@ -1059,12 +1336,12 @@ template <typename T, int D, int G, class Pol>
 __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
-    constexpr int ELT = sizeof(T);
+    constexpr int ELT = Pol::kKvBytes;             // bytes per pool element
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int B = p.batch, S = p.stages, H = p.num_kv_heads, bs = p.bs;
-    const Layout lay(S, B, bs, G, D, ELT, p.num_groups);
+    const Layout lay(S, B, bs, G, D, ELT, p.num_groups, Pol::kScaleBytes, Pol::kCvtBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
@@ -1174,14 +1451,21 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                     const uint32_t fb = smem_u32(&full[s]);
                     if (ok && id >= 0 && id < p.num_blocks) {
                         valid[s] = 1;
-                        mbar_arrive_tx(fb, lay.stage_bytes);
+                        mbar_arrive_tx(fb, lay.tx_bytes);
                         const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
+                        const uint32_t vdst = dst + (uint32_t)(bs * D * ELT);
 #pragma unroll
                         for (int x = 0; x < kBoxes; ++x) {
                             const int col = x * (int)(128 / ELT);
                             tma_load_3d(dst + x * box_bytes, &tmap_k, col, gg, id * bs, fb);
-                            tma_load_3d(dst + lay.stage_bytes / 2 + x * box_bytes, &tmap_v, col, gg,
-                                        id * bs, fb);
+                            tma_load_3d(vdst + x * box_bytes, &tmap_v, col, gg, id * bs, fb);
+                        }
+                        if constexpr (Pol::kScaleBytes > 0) {
+                            const size_t srow = ((size_t)id * H + gg) * bs;
+                            const uint32_t sdst = dst + (uint32_t)(2 * bs * D * ELT);
+                            bulk_load(sdst, p.k_scales + srow, (uint32_t)bs * 4u, fb);
+                            bulk_load(sdst + (uint32_t)bs * 4u, p.v_scales + srow, (uint32_t)bs * 4u,
+                                      fb);
                         }
                     } else {
                         valid[s] = 0;
@@ -1213,6 +1497,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     const T* qbase = static_cast<const T*>(p.q);
     T* obase = static_cast<T*>(p.out);
     Pol pol(pb, ab);
+    pol.setup(p, smem + lay.cvt + (size_t)w * ((Pol::kCvtBytes + 1023) & ~1023));
 
     bool first_piece = true;
     for (int u = start; u < end;) {
@@ -1251,7 +1536,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
             if (ok && valid[s]) {
                 const int j = skip + j0 + (uu - u);
                 const unsigned char* Ks = ring + (size_t)s * lay.stage_bytes;
-                pol.block(Ks, Ks + lay.stage_bytes / 2, min(bs, Lb - j * bs), bs, p.qscale, lane);
+                pol.block(Ks, Ks + bs * D * ELT, min(bs, Lb - j * bs), bs, p.qscale, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
@@ -1345,6 +1630,10 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.num_groups = call.num_groups;
     p.pst_o = call.pst_o;
     p.pst_lse = call.pst_lse;
+    p.k_scales = pool.k_scales;
+    p.v_scales = pool.v_scales;
+    p.fp8_k_scale = pool.fp8_k_scale;
+    p.fp8_v_scale = pool.fp8_v_scale;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.num_ctas);
     cfg.blockDim = dim3(NTHREADS);
@@ -1432,6 +1721,42 @@ cudaError_t attrs(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm)
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
 #undef PKV_CASE
+    return cudaErrorNotSupported;
+}
+
+// 8-bit pools: Tc8Policy for head_dim 128, block sizes that are multiples of
+// 16, groups of 1, 2, 4 or 8 (T = the query / output type).
+inline bool q8_shape_ok(const kv_pool& pool) {
+    return pool.head_dim == 128 && pool.block_size % 16 == 0 && pool.block_size <= 256;
+}
+
+template <typename T, int FMT, template <typename, int, int, class> class Fn, typename... A>
+cudaError_t with_q8_policy(int G, A... args) {
+    if (G == 1) return Fn<T, 128, 1, Tc8Policy<T, 128, 1, FMT>>::run(args...);
+    if (G == 2) return Fn<T, 128, 2, Tc8Policy<T, 128, 2, FMT>>::run(args...);
+    if (G == 4) return Fn<T, 128, 4, Tc8Policy<T, 128, 4, FMT>>::run(args...);
+    if (G == 8) return Fn<T, 128, 8, Tc8Policy<T, 128, 8, FMT>>::run(args...);
+    return cudaErrorNotSupported;
+}
+
+template <typename T>
+cudaError_t dispatch_q8(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
+                        cudaStream_t stream) {
+    if (!q8_shape_ok(pool)) return cudaErrorNotSupported;
+    if (pool.cache_dtype == KV_FP8_E4M3)
+        return with_q8_policy<T, kFmtE4M3, LaunchFn>(plan.group, &pool, &call, &plan, stream);
+    if (pool.cache_dtype == KV_INT8)
+        return with_q8_policy<T, kFmtInt8, LaunchFn>(plan.group, &pool, &call, &plan, stream);
+    return cudaErrorNotSupported;
+}
+
+template <typename T>
+cudaError_t attrs_q8(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm) {
+    if (!q8_shape_ok(pool)) return cudaErrorNotSupported;
+    if (pool.cache_dtype == KV_FP8_E4M3)
+        return with_q8_policy<T, kFmtE4M3, AttrsFn>(group, smem, ctas_per_sm);
+    if (pool.cache_dtype == KV_INT8)
+        return with_q8_policy<T, kFmtInt8, AttrsFn>(group, smem, ctas_per_sm);
     return cudaErrorNotSupported;
 }
 

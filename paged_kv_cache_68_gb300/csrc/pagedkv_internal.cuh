@@ -26,10 +26,15 @@ struct kv_pool {
     int block_size;
     int num_kv_heads;
     int head_dim;
-    kv_dtype dtype;
-    int elem_bytes;
+    kv_dtype dtype;         // q, out and new K/V rows
+    kv_dtype cache_dtype;   // the pool's elements: dtype, or KV_FP8_E4M3 / KV_INT8
+    int elem_bytes;         // bytes per pool element
     void* k;
     void* v;
+    float* k_scales = nullptr;   // KV_INT8: [num_blocks][num_kv_heads][block_size]
+    float* v_scales = nullptr;
+    float fp8_k_scale = 1.f;     // KV_FP8_E4M3: per-pool scales
+    float fp8_v_scale = 1.f;
     int* d_err;             // device error word (KV_DEVERR_* bits)
     CUtensorMap tmap_k;     // 3-D {head_dim, num_kv_heads, num_blocks*block_size},
     CUtensorMap tmap_v;     //   box {head_dim, 1, block_size}, no swizzle
@@ -111,5 +116,14 @@ cudaError_t decode_dispatch_bf16(const kv_pool&, const DecodeCall&, const Decode
 cudaError_t decode_attrs_f32(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
 cudaError_t decode_attrs_f16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
 cudaError_t decode_attrs_bf16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
+// 8-bit pools, by query type
+cudaError_t decode_dispatch_q8_f16(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
+cudaError_t decode_dispatch_q8_bf16(const kv_pool&, const DecodeCall&, const DecodePlan&, cudaStream_t);
+cudaError_t decode_attrs_q8_f16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
+cudaError_t decode_attrs_q8_bf16(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm);
+
+inline bool is_q8(const kv_pool& pool) {
+    return pool.cache_dtype == KV_FP8_E4M3 || pool.cache_dtype == KV_INT8;
+}
 
 }  // namespace pagedkv

@@ -6,6 +6,7 @@ There is no fallback: if the library cannot be built or loaded, or a call
 fails, an exception is raised.
 
 The module-level functions carry the C names (``kv_pool_create``,
+``kv_pool_create_quantized``,
 ``kv_append``, ``copy_blocks``, ``paged_attention_workspace_size``,
 ``paged_attention_decode``, ``paged_attention_cascade_workspace_size``,
 ``paged_attention_decode_cascade``, ``paged_attention_decode_noalloc``,
@@ -33,6 +34,8 @@ KV_DEVERR_TIMEOUT = 0x10
 KV_DEVERR_GROUP_RANGE = 0x20
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+KV_FP8_E4M3, KV_INT8 = 3, 4
+CACHE_CODE = {"fp8_e4m3": KV_FP8_E4M3, "int8": KV_INT8}
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -65,6 +68,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         sig = {
             "kv_pool_create": ([I, I, I, I, I, P, P, ctypes.POINTER(P)], I),
+            "kv_pool_create_quantized": ([I, I, I, I, I, I, P, P, P, P, F, F, ctypes.POINTER(P)], I),
             "kv_pool_destroy": ([P], I),
             "kv_append": ([P, P, P, P, I, P], I),
             "copy_blocks": ([P, P, I, P], I),
@@ -120,6 +124,33 @@ def kv_pool_create(k_pool: torch.Tensor, v_pool: torch.Tensor) -> ctypes.c_void_
     _check(load().kv_pool_create(n, bs, hkv, d, DTYPE_CODE[k_pool.dtype],
                                  _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), ctypes.byref(h)),
            "kv_pool_create")
+    return h
+
+
+def kv_pool_create_quantized(k_codes: torch.Tensor, v_codes: torch.Tensor, dtype, cache: str,
+                             k_scales: Optional[torch.Tensor] = None,
+                             v_scales: Optional[torch.Tensor] = None, k_scale: float = 1.0,
+                             v_scale: float = 1.0) -> ctypes.c_void_p:
+    """Describe an 8-bit pool: uint8 codes [num_blocks, block_size, num_kv_heads,
+    head_dim]; ``cache`` "fp8_e4m3" (per-pool scales k_scale, v_scale) or
+    "int8" (fp32 scales [num_blocks, num_kv_heads, block_size]); ``dtype`` the
+    16-bit type of q, out and new K/V rows."""
+    if k_codes.shape != v_codes.shape or k_codes.dim() != 4:
+        raise ValueError("k_codes and v_codes must be equal-shaped 4-D tensors")
+    if cache not in CACHE_CODE:
+        raise ValueError(f"unknown cache format {cache!r}")
+    n, bs, hkv, d = k_codes.shape
+    ks = vs = None
+    if cache == "int8":
+        for t, name in ((k_scales, "k_scales"), (v_scales, "v_scales")):
+            if t is None or tuple(t.shape) != (n, hkv, bs):
+                raise ValueError(f"{name} must be [num_blocks, num_kv_heads, block_size]")
+        ks, vs = _dev(k_scales, "k_scales", torch.float32), _dev(v_scales, "v_scales", torch.float32)
+    h = ctypes.c_void_p()
+    _check(load().kv_pool_create_quantized(
+        n, bs, hkv, d, CACHE_CODE[cache], DTYPE_CODE[dtype], _dev(k_codes, "k_codes", torch.uint8),
+        _dev(v_codes, "v_codes", torch.uint8), ks, vs, float(k_scale), float(v_scale),
+        ctypes.byref(h)), "kv_pool_create_quantized")
     return h
 
 
@@ -200,11 +231,24 @@ def kv_pool_clear_error(handle) -> None:
 class KVPool:
     """A KV block pool (two caller-owned tensors) plus its library handle."""
 
-    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor):
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, *, cache: Optional[str] = None,
+                 dtype=None, k_scales: Optional[torch.Tensor] = None,
+                 v_scales: Optional[torch.Tensor] = None, k_scale: float = 1.0,
+                 v_scale: float = 1.0):
+        """A 16-bit or fp32 pool (k_pool, v_pool of that type), or with
+        ``cache`` set an 8-bit pool: uint8 codes, ``dtype`` the 16-bit type of
+        q / out / new rows, and the scales ``kv_pool_create_quantized`` takes."""
         self.k_pool, self.v_pool = k_pool, v_pool
-        self.dtype = k_pool.dtype
+        self.cache = cache
+        self.k_scales, self.v_scales = k_scales, v_scales
         self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim = k_pool.shape
-        self.handle = kv_pool_create(k_pool, v_pool)
+        if cache is None:
+            self.dtype = k_pool.dtype
+            self.handle = kv_pool_create(k_pool, v_pool)
+        else:
+            self.dtype = dtype
+            self.handle = kv_pool_create_quantized(k_pool, v_pool, dtype, cache, k_scales,
+                                                   v_scales, k_scale, v_scale)
         self._ws: Optional[torch.Tensor] = None
 
     def close(self) -> None:

@@ -459,3 +459,66 @@ def on_host(w: Workload) -> Workload:
     for f in _VALUE_FIELDS:
         setattr(h, f, value_to_numpy(getattr(w, f), w.dtype))
     return h
+
+
+# -- 8-bit pools ---------------------------------------------------------------
+
+@dataclass
+class Q8Pools:
+    """An 8-bit pool of a workload's geometry: uint8 codes [N, bs, Hkv, D] and,
+    for INT8, fp32 scales [N, Hkv, bs]; per-pool scales for FP8."""
+    cache: str
+    k_codes: object
+    v_codes: object
+    k_scales: object = None
+    v_scales: object = None
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    def kv_bytes(self, w: "Workload") -> int:
+        """Bytes attention reads for K and V: one byte per element, plus the
+        INT8 scales of every token row."""
+        tok = int(w.seq_lens.astype(np.int64).sum())
+        per = w.num_kv_heads * w.head_dim * 2 + (8 * w.num_kv_heads if self.cache == "int8" else 0)
+        return tok * per
+
+
+def q8_pools(w: "Workload", cache: str, seed: int, k_scale: float = 1.0,
+             v_scale: float = 1.0) -> Q8Pools:
+    """Seeded codes for the rows ``w``'s pools hold (rows that are NaN in the
+    16-bit pools stay unreadable: E4M3 NaN codes 0x7F, INT8 scales NaN).
+
+    FP8: N(0, 1) draws cast to E4M3 by torch (values like stored K/V);
+    INT8: codes round(N(0, 42)) clipped to [-127, 127], scales U(0.01, 0.04)
+    per (block, head, row).  On the device of ``w`` (numpy or CUDA torch)."""
+    import torch
+    dev = w.k_pool.device if isinstance(w.k_pool, torch.Tensor) else torch.device("cpu")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0x0C8D0000 + int(seed))
+    shape = tuple(w.k_pool.shape)
+    N, bs, H, D = shape
+
+    def filled(pool):
+        t = pool if isinstance(pool, torch.Tensor) else value_to_torch(pool, w.dtype, dev)
+        return ~torch.isnan(t.reshape(N, bs, H, D)[..., 0].float())     # [N, bs, H]
+
+    out = []
+    for pool in (w.k_pool, w.v_pool):
+        live = filled(pool)
+        if cache == "fp8_e4m3":
+            x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+            codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
+            codes = torch.where(live[..., None], codes, torch.full_like(codes, 0x7F))
+            scales = None
+        elif cache == "int8":
+            x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * 42.0
+            codes = x.round().clamp(-127, 127).to(torch.int8).view(torch.uint8)
+            sc = torch.rand((N, H, bs), generator=gen, device=dev, dtype=torch.float32) * 0.03 + 0.01
+            scales = torch.where(live.permute(0, 2, 1), sc, torch.full_like(sc, float("nan")))
+        else:
+            raise ValueError(f"unknown cache format {cache!r}")
+        out.append((codes.contiguous(), None if scales is None else scales.contiguous()))
+    if dev.type == "cpu":
+        out = [(c.numpy(), None if s is None else s.numpy()) for c, s in out]
+    return Q8Pools(cache, out[0][0], out[1][0], out[0][1], out[1][1],
+                   k_scale if cache == "fp8_e4m3" else 1.0, v_scale if cache == "fp8_e4m3" else 1.0)

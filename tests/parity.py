@@ -95,3 +95,65 @@ def assert_pools_equal(got_k, got_v, ref_k, ref_v, what=""):
     assert got_k.shape == ref_k.shape
     assert got_k.tobytes() == ref_k.tobytes(), f"{what}: K pool differs from the oracle"
     assert got_v.tobytes() == ref_v.tobytes(), f"{what}: V pool differs from the oracle"
+
+
+# -- 8-bit pools -------------------------------------------------------------------
+
+def _t(a, device):
+    return a.to(device) if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def gpu_step_q8(w: wl.Workload, p: wl.Q8Pools, device="cuda", return_pools=True):
+    """copy_blocks -> kv_append (quantising) -> decode on an 8-bit pool.
+    Returns (k_codes, v_codes, k_scales, v_scales, out, error_bits) on the host."""
+    tv = lambda a: wl.value_to_torch(a, w.dtype, device)
+    kc, vc = _t(p.k_codes, device).clone(), _t(p.v_codes, device).clone()
+    ks = None if p.k_scales is None else _t(p.k_scales, device).clone()
+    vs = None if p.v_scales is None else _t(p.v_scales, device).clone()
+    pool = pagedkv.KVPool(kc, vc, cache=p.cache, dtype=TORCH_DTYPE[w.dtype], k_scales=ks,
+                          v_scales=vs, k_scale=p.k_scale, v_scale=p.v_scale)
+    try:
+        pool.copy_blocks(torch.from_numpy(np.ascontiguousarray(w.pairs, dtype=np.int32)).to(device))
+        pool.append(tv(w.k_new), tv(w.v_new), torch.from_numpy(w.slot_mapping).to(device))
+        out = pool.decode(tv(w.q), torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device),
+                          torch.from_numpy(w.seq_lens).to(device), w.scale)
+        torch.cuda.synchronize()
+        err = pool.get_error()
+    finally:
+        pool.close()
+    res = wl.value_to_numpy(out, w.dtype)
+    if not return_pools:
+        return None, None, None, None, res, err
+    host = lambda t: None if t is None else t.cpu().numpy()
+    return host(kc), host(vc), host(ks), host(vs), res, err
+
+
+def oracle_step_q8(w: wl.Workload, p: wl.Q8Pools, seqs=None):
+    """The same step on the C oracle: returns (codes and scales after the
+    append, attention output for `seqs` or every sequence)."""
+    h = wl.on_host(w)
+    host = lambda a: None if a is None else np.ascontiguousarray(
+        a.cpu().numpy() if isinstance(a, torch.Tensor) else a).copy()
+    kc, vc, ks, vs = host(p.k_codes), host(p.v_codes), host(p.k_scales), host(p.v_scales)
+    assert c_oracle.copy_blocks_q8(kc, vc, ks, vs, h.pairs) == 0
+    c_oracle.append_q8(kc, vc, ks, vs, h.k_new, h.v_new, h.dtype, h.slot_mapping, p.cache,
+                       p.k_scale, p.v_scale)
+    sel = np.arange(h.batch) if seqs is None else np.asarray(seqs, dtype=np.int64)
+    out = c_oracle.decode_q8(np.ascontiguousarray(h.q[sel]), h.dtype, kc, vc, ks, vs, p.cache,
+                             np.ascontiguousarray(h.block_tables[sel]),
+                             np.ascontiguousarray(h.seq_lens[sel]), h.scale, h.num_kv_heads,
+                             p.k_scale, p.v_scale, num_threads=ORACLE_THREADS)
+    return kc, vc, ks, vs, out
+
+
+def assert_q8_pools_equal(got, want, what=""):
+    for g, r, name in zip(got, want, ("k codes", "v codes", "k scales", "v scales")):
+        if r is None:
+            assert g is None, f"{what}: {name}"
+            continue
+        if r.dtype == np.uint8:
+            bad = np.flatnonzero(g.reshape(-1) != r.reshape(-1))
+            assert bad.size == 0, f"{what}: {name} differ at {bad.size} bytes, first {bad[:5]}"
+        else:
+            ok = (g.view(np.uint32) == r.view(np.uint32)) | (np.isnan(g) & np.isnan(r))
+            assert ok.all(), f"{what}: {name} differ at {np.flatnonzero(~ok.reshape(-1))[:5]}"
