@@ -20,6 +20,7 @@ rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import os
@@ -72,6 +73,9 @@ def parse_args(argv=None):
                     help="block size of the long-context workload (8, 16 or 32)")
     ap.add_argument("--prompt-len", type=int, default=None,
                     help="prompt length of the shared-prefix workload (2000 or 2008)")
+    ap.add_argument("--kv-cache", choices=["fp8_e4m3", "int8"], default=None,
+                    help="an 8-bit pool (quantising append, dequantising decode) instead of "
+                         "the workload's 16-bit one")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix workload: decode with the cascade entry point")
     return ap.parse_args(argv)
@@ -224,11 +228,29 @@ def unique_bytes_fields(w, world, dec_ms):
 
 # ----------------------------------------------------------- CPU baseline --
 
-def oracle_sample_step(host_w, seqs, threads):
+def oracle_sample_step(host_w, seqs, threads, q8=None):
     """One oracle step (copy, append, attention) restricted to `seqs`;
-    returns (seconds, algorithmic bytes of that sample)."""
+    returns (seconds, algorithmic bytes of that sample).  `q8`: host arrays
+    of an 8-bit pool (workloads.Q8Pools) to step instead of the 16-bit one."""
     import numpy as np
     from oracle import c_oracle
+    if q8 is not None:
+        t0 = time.perf_counter()
+        c_oracle.copy_blocks_q8(q8.k_codes, q8.v_codes, q8.k_scales, q8.v_scales, host_w.pairs)
+        c_oracle.append_q8(q8.k_codes, q8.v_codes, q8.k_scales, q8.v_scales, host_w.k_new[seqs],
+                           host_w.v_new[seqs], host_w.dtype, host_w.slot_mapping[seqs], q8.cache,
+                           q8.k_scale, q8.v_scale)
+        c_oracle.decode_q8(np.ascontiguousarray(host_w.q[seqs]), host_w.dtype, q8.k_codes,
+                           q8.v_codes, q8.k_scales, q8.v_scales, q8.cache,
+                           np.ascontiguousarray(host_w.block_tables[seqs]),
+                           np.ascontiguousarray(host_w.seq_lens[seqs]), host_w.scale,
+                           host_w.num_kv_heads, q8.k_scale, q8.v_scale, num_threads=threads)
+        dt = time.perf_counter() - t0
+        sub = copy.copy(host_w)
+        sub.seq_lens = host_w.seq_lens[seqs]
+        sub.q = host_w.q[seqs]
+        sub.slot_mapping = host_w.slot_mapping[seqs]
+        return dt, q8.step_bytes(sub)
     k, v = host_w.k_pool, host_w.v_pool          # state: appends are idempotent
     t0 = time.perf_counter()
     c_oracle.copy_blocks(k, v, host_w.pairs, host_w.dtype)
@@ -245,12 +267,20 @@ def oracle_sample_step(host_w, seqs, threads):
     return dt, nbytes
 
 
-def pick_sample(host_w, budget_s, threads):
+def q8_on_host(q8):
+    """Host numpy copies of an 8-bit pool's arrays (for the oracle)."""
+    import dataclasses
+    h = lambda a: None if a is None else (a.cpu().numpy() if hasattr(a, "cpu") else a).copy()
+    return dataclasses.replace(q8, k_codes=h(q8.k_codes), v_codes=h(q8.v_codes),
+                               k_scales=h(q8.k_scales), v_scales=h(q8.v_scales))
+
+
+def pick_sample(host_w, budget_s, threads, q8=None):
     """Sequences (a prefix of a fixed shuffle) whose oracle step takes about budget_s."""
     import numpy as np
     order = np.random.default_rng(1234).permutation(host_w.batch)
     n = min(host_w.batch, max(1, threads))
-    dt, _ = oracle_sample_step(host_w, order[:n], threads)
+    dt, _ = oracle_sample_step(host_w, order[:n], threads, q8)
     if dt < budget_s and n < host_w.batch:
         n = int(min(host_w.batch, max(n, n * budget_s / max(dt, 1e-3))))
     return np.sort(order[:n])
@@ -293,7 +323,16 @@ def run_ours(args):
     q, k_new, v_new = view["q"], view["k_new"], view["v_new"]
     slots, tables, lens, pairs = view["slots"], view["tables"], view["lens"], view["pairs"]
     host_in = dev_in.cpu().pin_memory()
-    pool = pagedkv.KVPool(k_pool, v_pool)
+    q8 = None
+    if args.kv_cache:
+        q8 = wl.q8_pools(w, args.kv_cache, args.seed)
+        w.k_pool = w.v_pool = k_pool = v_pool = None              # the 16-bit pools are not used
+        torch.cuda.empty_cache()
+        pool = pagedkv.KVPool(q8.k_codes, q8.v_codes, cache=q8.cache, dtype=q.dtype,
+                              k_scales=q8.k_scales, v_scales=q8.v_scales, k_scale=q8.k_scale,
+                              v_scale=q8.v_scale)
+    else:
+        pool = pagedkv.KVPool(k_pool, v_pool)
     out = torch.empty_like(q)
     cascade = args.cascade and w.groups is not None
     if cascade:
@@ -370,8 +409,9 @@ def run_ours(args):
     barrier()
     e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eve) / KE
 
-    step_bytes = w.step_bytes()
-    att_bytes = w.attention_bytes()
+    step_bytes = w.step_bytes() if q8 is None else q8.step_bytes(w)
+    att_bytes = w.attention_bytes() if q8 is None else q8.attention_bytes(w)
+    kv_bytes = w.kv_bytes() if q8 is None else q8.kv_bytes(w)
     max_step_ms, total_bytes = reduce_max_sum(step_ms, step_bytes)
     max_e2e_ms, _ = reduce_max_sum(e2e_ms, step_bytes)
     max_dec_ms, _ = reduce_max_sum(dec_ms, att_bytes)
@@ -389,11 +429,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host_w = wl.on_host(w)
+        hq8 = None if q8 is None else q8_on_host(q8)
         threads = os.cpu_count() or 1
-        seqs = pick_sample(host_w, 10.0, threads)
+        seqs = pick_sample(host_w, 10.0, threads, hq8)
         dt, nb, passes = 0.0, 0, 0
         while passes < 3 or dt < 5.0:                   # a few seconds of CPU work at least
-            t, b = oracle_sample_step(host_w, seqs, threads)
+            t, b = oracle_sample_step(host_w, seqs, threads, hq8)
             dt, nb, passes = dt + t, nb + b, passes + 1
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{len(seqs)} of {w.batch} sequences of the same step (copy + append + "
@@ -405,15 +446,20 @@ def run_ours(args):
     return {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(max_step_ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype if q8 is None else f"{q8.cache} storage, f16 MMA, fp32 softmax",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload]
                    + ("" if args.batch is None else f" (batch overridden to {args.batch})")
                    + ("" if args.block_size is None else f" (block_size {args.block_size})")
-                   + ("" if args.prompt_len is None else f" (prompt_len {args.prompt_len})"),
+                   + ("" if args.prompt_len is None else f" (prompt_len {args.prompt_len})")
+                   + ("" if q8 is None else f", K/V stored as {q8.cache} codes"),
                    "seed": args.seed, "placement": args.placement, "global_batch": w.batch * world,
+                   "kv_cache": q8.cache if q8 is not None else w.dtype,
                    "tokens_per_replica": int(w.seq_lens.sum()),
-                   "kv_bytes_per_replica": w.kv_bytes(), "step_bytes_per_replica": step_bytes,
-                   "l2": "flushed (512 MB write) between timed steps; KV 1.7 GB > 129 MB L2",
+                   "kv_bytes_per_replica": kv_bytes, "step_bytes_per_replica": step_bytes,
+                   "l2": f"flushed (512 MB write) between timed steps; K/V read per step "
+                         f"{kv_bytes / 1e9:.2f} GB > 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "seq_steps_per_s": round(total_seqs / (max_step_ms * 1e-3), 1),
         **unique_bytes_fields(w, world, max_dec_ms),
@@ -424,7 +470,7 @@ def run_ours(args):
                                 "paged_decode_split (the whole decode call: one kernel, merges included)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": None if cascade else profiled_traffic(),
+                     "traffic": None if (cascade or q8 is not None) else profiled_traffic(),
                      "algorithmic_bytes": roof_bytes},
         "e2e": {"value": round(total_bytes / (max_e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(max_e2e_ms, 5), "h2d_bytes_per_step": h2d,
@@ -447,16 +493,19 @@ def run_reference(args):
     from paged_kv_cache_68_gb300 import workloads as wl
     c_oracle.build()
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
-    w = wl.on_host(make_workload(args.workload, args.seed, dev, args.placement, args.batch,
-                                 args.block_size, args.prompt_len))
+    wd = make_workload(args.workload, args.seed, dev, args.placement, args.batch,
+                       args.block_size, args.prompt_len)
+    q8 = None if not args.kv_cache else q8_on_host(wl.q8_pools(wd, args.kv_cache, args.seed))
+    w = wl.on_host(wd)
+    del wd
     threads = os.cpu_count() or 1
     per_step = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    seqs = pick_sample(w, per_step, threads)
+    seqs = pick_sample(w, per_step, threads, q8)
     for _ in range(args.warmup):
-        oracle_sample_step(w, seqs, threads)
+        oracle_sample_step(w, seqs, threads, q8)
     tot_t, tot_b = 0.0, 0
     for _ in range(args.steps):
-        dt, nb = oracle_sample_step(w, seqs, threads)
+        dt, nb = oracle_sample_step(w, seqs, threads, q8)
         tot_t += dt
         tot_b += nb
     value = tot_b / tot_t / 1e9
@@ -468,8 +517,10 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed,
-                   "placement": args.placement},
+        "config": {"workload": WORKLOAD_TEXT[args.workload]
+                   + ("" if q8 is None else f", K/V stored as {q8.cache} codes"),
+                   "seed": args.seed, "placement": args.placement,
+                   "kv_cache": q8.cache if q8 is not None else w.dtype},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,

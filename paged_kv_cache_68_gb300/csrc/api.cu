@@ -51,9 +51,14 @@ bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p, bool swizzl
     const CUtensorMapDataType dt = p.elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : p.elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    // L2 fills of 256 B match a 16-bit head row (or a 128-byte half of it); an
+    // 8-bit head row is 128 B and a 256-byte fill would drag in the next head's row
+    const CUtensorMapL2promotion l2 = p.elem_bytes == 1 && p.head_dim * elt <= 128
+                                          ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                          : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     return enc(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, l2,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -85,7 +90,6 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     const int D = pool.head_dim, bs = pool.block_size, elt = pool.elem_bytes;
     const bool q8 = is_q8(pool);
     const int sb = pool.cache_dtype == KV_INT8 ? 4 : 0;     // scale bytes per tile row
-    const int cvt = q8 ? 16 * D * 2 : 0;                    // f16 tile per consumer warp
     const size_t stage = 2ull * bs * D * elt + 2ull * bs * sb;
     // Ring depth S is a multiple of the consumer-warp count (each stage has a
     // fixed consumer).  Pick the S with the most (resident CTAs x stages per
@@ -96,7 +100,7 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     for (int S = ncw; S <= 8 * ncw; S += ncw) {
         if (S > ncw && (size_t)S * stage > kMaxRingBytes) break;
         // + 1 KB: the kernel rounds its shared-memory base up to 1 KB
-        const size_t smem = dec::Layout(S, batch, bs, G, D, elt, num_groups, sb, cvt).total + 1024;
+        const size_t smem = dec::Layout(S, batch, bs, G, D, elt, num_groups, sb).total + 1024;
         if (smem > kMaxSmem) break;
         int occ = 0;
         cudaError_t e = cudaErrorNotSupported;
@@ -252,7 +256,10 @@ static kv_status finish_pool(kv_pool* p, kv_pool_t* out) {
         delete p;
         return pagedkv::cuda_fail(e, "kv_pool_create");
     }
-    p->has_swizzled_maps = p->elem_bytes == 2 && head_dim == 128 && block_size <= 256;
+    // 128-byte-swizzled boxes: 16-bit pools (two per row of head_dim 128) and
+    // 8-bit pools (one per row)
+    p->has_swizzled_maps = (p->elem_bytes == 2 || p->elem_bytes == 1) && head_dim == 128 &&
+                           block_size <= 256;
     bool maps_ok = encode_pool_map(&p->tmap_k, k_pool, *p, false) &&
                    encode_pool_map(&p->tmap_v, v_pool, *p, false);
     if (maps_ok && p->has_swizzled_maps)

@@ -102,14 +102,12 @@ struct Params {
 
 // ---------------------------------------------------------------- layout ---
 struct Layout {
-    uint32_t full, empty, valid, misc, prefix, groups, skip, pst, pbuf, abuf, merge_o, merge_ml, cvt,
-        ring;
+    uint32_t full, empty, valid, misc, prefix, groups, skip, pst, pbuf, abuf, merge_o, merge_ml,
+        sring, ring;
     uint32_t tx_bytes, stage_bytes, total;
     // elt: bytes per pool element; K: cascade groups (0 for plain decode);
-    // sb: scale bytes per token row of a tile (INT8 pools: 4); cvt_warp: bytes
-    // of each consumer warp's conversion tile (8-bit pools)
-    __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt, int K = 0, int sb = 0,
-                               int cvt_warp = 0) {
+    // sb: scale bytes per token row of a tile (INT8 pools: 4)
+    __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt, int K = 0, int sb = 0) {
         uint32_t off = 0;
         full = off;   off += 8u * S;
         empty = off;  off += 8u * S;
@@ -124,12 +122,12 @@ struct Layout {
         abuf = off;   off += 8u * NCW * G;
         merge_o = off;  off += 4u * (NCW - 1) * G * D;
         merge_ml = off; off += 2u * 4u * (NCW - 1) * G;
+        off = (off + 15u) & ~15u;
+        sring = off;  off += (uint32_t)S * 2u * bs * sb;  // per stage: K then V scales
         off = (off + 1023u) & ~1023u;              // swizzle atoms are 1 KB
-        cvt = off;    off += (uint32_t)NCW * (((uint32_t)cvt_warp + 1023u) & ~1023u);
         ring = off;
-        // K tile, V tile, then (INT8) the K and V scales of the tile's rows
+        stage_bytes = (2u * bs * D * elt + 127u) & ~127u;   // K tile then V tile
         tx_bytes = 2u * bs * D * elt + 2u * bs * sb;
-        stage_bytes = (tx_bytes + 127u) & ~127u;
         off += stage_bytes * S;
         total = off;
     }
@@ -455,7 +453,6 @@ struct CorePolicy {
     static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
     static constexpr int kKvBytes = sizeof(T);   // pool element
     static constexpr int kScaleBytes = 0;
-    static constexpr int kCvtBytes = 0;
 
     float2* pb;                   // this warp's (score | p, p) [bs][G]
     float2* ab;                   // this warp's (alpha, alpha) [G]
@@ -464,7 +461,7 @@ struct CorePolicy {
     float m_run, l_run;           // for head lane % G
 
     __device__ __forceinline__ CorePolicy(float2* pbuf, float2* abuf) : pb(pbuf), ab(abuf) {}
-    __device__ __forceinline__ void setup(const Params&, unsigned char*) {}
+    __device__ __forceinline__ void setup(const Params&) {}
 
     __device__ __forceinline__ void begin(const T* qp, float qscale, int lane) {
         const int jl = lane % C::TPT;
@@ -487,7 +484,7 @@ struct CorePolicy {
     }
 
     __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
-                                          int n_valid, int bs_rt, float, int lane) {
+                                          const float*, int n_valid, int bs_rt, float, int lane) {
         const int bs = BSC > 0 ? BSC : bs_rt;
         const int tg = lane / C::TPT, jl = lane % C::TPT;
         const int hsel = (jl >> C::HSHIFT) & (G - 1);
@@ -659,7 +656,10 @@ struct CorePolicy {
 // each 16-token tile for heads 2 tig, 2 tig + 1.  O^T (dims x heads): the lane
 // holds dims 16 mt + gid, 16 mt + gid + 8 for the same two heads.  Heads >= G
 // are padding (zero query rows) and are never written out.
-template <typename T, int D, int G, int BSC>
+// kPermV: the MMA's output rows (m-slots) 16 mt + gid + 8 hf hold dims
+// 16 gid + 2 mt + hf instead of 16 mt + gid + 8 hf (the 8-bit policy loads V
+// that way); put / merge_store write every value to its own dim.
+template <typename T, int D, int G, int BSC, bool kPermV = false>
 struct TcPolicy {
     static_assert(sizeof(T) == 2, "tensor-core path takes 16-bit pools");
     static_assert(BSC % 16 == 0 && BSC > 0, "tensor-core path needs a block size of 16k");
@@ -668,7 +668,6 @@ struct TcPolicy {
     static constexpr int kMinBlocks = 3;
     static constexpr int kKvBytes = sizeof(T);
     static constexpr int kScaleBytes = 0;
-    static constexpr int kCvtBytes = 0;
     static constexpr int KS = D / 16;      // QK k-steps (16 dims each)
     static constexpr int MT = D / 16;      // PV m-tiles (16 dims each)
     static constexpr int TT = BSC / 16;    // 16-token tiles per block
@@ -678,7 +677,11 @@ struct TcPolicy {
     float m_run[2], l_run[2];              // heads 2 tig, 2 tig + 1
 
     __device__ __forceinline__ TcPolicy(float2*, float2*) {}
-    __device__ __forceinline__ void setup(const Params&, unsigned char*) {}
+    __device__ __forceinline__ void setup(const Params&) {}
+
+    __device__ static __forceinline__ int dim(int mt, int gid, int hf) {
+        return kPermV ? 16 * gid + 2 * mt + hf : mt * 16 + gid + 8 * hf;
+    }
 
     // Shared address of 16-byte chunk c of row r in a 128-byte-swizzled tile
     // of `rows` rows (chunks 0-7 in the first 128-byte half, 8-15 in the second).
@@ -702,7 +705,7 @@ struct TcPolicy {
     }
 
     __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
-                                          int n_valid, int, float qscale, int lane) {
+                                          const float*, int n_valid, int, float qscale, int lane) {
         const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, r8 = lane & 7;
         const uint32_t kbase = smem_u32(Ks), vbase = smem_u32(Vs);
         if (n_valid < BSC) {
@@ -807,8 +810,8 @@ struct TcPolicy {
                 float* row = mo + ((w - 1) * G + h) * D;
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    row[mt * 16 + gid] = oacc[mt][j];
-                    row[mt * 16 + gid + 8] = oacc[mt][j + 2];
+                    row[dim(mt, gid, 0)] = oacc[mt][j];
+                    row[dim(mt, gid, 1)] = oacc[mt][j + 2];
                 }
                 if (gid == 0) {
                     mm[(w - 1) * G + h] = m_run[j];
@@ -847,7 +850,7 @@ struct TcPolicy {
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int d = mt * 16 + gid + 8 * hf;
+                    const int d = dim(mt, gid, hf);
                     float num = c[0] * oacc[mt][j + 2 * hf];
 #pragma unroll
                     for (int w2 = 1; w2 < NCW; ++w2) num += c[w2] * mo[((w2 - 1) * G + h) * D + d];
@@ -858,7 +861,7 @@ struct TcPolicy {
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int d = mt * 16 + gid + 8 * hf;
+                    const int d = dim(mt, gid, hf);
                     if (po.complete)
                         static_cast<T*>(po.out)[h * D + d] = Elt<T>::store(v[mt][hf]);
                     else
@@ -875,66 +878,60 @@ struct TcPolicy {
 // ch. 10: a token's K and V are scaled and rounded to 8 bits when written and
 // turned back into wider numbers when read): FP8 E4M3 with one scale per pool,
 // or INT8 with one fp32 scale per (block, KV head, token row).  The tiles
-// arrive unswizzled, one byte per element (INT8: the tile's K and V scales
-// follow them in the stage).  Each consumer warp converts a 16-token tile of
-// codes to f16 -- exactly: every E4M3 value and every integer in [-128, 127]
-// is an f16 -- into its own 128-byte-swizzled shared tile and runs the
-// tensor-core policy's MMAs on it (f16 x f16 -> fp32).  The scales never pass
-// through f16:
-//   * Q is held as f16 * 2^e (a power of two per piece keeps the group's
-//     largest |q| below 2^15; bf16 and f16 queries convert exactly), and the
-//     score of token t is acc * scale * log2(e) * 2^-e * kscale_t in fp32;
-//   * P is multiplied by vscale_t / vref before its hi + lo f16 split, vref
-//     the tile's largest V scale, and the accumulator is kept as O / R with R
-//     the last tile's vref (a change of R rescales it with the softmax alpha).
-// The MMA type is f16 whatever the query type; outputs use the query type.
+// arrive by TMA with the 128-byte swizzle (one 128-byte row per token); INT8
+// scales come by bulk copy into a small ring beside them.  The consumer builds
+// the f16 MMA fragments straight from the codes in registers -- every E4M3
+// value and every integer in [-128, 127] is an f16, so the conversion is
+// exact -- with no shared-memory round trip:
+//   * QK (A = K rows): MMA k-slot 2 tig + {0, 1, 8, 9} of k-step ks stands for
+//     dim 32 tig + 4 ks + {0, 1, 2, 3} (a relabelling of the dot product's
+//     terms, applied to Q too), so a lane's K codes for all k-steps are two
+//     16-byte chunks per row;
+//   * PV (A = V^T): output row (m-slot) 16 mt + gid + 8 hf stands for dim
+//     16 gid + 2 mt + hf, so a lane's V codes are one 16-byte chunk of each of
+//     its four token rows; the merge writes every value to its own dim.
+// Both read patterns are bank-conflict-free under the swizzle.  The scales
+// never pass through f16: Q is held as f16 * 2^e (a power of two per piece
+// keeps the group's largest |q| below 2^15; bf16 and f16 queries convert
+// exactly) and a score is acc * scale * log2(e) * 2^-e * kscale_t in fp32; P
+// is multiplied by vscale_t / vref (vref the tile's largest V scale) before
+// its hi + lo f16 split, and the accumulator is kept as O / R with R the last
+// vref (a change of R rescales it with the softmax alpha).
 constexpr int kFmtE4M3 = 0;
 constexpr int kFmtInt8 = 1;
 
+// Four codes (bytes 0..3 of w) -> f16x2 of bytes (0, 1) and of bytes (2, 3).
 template <int FMT>
-__device__ __forceinline__ void codes16_to_f16(uint4 w, uint4& lo, uint4& hi) {
-    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-    uint32_t o[8];
+__device__ __forceinline__ void cvt4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     if constexpr (FMT == kFmtE4M3) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(
-                (__nv_fp8x2_storage_t)(in[i] & 0xffffu), __NV_E4M3);
-            const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(
-                (__nv_fp8x2_storage_t)(in[i] >> 16), __NV_E4M3);
-            o[2 * i] = (uint32_t)a.x | ((uint32_t)a.y << 16);
-            o[2 * i + 1] = (uint32_t)b.x | ((uint32_t)b.y << 16);
-        }
+        const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+        const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+        lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
+        hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
     } else {
-        // two's complement byte b -> f16 (1024 + (b ^ 0x80)) - 1152 = b, exactly
+        // two's complement byte b -> f16 (1024 + (b ^ 0x80)) - 1152 = b
         const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t x = in[i] ^ 0x80808080u;
-            const uint32_t l = __byte_perm(x, 0x64646464u, 0x7150);
-            const uint32_t h = __byte_perm(x, 0x64646464u, 0x7352);
-            const __half2 lh = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
-            const __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
-            o[2 * i] = *reinterpret_cast<const uint32_t*>(&lh);
-            o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hh);
-        }
+        const uint32_t x = w ^ 0x80808080u;
+        const uint32_t l = __byte_perm(x, 0x64646464u, 0x7150);
+        const uint32_t h = __byte_perm(x, 0x64646464u, 0x7352);
+        const __half2 lh = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
+        const __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+        lo = *reinterpret_cast<const uint32_t*>(&lh);
+        hi = *reinterpret_cast<const uint32_t*>(&hh);
     }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 template <typename T, int D, int G, int FMT>
-struct Tc8Policy : TcPolicy<T, D, G, 16> {
-    using Base = TcPolicy<T, D, G, 16>;
+struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
+    using Base = TcPolicy<T, D, G, 16, true>;
+    static_assert(D == 128, "one 128-byte code row per token");
     static constexpr int KS = Base::KS;
     static constexpr int MT = Base::MT;
-    static constexpr bool kSwizzled = false;
-    static constexpr int kMinBlocks = 3;
+    static constexpr bool kSwizzled = true;
+    static constexpr int kMinBlocks = 3;         // 12 consumer warps per SM beat 8 unspilled ones
     static constexpr int kKvBytes = 1;
     static constexpr int kScaleBytes = FMT == kFmtInt8 ? 4 : 0;
-    static constexpr int kCvtBytes = 16 * D * 2;   // one 16-token f16 tile per warp
 
-    unsigned char* cvt;   // this warp's f16 tile [16][D], 128-byte swizzled halves
     float qs;             // scale * log2(e) * 2^-e (* the FP8 K scale)
     float vq;             // FP8: the V scale; INT8: 1
     float kq;             // FP8: the K scale; INT8: 1
@@ -942,14 +939,14 @@ struct Tc8Policy : TcPolicy<T, D, G, 16> {
 
     __device__ __forceinline__ Tc8Policy(float2* a, float2* b) : Base(a, b) {}
 
-    __device__ __forceinline__ void setup(const Params& p, unsigned char* buf) {
-        cvt = buf;
+    __device__ __forceinline__ void setup(const Params& p) {
         kq = FMT == kFmtE4M3 ? p.fp8_k_scale : 1.f;
         vq = FMT == kFmtE4M3 ? p.fp8_v_scale : 1.f;
     }
 
-    __device__ static __forceinline__ uint32_t swz16(uint32_t tile, int r, int c) {
-        return tile + (uint32_t)((c >> 3) * 16 * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    // 16-byte chunk c of row r of a 128-byte-swizzled tile (1 KB-aligned base)
+    __device__ static __forceinline__ uint4 chunk(const unsigned char* tile, int r, int c) {
+        return *reinterpret_cast<const uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4));
     }
 
     __device__ __forceinline__ void begin(const T* qp, float qscale, int lane) {
@@ -957,15 +954,15 @@ struct Tc8Policy : TcPolicy<T, D, G, 16> {
         float2 qf[KS][2];
         float amax = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
+        for (int ks = 0; ks < KS; ++ks) {
+            uint2 raw = make_uint2(0u, 0u);
+            if (gid < G) raw = __ldg(reinterpret_cast<const uint2*>(qp + gid * D + 32 * tig + 4 * ks));
+            qf[ks][0] = Mma<T>::unpack(raw.x);
+            qf[ks][1] = Mma<T>::unpack(raw.y);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint32_t raw = gid < G ? __ldg(reinterpret_cast<const uint32_t*>(
-                                                   qp + gid * D + ks * 16 + j * 8 + tig * 2))
-                                             : 0u;
-                qf[ks][j] = Mma<T>::unpack(raw);
+            for (int j = 0; j < 2; ++j)
                 amax = fmaxf(amax, fmaxf(fabsf(qf[ks][j].x), fabsf(qf[ks][j].y)));
-            }
+        }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, off));
         // 2^e with amax * 2^e in [2^14, 2^15): exponent field of amax, clamped
@@ -991,44 +988,32 @@ struct Tc8Policy : TcPolicy<T, D, G, 16> {
         R = vq;
     }
 
-    // Rows r < keep of the 16-row code tile at `src` -> f16 in cvt; rows >= keep -> 0.
-    __device__ __forceinline__ void convert(const unsigned char* src, int keep, int lane) const {
-        constexpr int CPR = D / 16;                 // 16-byte code chunks per row
-#pragma unroll 1
-        for (int i = lane; i < 16 * CPR; i += 32) {
-            const int r = i / CPR, c = i % CPR;
-            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-            if (r < keep) codes16_to_f16<FMT>(*reinterpret_cast<const uint4*>(src + r * D + c * 16), lo, hi);
-            const int c0 = 2 * c, c1 = 2 * c + 1;
-            *reinterpret_cast<uint4*>(cvt + (c0 >> 3) * 2048 + r * 128 + (((c0 & 7) ^ (r & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(cvt + (c1 >> 3) * 2048 + r * 128 + (((c1 & 7) ^ (r & 7)) << 4)) = hi;
-        }
-    }
-
     __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
-                                          int n_valid, int bs, float, int lane) {
-        const int gid = lane >> 2, mi = lane >> 3, r8 = lane & 7;
-        const uint32_t cb = smem_u32(cvt);
-        const float* ksc = reinterpret_cast<const float*>(Vs + bs * D);   // INT8 only
-        const float* vsc = ksc + bs;
+                                          const float* sc, int n_valid, int bs, float, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
         for (int t0 = 0; t0 < n_valid; t0 += 16) {
-            // -- S^T of the tile: 16 tokens x the group's heads ---------------
-            convert(Ks + t0 * D, 16, lane);
-            __syncwarp();
+            const unsigned char* Kt = Ks + t0 * 128;
+            const unsigned char* Vt = Vs + t0 * 128;
+            // -- S^T of the tile: 16 tokens x the group's heads -----------------
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(a, swz16(cb, (mi & 1) * 8 + r8, ks * 2 + (mi >> 1)));
-                Mma<__half>::run(acc[ks & 1], a, this->qb[ks][0], this->qb[ks][1]);
+            for (int h = 0; h < 2; ++h) {
+                const uint4 ra = chunk(Kt, gid, 2 * tig + h), rb = chunk(Kt, gid + 8, 2 * tig + h);
+                const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t a[4];
+                    cvt4<FMT>(wa[q], a[0], a[2]);
+                    cvt4<FMT>(wb[q], a[1], a[3]);
+                    Mma<__half>::run(acc[q & 1], a, this->qb[4 * h + q][0], this->qb[4 * h + q][1]);
+                }
             }
-            __syncwarp();                             // the tile is read; V may overwrite it
             const int ta = t0 + gid, tb = ta + 8;
             const bool v0 = ta < n_valid, v1 = tb < n_valid;
             float fa = qs, fb = qs;
             if constexpr (FMT == kFmtInt8) {
-                fa *= v0 ? ksc[ta] : 0.f;
-                fb *= v1 ? ksc[tb] : 0.f;
+                fa *= v0 ? sc[ta] : 0.f;
+                fb *= v1 ? sc[tb] : 0.f;
             }
             float s[4];
             s[0] = v0 ? (acc[0][0] + acc[1][0]) * fa : -CUDART_INF_F;
@@ -1062,22 +1047,22 @@ struct Tc8Policy : TcPolicy<T, D, G, 16> {
                 this->m_run[j] = mnew[j];
             }
             // -- V scales: P' = P * vscale_t / vref, accumulators kept as O / vref --
-            float vref = R, wa = 1.f, wb = 1.f;
+            float rf = 1.f, wa = 1.f, wb = 1.f;
             if constexpr (FMT == kFmtInt8) {
-                const float sa = v0 ? vsc[ta] : 0.f, sb = v1 ? vsc[tb] : 0.f;
+                const float sa = v0 ? sc[bs + ta] : 0.f, sb = v1 ? sc[bs + tb] : 0.f;
                 float mx = fmaxf(sa, sb);
 #pragma unroll
                 for (int off = 16; off >= 4; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
                 if (mx > 0.f) {
-                    vref = mx;
-                    wa = sa / mx;
-                    wb = sb / mx;
+                    const float inv = __frcp_rn(mx);
+                    wa = sa * inv;
+                    wb = sb * inv;
+                    rf = R * inv;
+                    R = mx;
                 } else {
                     wa = wb = 0.f;                    // the tile's V rows are all zero
                 }
             }
-            const float rf = R / vref;
-            R = vref;
             const float2 a2 = make_float2(alpha[0] * rf, alpha[1] * rf);
             if (!__all_sync(FULL, a2.x == 1.f && a2.y == 1.f))
 #pragma unroll
@@ -1088,23 +1073,35 @@ struct Tc8Policy : TcPolicy<T, D, G, 16> {
                 this->oacc[mt][2] = hi.x; this->oacc[mt][3] = hi.y;
             }
             s[0] *= wa; s[1] *= wa; s[2] *= wb; s[3] *= wb;
-            // -- O^T += V_tile^T P'^T, P' as hi + lo f16 halves -----------------
-            convert(Vs + t0 * D, n_valid - t0, lane);
-            __syncwarp();
             const uint32_t h01 = Mma<__half>::pack(s[0], s[1]), h23 = Mma<__half>::pack(s[2], s[3]);
             const float2 f01 = Mma<__half>::unpack(h01), f23 = Mma<__half>::unpack(h23);
             const uint32_t l01 = Mma<__half>::pack(s[0] - f01.x, s[1] - f01.y);
             const uint32_t l23 = Mma<__half>::pack(s[2] - f23.x, s[3] - f23.y);
             const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
             const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+            // -- O^T += V_tile^T P'^T: token rows 2 tig, 2 tig + 1, + 8, + 9 ------
+            // (rows past the sequence end read as zero codes: P' is 0 there, but
+            // an E4M3 NaN code would still poison the MMA)
+            uint32_t vw[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 2 * tig + (i & 1) + 8 * (i >> 1);
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (t0 + r < n_valid) v = chunk(Vt, r, gid);
+                vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;
+            }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
+                // dims 16 gid + 2 mt (+1): bytes 2 mt, 2 mt + 1 of each row's chunk
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t x01 = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
+                const uint32_t x23 = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
                 uint32_t a[4];
-                ldsm_x4_t(a, swz16(cb, (mi >> 1) * 8 + r8, mt * 2 + (mi & 1)));
+                cvt4<FMT>(x01, a[0], a[1]);
+                cvt4<FMT>(x23, a[2], a[3]);
                 Mma<__half>::run(this->oacc[mt], a, bh0, bh1);
                 Mma<__half>::run(this->oacc[mt], a, bl0, bl1);
             }
-            __syncwarp();                             // before the next tile's K overwrites it
         }
     }
 
@@ -1341,7 +1338,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int B = p.batch, S = p.stages, H = p.num_kv_heads, bs = p.bs;
-    const Layout lay(S, B, bs, G, D, ELT, p.num_groups, Pol::kScaleBytes, Pol::kCvtBytes);
+    const Layout lay(S, B, bs, G, D, ELT, p.num_groups, Pol::kScaleBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
@@ -1462,7 +1459,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                         }
                         if constexpr (Pol::kScaleBytes > 0) {
                             const size_t srow = ((size_t)id * H + gg) * bs;
-                            const uint32_t sdst = dst + (uint32_t)(2 * bs * D * ELT);
+                            const uint32_t sdst = smem_u32(smem + lay.sring) + (uint32_t)(s * 2 * bs * 4);
                             bulk_load(sdst, p.k_scales + srow, (uint32_t)bs * 4u, fb);
                             bulk_load(sdst + (uint32_t)bs * 4u, p.v_scales + srow, (uint32_t)bs * 4u,
                                       fb);
@@ -1497,7 +1494,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     const T* qbase = static_cast<const T*>(p.q);
     T* obase = static_cast<T*>(p.out);
     Pol pol(pb, ab);
-    pol.setup(p, smem + lay.cvt + (size_t)w * ((Pol::kCvtBytes + 1023) & ~1023));
+    pol.setup(p);
 
     bool first_piece = true;
     for (int u = start; u < end;) {
@@ -1536,7 +1533,10 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
             if (ok && valid[s]) {
                 const int j = skip + j0 + (uu - u);
                 const unsigned char* Ks = ring + (size_t)s * lay.stage_bytes;
-                pol.block(Ks, Ks + bs * D * ELT, min(bs, Lb - j * bs), bs, p.qscale, lane);
+                const float* sc = Pol::kScaleBytes > 0
+                                      ? reinterpret_cast<const float*>(smem + lay.sring) + s * 2 * bs
+                                      : nullptr;
+                pol.block(Ks, Ks + bs * D * ELT, sc, min(bs, Lb - j * bs), bs, p.qscale, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));

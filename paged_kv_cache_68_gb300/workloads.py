@@ -475,12 +475,31 @@ class Q8Pools:
     k_scale: float = 1.0
     v_scale: float = 1.0
 
+    def row_bytes(self, w: "Workload") -> int:
+        """Stored bytes of one token's K and V rows: one byte per element plus
+        the INT8 scales (one fp32 per KV head, for K and for V)."""
+        return w.num_kv_heads * w.head_dim * 2 + (8 * w.num_kv_heads if self.cache == "int8" else 0)
+
     def kv_bytes(self, w: "Workload") -> int:
-        """Bytes attention reads for K and V: one byte per element, plus the
-        INT8 scales of every token row."""
-        tok = int(w.seq_lens.astype(np.int64).sum())
-        per = w.num_kv_heads * w.head_dim * 2 + (8 * w.num_kv_heads if self.cache == "int8" else 0)
-        return tok * per
+        """Bytes attention reads for K and V (exact tokens)."""
+        return int(w.seq_lens.astype(np.int64).sum()) * self.row_bytes(w)
+
+    def attention_bytes(self, w: "Workload") -> int:
+        bs = w.block_size
+        tbl = int(sum(-(-int(L) // bs) for L in w.seq_lens)) * 4
+        qo = 2 * int(np.prod(tuple(w.q.shape))) * w.elem_bytes
+        return self.kv_bytes(w) + qo + tbl + 4 * w.batch
+
+    def append_bytes(self, w: "Workload") -> int:
+        """16-bit rows read, codes (and scales) written, slots read."""
+        n = int((np.asarray(w.slot_mapping) >= 0).sum())
+        return n * (w.num_kv_heads * w.head_dim * w.elem_bytes * 2 + self.row_bytes(w) + 8)
+
+    def copy_bytes(self, w: "Workload") -> int:
+        return int(w.pairs.shape[0]) * w.block_size * self.row_bytes(w) * 2
+
+    def step_bytes(self, w: "Workload") -> int:
+        return self.attention_bytes(w) + self.append_bytes(w) + self.copy_bytes(w)
 
 
 def q8_pools(w: "Workload", cache: str, seed: int, k_scale: float = 1.0,
