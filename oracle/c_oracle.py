@@ -67,6 +67,8 @@ def _load():
             lib.oracle_decode_q8.argtypes = [P, I, P, P, P, P, I, D, D, L, L, L, L, P, L, P, L, L,
                                              D, P, I]
             lib.oracle_decode_q8.restype = L
+            lib.oracle_swap_blocks.argtypes = [P, P, P, I, L, L, P, L, I]
+            lib.oracle_swap_blocks.restype = L
             _lib = lib
     return _lib
 
@@ -174,3 +176,21 @@ def decode_q8(q, in_dtype: str, k_codes, v_codes, k_scales, v_scales, fmt: str, 
     if st < 0:
         raise ValueError("oracle_decode_q8 rejected its arguments")
     return (out, st) if return_status else out
+
+
+# ------------------------------------------------------- swap to host ----
+
+def swap_blocks(gpu_arrays, host_arrays, pairs, direction: int) -> int:
+    """See ``oracle_swap_blocks``: arrays share their leading (block) axis."""
+    assert len(gpu_arrays) == len(host_arrays)
+    n = len(gpu_arrays)
+    for g, h in zip(gpu_arrays, host_arrays):
+        assert g.shape[1:] == h.shape[1:] and g.dtype == h.dtype
+        _ptr(g), _ptr(h)
+    gp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in gpu_arrays])
+    hp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in host_arrays])
+    bb = (ctypes.c_long * n)(*[a[0].nbytes if a.shape[0] else a.itemsize * int(np.prod(a.shape[1:]))
+                               for a in gpu_arrays])
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    return _load().oracle_swap_blocks(gp, hp, bb, n, gpu_arrays[0].shape[0], host_arrays[0].shape[0],
+                                      _ptr(pr), pr.shape[0], int(direction))

@@ -331,3 +331,34 @@ def decode_q8(q, in_dtype: str, k_codes, v_codes, k_scales, v_scales, fmt: str,
             w = w / w.sum(axis=1, keepdims=True)
             out[b, heads] = w @ V[:, g, :]
     return out
+
+
+# ------------------------------------------------------- swap to host ----
+#
+# "Lecture 3" (semidirectx.com, CS349D notes), sec. 5.2 and "Part 3: single
+# node" (random-liu.github.io), ch. 14 sec. 3: a preempted request's KV blocks
+# are copied to CPU memory (a CPU block allocator hands out the host blocks)
+# and copied back to GPU blocks when it resumes.  The copy is whole blocks;
+# the definition is the same as copy_blocks with the source and destination
+# in different pools.
+
+SWAP_OUT, SWAP_IN = 0, 1
+
+
+def swap_blocks(gpu_arrays, host_arrays, pairs, direction: int) -> int:
+    """For each (gpu_block, host_block) pair in order: host[h] <- gpu[g]
+    (SWAP_OUT) or gpu[g] <- host[h] (SWAP_IN), for every array of the pool
+    (K, V, and INT8 scales when present; leading axis = block).  Pairs naming a
+    block outside either pool are skipped and counted."""
+    ng, nh = gpu_arrays[0].shape[0], host_arrays[0].shape[0]
+    bad = 0
+    for g, h in np.asarray(pairs, dtype=np.int64).reshape(-1, 2):
+        if not (0 <= g < ng and 0 <= h < nh):
+            bad += 1
+            continue
+        for ga, ha in zip(gpu_arrays, host_arrays):
+            if direction == SWAP_OUT:
+                ha[h] = ga[g].copy()
+            else:
+                ga[g] = ha[h].copy()
+    return bad

@@ -483,3 +483,29 @@ long oracle_decode_q8(const void* q, int dtype, const uint8_t* k_codes, const ui
                       block_tables, max_blocks_per_seq, seq_lens, batch, num_q_heads, scale,
                       out, num_threads);
 }
+
+/*
+ * Swap to host ("Lecture 3", CS349D notes, sec. 5.2; "Part 3: single node",
+ * ch. 14 sec. 3): a preempted request's blocks go to CPU memory and come back
+ * when it resumes.  For each (gpu_block, host_block) pair in order, every
+ * array of the pool (n_arrays of them: K, V, and INT8 scales when present,
+ * block_bytes[a] bytes per block) is copied whole: host <- gpu (direction 0,
+ * out) or gpu <- host (direction 1, in).  Pairs outside either pool are
+ * skipped and counted.
+ */
+long oracle_swap_blocks(void* const* gpu, void* const* host, const long* block_bytes, int n_arrays,
+                        long num_gpu_blocks, long num_host_blocks, const int32_t* pairs,
+                        long num_pairs, int direction) {
+    long bad = 0;
+    for (long p = 0; p < num_pairs; ++p) {
+        long g = pairs[2 * p], h = pairs[2 * p + 1];
+        if (g < 0 || g >= num_gpu_blocks || h < 0 || h >= num_host_blocks) { ++bad; continue; }
+        for (int a = 0; a < n_arrays; ++a) {
+            char* gp = (char*)gpu[a] + (size_t)g * block_bytes[a];
+            char* hp = (char*)host[a] + (size_t)h * block_bytes[a];
+            if (direction == 0) memmove(hp, gp, (size_t)block_bytes[a]);
+            else memmove(gp, hp, (size_t)block_bytes[a]);
+        }
+    }
+    return bad;
+}

@@ -27,6 +27,10 @@ Sources (page title and section):
 * The kwkr.cn blog's toy ``KVCacheManager``: prefill takes ceil(L / bs)
   blocks, decode takes one more block exactly when the new token starts a
   block, and running out raises ``RuntimeError("OOM")``.
+* "Lecture 3", sec. 5.2 and "Part 3: single node", ch. 14 sec. 3: a preempted
+  request's blocks are swapped out to CPU memory, handed out by a CPU block
+  allocator, and swapped back in when it resumes; the swap space needed is
+  bounded by the GPU pool.
 """
 
 from __future__ import annotations
@@ -51,7 +55,8 @@ class BlockManager:
     """
 
     def __init__(self, num_blocks: int, block_size: int,
-                 free_order: Optional[Iterable[int]] = None, pop: str = "front"):
+                 free_order: Optional[Iterable[int]] = None, pop: str = "front",
+                 num_cpu_blocks: int = 0):
         if block_size < 1 or num_blocks < 0:
             raise ValueError("block_size must be >= 1 and num_blocks >= 0")
         if pop not in ("front", "back"):
@@ -66,6 +71,11 @@ class BlockManager:
         self.tables: Dict[int, List[int]] = {}
         self.lens: Dict[int, int] = {}
         self.copies_made = 0
+        # swap space: CPU blocks, their counts, and the sequences living there
+        self.num_cpu_blocks = num_cpu_blocks
+        self.cpu_free: List[int] = list(range(num_cpu_blocks))
+        self.cpu_ref: List[int] = [0] * num_cpu_blocks
+        self.swapped: set = set()
 
     # -- allocation ------------------------------------------------------
     def _take(self) -> int:
@@ -99,6 +109,56 @@ class BlockManager:
         self.lens[seq_id] = n_tokens
         return list(self.tables[seq_id])
 
+    # -- swap to host ----------------------------------------------------
+    def _group_blocks(self, seq_ids, on_cpu: bool) -> List[int]:
+        """Distinct blocks of the group's tables, in first-use order; every one
+        must be held by group members only (a block shared with a sequence
+        outside the group cannot move)."""
+        ids = list(seq_ids)
+        for sid in ids:
+            if (sid in self.swapped) != on_cpu:
+                raise ValueError(f"sequence {sid} is {'not ' if on_cpu else ''}swapped out")
+        held = Counter(b for sid in ids for b in self.tables[sid])
+        refs = self.cpu_ref if on_cpu else self.ref
+        for b, n in held.items():
+            if refs[b] != n:
+                raise ValueError(f"block {b} is shared outside the group")
+        return list(dict.fromkeys(b for sid in ids for b in self.tables[sid]))
+
+    def swap_out(self, seq_ids) -> List[Tuple[int, int]]:
+        """Move a group's blocks to CPU blocks (all or nothing); returns the
+        (gpu_block, cpu_block) pairs to copy device -> host, after which the
+        GPU blocks are free."""
+        blocks = self._group_blocks(seq_ids, on_cpu=False)
+        if len(blocks) > len(self.cpu_free):
+            raise OutOfBlocks(f"swap space: {len(blocks)} blocks needed")
+        cpu = {b: self.cpu_free.pop(0) for b in blocks}
+        for b in blocks:
+            self.cpu_ref[cpu[b]] = self.ref[b]
+            self.ref[b] = 0
+            self.free.append(b)
+        for sid in seq_ids:
+            self.tables[sid] = [cpu[b] for b in self.tables[sid]]
+            self.swapped.add(sid)
+        return [(b, cpu[b]) for b in blocks]
+
+    def swap_in(self, seq_ids) -> List[Tuple[int, int]]:
+        """Bring a swapped-out group back into fresh GPU blocks (all or
+        nothing); returns the (gpu_block, cpu_block) pairs to copy host ->
+        device, after which the CPU blocks are free."""
+        blocks = self._group_blocks(seq_ids, on_cpu=True)
+        if len(blocks) > len(self.free):
+            raise OutOfBlocks(f"swap-in: {len(blocks)} blocks needed")
+        gpu = {c: self._take() for c in blocks}
+        for c in blocks:
+            self.ref[gpu[c]] = self.cpu_ref[c]
+            self.cpu_ref[c] = 0
+            self.cpu_free.append(c)
+        for sid in seq_ids:
+            self.tables[sid] = [gpu[c] for c in self.tables[sid]]
+            self.swapped.discard(sid)
+        return [(gpu[c], c) for c in blocks]
+
     def append_slot(self, seq_id: int) -> Tuple[int, Optional[Tuple[int, int]]]:
         """Reserve the slot of the next token of ``seq_id``.
 
@@ -108,6 +168,8 @@ class BlockManager:
         a copy-on-write was planned (else ``None``).  The caller must run the
         copy before writing the slot.
         """
+        if seq_id in self.swapped:
+            raise ValueError(f"sequence {seq_id} is swapped out")
         table = self.tables[seq_id]
         pos = self.lens[seq_id]
         j = pos // self.block_size
@@ -135,8 +197,15 @@ class BlockManager:
 
     def free_seq(self, seq_id: int) -> None:
         """Drop a sequence; blocks whose count reaches zero return to the pool."""
-        for blk in self.tables.pop(seq_id):
-            self._release(blk)
+        if seq_id in self.swapped:
+            self.swapped.discard(seq_id)
+            for c in self.tables.pop(seq_id):
+                self.cpu_ref[c] -= 1
+                if self.cpu_ref[c] == 0:
+                    self.cpu_free.append(c)
+        else:
+            for blk in self.tables.pop(seq_id):
+                self._release(blk)
         del self.lens[seq_id]
 
     # -- views -----------------------------------------------------------
@@ -160,8 +229,15 @@ class BlockManager:
         return n
 
     def check_invariant(self) -> None:
-        """Tables holding each block == its reference count; free <=> count 0."""
-        holders = Counter(blk for t in self.tables.values() for blk in t)
+        """Tables holding each block == its reference count; free <=> count 0
+        (GPU blocks and, for swapped-out sequences, CPU blocks)."""
+        cpu_holders = Counter(c for sid, t in self.tables.items() if sid in self.swapped for c in t)
+        for c in range(self.num_cpu_blocks):
+            if cpu_holders.get(c, 0) != self.cpu_ref[c]:
+                raise AssertionError(f"cpu block {c}: held by {cpu_holders.get(c, 0)}, count {self.cpu_ref[c]}")
+            if (c in set(self.cpu_free)) != (self.cpu_ref[c] == 0):
+                raise AssertionError(f"cpu block {c}: free-list membership disagrees with count")
+        holders = Counter(blk for sid, t in self.tables.items() if sid not in self.swapped for blk in t)
         for blk in range(self.num_blocks):
             if holders.get(blk, 0) != self.ref[blk]:
                 raise AssertionError(
