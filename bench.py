@@ -76,6 +76,9 @@ def parse_args(argv=None):
     ap.add_argument("--kv-cache", choices=["fp8_e4m3", "int8"], default=None,
                     help="an 8-bit pool (quantising append, dequantising decode) instead of "
                          "the workload's 16-bit one")
+    ap.add_argument("--swap-frac", type=float, default=0.0,
+                    help="also time kv_swap_blocks out to pinned host memory and back for the "
+                         "blocks of this fraction of the sequences")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix workload: decode with the cascade entry point")
     return ap.parse_args(argv)
@@ -286,6 +289,52 @@ def pick_sample(host_w, budget_s, threads, q8=None):
     return np.sort(order[:n])
 
 
+def time_swap(pool, w, frac, flush, K, dev):
+    """kv_swap_blocks of every block of a fraction of the sequences: out to a
+    pinned host pool, then back into the same blocks (the pool is unchanged),
+    each timed with CUDA events after an L2 flush; beside it one contiguous
+    pinned-host copy of the same bytes each way (the link's ceiling)."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(4321)
+    seqs = np.sort(rng.permutation(w.batch)[:max(1, int(round(frac * w.batch)))])
+    blocks = [int(w.block_tables[b, j]) for b in seqs
+              for j in range(-(-int(w.seq_lens[b]) // w.block_size))]
+    n = len(blocks)
+    host = pool.host_pool(n)
+    pairs = torch.tensor([[g, i] for i, g in enumerate(blocks)], dtype=torch.int32, device=dev)
+    nbytes = sum(a[:n].numel() * a.element_size() for a in host if a is not None)
+    ref_host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    ref_dev = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ms = 0.0
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        return ms / K
+
+    out_ms = timed(lambda: pool.swap_out(host, pairs))
+    in_ms = timed(lambda: pool.swap_in(host, pairs))
+    d2h_ms = timed(lambda: ref_host.copy_(ref_dev, non_blocking=True))
+    h2d_ms = timed(lambda: ref_dev.copy_(ref_host, non_blocking=True))
+    assert pool.get_error() == 0, "device error word set during the swap timing"
+    gbs = lambda ms: round(nbytes / (ms * 1e-3) / 1e9, 2)
+    return {"sequences": int(seqs.shape[0]), "blocks": n, "bytes_per_direction": nbytes,
+            "launches_per_direction": 1, "out_ms": round(out_ms, 4), "in_ms": round(in_ms, 4),
+            "out_gbs": gbs(out_ms), "in_gbs": gbs(in_ms),
+            "contiguous_copy_gbs": {"d2h": gbs(d2h_ms), "h2d": gbs(h2d_ms)},
+            "host_memory": "pinned (cudaHostAlloc through torch), addressed by the kernel"}
+
+
 # --------------------------------------------------------------- our arm --
 
 def run_ours(args):
@@ -409,6 +458,10 @@ def run_ours(args):
     barrier()
     e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eve) / KE
 
+    swap = None
+    if args.swap_frac > 0:
+        swap = time_swap(pool, w, args.swap_frac, flush, K, dev)
+
     step_bytes = w.step_bytes() if q8 is None else q8.step_bytes(w)
     att_bytes = w.attention_bytes() if q8 is None else q8.attention_bytes(w)
     kv_bytes = w.kv_bytes() if q8 is None else q8.kv_bytes(w)
@@ -476,6 +529,7 @@ def run_ours(args):
                 "ms_per_step": round(max_e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,
+        **({"swap": swap} if swap is not None else {}),
         "gpu_launches": launches_per_step * K,
         "cpu_baseline": cpu,
     }

@@ -1,9 +1,10 @@
 /*
  * pagedkv.h -- C ABI of the paged KV cache hot path for NVIDIA GB300 (sm_103a).
  *
- * Three operations on a pool of fixed-size KV blocks:
+ * Operations on a pool of fixed-size KV blocks:
  *
  *   copy_blocks             batched copy-on-write block copies (src -> dst);
+ *   kv_swap_blocks          batched block moves to and from host memory;
  *   kv_append               slot-mapped write of each new token's K and V row
  *                           (the pages' reshape-and-cache step);
  *   paged_attention_decode  single-query attention per sequence, reading K and
@@ -166,6 +167,35 @@ kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
  *   sets KV_DEVERR_PAIR_RANGE.  num_pairs = 0 enqueues nothing.
  */
 kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void* stream);
+
+/*
+ * kv_swap_blocks -- move whole blocks between the pool and a host-memory pool
+ * of the same layout, all pairs in one launch ("Lecture 3", semidirectx.com
+ * CS349D notes, sec. 5.2 and "Part 3: single node", ch. 14 sec. 3: a
+ * preempted request's KV blocks are copied to CPU memory, handed out by a CPU
+ * block allocator, and copied back to GPU blocks when it resumes).
+ *
+ * host_k, host_v: [num_host_blocks, block_size, num_kv_heads, head_dim] of the
+ *   pool's element type (codes for an 8-bit pool), 16-byte aligned, in pinned
+ *   host memory the device can address (cudaHostAlloc / cudaHostRegister, or
+ *   managed memory); the kernel reads or writes it directly.
+ * host_k_scales, host_v_scales: INT8 pools only, fp32 [num_host_blocks,
+ *   num_kv_heads, block_size] in the same kind of memory; NULL otherwise.
+ * pairs: int32 [num_pairs, 2] = (pool block, host block), device-accessible.
+ *   KV_SWAP_OUT: host[h] <- pool[g]; KV_SWAP_IN: pool[g] <- host[h], codes and
+ *   scales alike.  Precondition: destination blocks are distinct and no
+ *   destination is a source of the same call.  A pair outside either pool is
+ *   skipped and sets KV_DEVERR_PAIR_RANGE.  num_pairs = 0 enqueues nothing.
+ * The host pool is read or written by the GPU when the stream reaches the
+ *   call: the host must not touch those blocks until the stream has passed it.
+ * Errors: KV_EINVAL (bad direction, pointer not device-accessible, misaligned,
+ *   scales given or missing), KV_ECUDA.
+ */
+#define KV_SWAP_OUT 0   /* device pool -> host pool */
+#define KV_SWAP_IN 1    /* host pool -> device pool */
+kv_status kv_swap_blocks(kv_pool_t pool, void* host_k, void* host_v, float* host_k_scales,
+                         float* host_v_scales, int num_host_blocks, const int32_t* pairs,
+                         int num_pairs, int direction, void* stream);
 
 /*
  * paged_attention_workspace_size -- bytes of device workspace that

@@ -304,6 +304,45 @@ kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void*
     return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "copy_blocks");
 }
 
+// Memory the device can address: device memory, or host memory that is
+// pinned (page-locked, mapped into the unified address space) or managed.
+static bool device_accessible(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+           (a.type == cudaMemoryTypeHost && a.devicePointer == p);
+}
+
+kv_status kv_swap_blocks(kv_pool_t pool, void* host_k, void* host_v, float* host_k_scales,
+                         float* host_v_scales, int num_host_blocks, const int32_t* pairs,
+                         int num_pairs, int direction, void* stream) {
+    if (!pool || num_pairs < 0 || num_pairs > (1 << 28) || num_host_blocks < 1) return KV_EINVAL;
+    if (direction != KV_SWAP_OUT && direction != KV_SWAP_IN) return KV_EINVAL;
+    if (num_pairs == 0) return KV_OK;
+    if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 7u) || !device_accessible(pairs))
+        return KV_EINVAL;
+    if (!host_k || !host_v || !aligned16(host_k) || !aligned16(host_v) ||
+        !device_accessible(host_k) || !device_accessible(host_v))
+        return KV_EINVAL;
+    if ((long long)num_host_blocks * pool->block_size >= (1ll << 31)) return KV_EINVAL;
+    if (pool->cache_dtype == KV_INT8) {
+        if (!host_k_scales || !host_v_scales || !aligned16(host_k_scales) ||
+            !aligned16(host_v_scales) || !device_accessible(host_k_scales) ||
+            !device_accessible(host_v_scales))
+            return KV_EINVAL;
+    } else if (host_k_scales || host_v_scales) {
+        return KV_EINVAL;
+    }
+    cudaError_t e = pagedkv::launch_swap_blocks(*pool, host_k, host_v, host_k_scales,
+                                                host_v_scales, num_host_blocks, pairs, num_pairs,
+                                                direction == KV_SWAP_OUT,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KV_OK : pagedkv::cuda_fail(e, "kv_swap_blocks");
+}
+
 static kv_status check_decode_shape(kv_pool_t pool, int batch, int num_q_heads) {
     if (!pool || batch < 1 || num_q_heads < 1) return KV_EINVAL;
     if (batch > pagedkv::kMaxBatch) return KV_EUNSUPPORTED;

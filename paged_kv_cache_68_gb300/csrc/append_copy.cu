@@ -199,6 +199,48 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(
     for (; i < blk16; i += 256) stg16(d + i, s[i]);
 }
 
+// Swap to host and back ("Lecture 3", semidirectx.com CS349D notes, sec. 5.2:
+// a preempted request's blocks go to CPU memory and return when it resumes):
+// one CTA per (pair, array), whole blocks with 16-byte accesses, the host side
+// addressed directly in pinned host memory (NVLink-C2C on Grace; no per-block
+// copy call).  out: host[h] <- gpu[g]; in: gpu[g] <- host[h].
+struct SwapArrays {
+    uint4* gpu[4];
+    uint4* host[4];
+    int blk16[4];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) swap_blocks_kernel(
+    const int32_t* __restrict__ pairs, int num_pairs, SwapArrays arrays, int num_gpu_blocks,
+    int num_host_blocks, int to_host, int* __restrict__ err) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int pair = blockIdx.x / arrays.n;
+    const int a = blockIdx.x % arrays.n;
+    if (pair >= num_pairs) return;
+    const int g = pairs[2 * pair], h = pairs[2 * pair + 1];
+    if (g < 0 || g >= num_gpu_blocks || h < 0 || h >= num_host_blocks) {
+        if (threadIdx.x == 0 && a == 0) atomicOr(err, KV_DEVERR_PAIR_RANGE);
+        return;
+    }
+    const int blk16 = arrays.blk16[a];
+    uint4* gp = arrays.gpu[a] + (size_t)g * blk16;
+    uint4* hp = arrays.host[a] + (size_t)h * blk16;
+    const uint4* s = to_host ? gp : hp;
+    uint4* d = to_host ? hp : gp;
+    int i = threadIdx.x;
+    for (; i + 3 * 256 < blk16; i += 4 * 256) {
+        const uint4 x0 = ldg_nc16(s + i), x1 = ldg_nc16(s + i + 256);
+        const uint4 x2 = ldg_nc16(s + i + 512), x3 = ldg_nc16(s + i + 768);
+        stg16(d + i, x0);
+        stg16(d + i + 256, x1);
+        stg16(d + i + 512, x2);
+        stg16(d + i + 768, x3);
+    }
+    for (; i < blk16; i += 256) stg16(d + i, ldg_nc16(s + i));
+}
+
 cudaLaunchConfig_t pdl_config(int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -272,6 +314,35 @@ cudaError_t launch_copy_blocks(const kv_pool& pool, const int32_t* pairs, int nu
     pdl_attr(cfg, attr);
     return cudaLaunchKernelEx(&cfg, copy_blocks_kernel, pairs, num_pairs, arr, pool.num_blocks,
                               pool.d_err);
+}
+
+cudaError_t launch_swap_blocks(const kv_pool& pool, void* host_k, void* host_v,
+                               float* host_k_scales, float* host_v_scales, int num_host_blocks,
+                               const int32_t* pairs, int num_pairs, bool to_host,
+                               cudaStream_t stream) {
+    if (num_pairs <= 0) return cudaSuccess;
+    SwapArrays arr = {};
+    const int blk16 = pool.block_size * pool.num_kv_heads * pool.head_dim * pool.elem_bytes / 16;
+    arr.gpu[0] = static_cast<uint4*>(pool.k);
+    arr.gpu[1] = static_cast<uint4*>(pool.v);
+    arr.host[0] = static_cast<uint4*>(host_k);
+    arr.host[1] = static_cast<uint4*>(host_v);
+    arr.blk16[0] = arr.blk16[1] = blk16;
+    arr.n = 2;
+    if (pool.cache_dtype == KV_INT8) {
+        arr.gpu[2] = reinterpret_cast<uint4*>(pool.k_scales);
+        arr.gpu[3] = reinterpret_cast<uint4*>(pool.v_scales);
+        arr.host[2] = reinterpret_cast<uint4*>(host_k_scales);
+        arr.host[3] = reinterpret_cast<uint4*>(host_v_scales);
+        arr.blk16[2] = arr.blk16[3] = pool.block_size * pool.num_kv_heads * 4 / 16;
+        arr.n = 4;
+    }
+    if ((long long)arr.n * num_pairs > 0x7fffffffll) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = pdl_config(arr.n * num_pairs, stream);
+    cudaLaunchAttribute attr;
+    pdl_attr(cfg, attr);
+    return cudaLaunchKernelEx(&cfg, swap_blocks_kernel, pairs, num_pairs, arr, pool.num_blocks,
+                              num_host_blocks, to_host ? 1 : 0, pool.d_err);
 }
 
 }  // namespace pagedkv

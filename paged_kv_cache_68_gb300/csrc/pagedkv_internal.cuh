@@ -79,6 +79,11 @@ cudaError_t launch_append(const kv_pool& pool, const void* k_new, const void* v_
 cudaError_t launch_copy_blocks(const kv_pool& pool, const int32_t* pairs, int num_pairs,
                                cudaStream_t stream);
 
+cudaError_t launch_swap_blocks(const kv_pool& pool, void* host_k, void* host_v,
+                               float* host_k_scales, float* host_v_scales, int num_host_blocks,
+                               const int32_t* pairs, int num_pairs, bool to_host,
+                               cudaStream_t stream);
+
 struct DecodeCall {
     const void* q;
     void* out;

@@ -7,7 +7,7 @@ fails, an exception is raised.
 
 The module-level functions carry the C names (``kv_pool_create``,
 ``kv_pool_create_quantized``,
-``kv_append``, ``copy_blocks``, ``paged_attention_workspace_size``,
+``kv_append``, ``copy_blocks``, ``kv_swap_blocks``, ``paged_attention_workspace_size``,
 ``paged_attention_decode``, ``paged_attention_cascade_workspace_size``,
 ``paged_attention_decode_cascade``, ``paged_attention_decode_noalloc``,
 ``kv_pool_get_error``, ``kv_pool_clear_error``, ``kv_pool_destroy``);
@@ -76,6 +76,7 @@ def load(build: bool = True) -> ctypes.CDLL:
             "paged_attention_decode": ([P, P, P, P, I, P, I, I, F, I, P, S, P], I),
             "paged_attention_cascade_workspace_size": ([P, I, I, I, ctypes.POINTER(S)], I),
             "paged_attention_decode_cascade": ([P, P, P, P, I, P, I, I, F, I, P, P, P, I, P, S, P], I),
+            "kv_swap_blocks": ([P, P, P, P, P, I, P, I, I, P], I),
             "kv_pool_get_error": ([P, ctypes.POINTER(I)], I),
             "kv_pool_clear_error": ([P], I),
             "kv_strerror": ([I], ctypes.c_char_p),
@@ -169,6 +170,28 @@ def copy_blocks(handle, pairs, stream=None) -> None:
     n = int(pairs.shape[0]) if pairs.numel() else 0
     ptr = _dev(pairs, "pairs", torch.int32) if n else None
     _check(load().copy_blocks(handle, ptr, n, _stream(stream)), "copy_blocks")
+
+
+KV_SWAP_OUT, KV_SWAP_IN = 0, 1
+
+
+def _host(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous pinned host tensor")
+    return t.data_ptr()
+
+
+def kv_swap_blocks(handle, host_k, host_v, pairs, direction: int, host_k_scales=None,
+                   host_v_scales=None, stream=None) -> None:
+    """Move whole blocks between the pool and pinned host pools of the same
+    layout: pairs int32 [P, 2] = (pool block, host block), on the device."""
+    n = int(pairs.shape[0]) if pairs.numel() else 0
+    ptr = _dev(pairs, "pairs", torch.int32) if n else None
+    hs = lambda t, nm: None if t is None else _host(t, nm)
+    _check(load().kv_swap_blocks(handle, _host(host_k, "host_k"), _host(host_v, "host_v"),
+                                 hs(host_k_scales, "host_k_scales"),
+                                 hs(host_v_scales, "host_v_scales"), int(host_k.shape[0]), ptr, n,
+                                 int(direction), _stream(stream)), "kv_swap_blocks")
 
 
 def paged_attention_workspace_size(handle, batch: int, num_q_heads: int) -> int:
@@ -267,6 +290,26 @@ class KVPool:
 
     def copy_blocks(self, pairs, stream=None) -> None:
         copy_blocks(self.handle, pairs, stream)
+
+    def host_pool(self, num_host_blocks: int):
+        """Pinned host arrays of this pool's layout for swapped-out blocks:
+        (k, v, k_scales, v_scales); the scales are None unless INT8."""
+        shape = (num_host_blocks, self.block_size, self.num_kv_heads, self.head_dim)
+        k = torch.empty(shape, dtype=self.k_pool.dtype, pin_memory=True)
+        v = torch.empty(shape, dtype=self.k_pool.dtype, pin_memory=True)
+        ks = vs = None
+        if self.cache == "int8":
+            sshape = (num_host_blocks, self.num_kv_heads, self.block_size)
+            ks = torch.empty(sshape, dtype=torch.float32, pin_memory=True)
+            vs = torch.empty(sshape, dtype=torch.float32, pin_memory=True)
+        return k, v, ks, vs
+
+    def swap_out(self, host, pairs, stream=None) -> None:
+        """host = host_pool(...); pairs (pool block, host block) on the device."""
+        kv_swap_blocks(self.handle, host[0], host[1], pairs, KV_SWAP_OUT, host[2], host[3], stream)
+
+    def swap_in(self, host, pairs, stream=None) -> None:
+        kv_swap_blocks(self.handle, host[0], host[1], pairs, KV_SWAP_IN, host[2], host[3], stream)
 
     def workspace(self, batch: int, num_q_heads: int) -> torch.Tensor:
         """A cached device workspace large enough for (batch, num_q_heads)."""
