@@ -69,6 +69,8 @@ def _load():
             lib.oracle_decode_q8.restype = L
             lib.oracle_swap_blocks.argtypes = [P, P, P, I, L, L, P, L, I]
             lib.oracle_swap_blocks.restype = L
+            lib.oracle_prefill.argtypes = [P, P, P, I, L, L, L, L, P, P, L, P, L, L, D, P, I]
+            lib.oracle_prefill.restype = L
             _lib = lib
     return _lib
 
@@ -194,3 +196,24 @@ def swap_blocks(gpu_arrays, host_arrays, pairs, direction: int) -> int:
     pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
     return _load().oracle_swap_blocks(gp, hp, bb, n, gpu_arrays[0].shape[0], host_arrays[0].shape[0],
                                       _ptr(pr), pr.shape[0], int(direction))
+
+
+# ------------------------------------------------- paged (chunked) prefill --
+
+def prefill(q, k_pool, v_pool, dtype: str, cu_seqlens, block_tables, seq_lens, scale: float,
+            num_kv_heads: int, num_threads: int = 1, return_status: bool = False):
+    """fp64 out [T, Hq, D] (see ``oracle_prefill``)."""
+    T, Hq, D = q.shape
+    nb, bs, hkv, d = k_pool.shape
+    assert hkv == num_kv_heads and d == D
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    st = _load().oracle_prefill(_ptr(np.ascontiguousarray(q)), _ptr(k_pool), _ptr(v_pool),
+                                _DTYPE_CODE[dtype], nb, bs, hkv, D, _ptr(cu), _ptr(bt),
+                                bt.shape[1], _ptr(sl), sl.shape[0], Hq, float(scale), _ptr(out),
+                                int(num_threads))
+    if st < 0:
+        raise ValueError("oracle_prefill rejected its arguments")
+    return (out, st) if return_status else out

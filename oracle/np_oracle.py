@@ -362,3 +362,46 @@ def swap_blocks(gpu_arrays, host_arrays, pairs, direction: int) -> int:
             else:
                 ga[g] = ha[h].copy()
     return bad
+
+
+# ------------------------------------------------- paged (chunked) prefill --
+#
+# "Part 3: single node" (random-liu.github.io), ch. 13 sec. 1 and 2: the new
+# tokens of every request in a batch are flattened into one stream whose
+# request boundaries are cu_seqlens; a long prompt is cut into chunks of at
+# most a token budget, processed one chunk per iteration, and a chunk's
+# attention reads the earlier part of the prompt (and any cached prefix)
+# through the block table, like decode.  Reading taken where the pages stop:
+# request b's C_b = cu_seqlens[b+1] - cu_seqlens[b] queries are its last C_b
+# positions, L_b - C_b .. L_b - 1 (L_b = seq_lens[b], the context after the
+# chunk's own K/V were appended), and query i attends causally to positions
+# 0 .. L_b - C_b + i.  C_b = 1 is decode.
+
+def prefill(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, dtype: str,
+            cu_seqlens: np.ndarray, block_tables: np.ndarray, seq_lens: np.ndarray,
+            scale: float, num_kv_heads: int) -> np.ndarray:
+    """q [T, Hq, D] raw (T = cu_seqlens[-1]) -> fp64 out [T, Hq, D]."""
+    T, Hq, D = q.shape
+    group = Hq // num_kv_heads
+    qf = to_f64(q, dtype)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        C = int(cu[b + 1] - cu[b])
+        L = int(seq_lens[b])
+        if C <= 0 or L <= 0:
+            continue
+        K = to_f64(gather_kv(k_pool, block_tables[b], L), dtype)          # [L, Hkv, D]
+        V = to_f64(gather_kv(v_pool, block_tables[b], L), dtype)
+        for i in range(C):
+            p = L - C + i                                                   # query position
+            if p < 0:
+                continue
+            for g in range(num_kv_heads):
+                heads = slice(g * group, (g + 1) * group)
+                s = scale * (qf[cu[b] + i, heads] @ K[:p + 1, g, :].T)     # [group, p + 1]
+                s = s - s.max(axis=1, keepdims=True)
+                w = np.exp(s)
+                w = w / w.sum(axis=1, keepdims=True)
+                out[cu[b] + i, heads] = w @ V[:p + 1, g, :]
+    return out

@@ -509,3 +509,118 @@ long oracle_swap_blocks(void* const* gpu, void* const* host, const long* block_b
     }
     return bad;
 }
+
+/*
+ * Paged (chunked) prefill ("Part 3: single node", ch. 13 sec. 1-2): request
+ * b's C_b = cu_seqlens[b+1] - cu_seqlens[b] queries (rows cu_seqlens[b] ..
+ * of q and out) are its last C_b positions of L_b = seq_lens[b]; query i
+ * attends to positions 0 .. L_b - C_b + i through the block table.  Same
+ * fp64 gather-then-softmax as oracle_decode; requests are independent and may
+ * go to separate threads.  Returns the count of invalid table entries / too
+ * long lengths met (skipped), or -1 on bad arguments / no memory.
+ */
+typedef struct {
+    const void* q; const void* k_pool; const void* v_pool; int dtype;
+    long num_blocks, block_size, num_kv_heads, head_dim;
+    const int32_t* cu; const int32_t* block_tables; long max_blocks_per_seq;
+    const int32_t* seq_lens; long num_q_heads; double scale; double* out;
+    long b_begin, b_end; long bad;
+} prefill_job;
+
+static void* prefill_worker(void* arg) {
+    prefill_job* J = (prefill_job*)arg;
+    long bs = J->block_size, Hkv = J->num_kv_heads, D = J->head_dim, Hq = J->num_q_heads;
+    long group = Hq / Hkv, maxL = J->max_blocks_per_seq * bs;
+    double* kbuf = (double*)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1) * D);
+    double* vbuf = (double*)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1) * D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
+    long* pos = (long*)malloc(sizeof(long) * (size_t)(maxL > 0 ? maxL : 1));
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!kbuf || !vbuf || !s || !pos || !qv) { J->bad = -1; goto done; }
+    for (long b = J->b_begin; b < J->b_end; ++b) {
+        long C = J->cu[b + 1] - J->cu[b], L = J->seq_lens[b];
+        if (C <= 0 || L <= 0) continue;
+        if (L > maxL) { J->bad++; L = maxL; }
+        const int32_t* table = J->block_tables + b * J->max_blocks_per_seq;
+        for (long g = 0; g < Hkv; ++g) {
+            /* gather positions 0..L-1 of kv head g (skipping invalid blocks) */
+            long n = 0;
+            for (long t = 0; t < L; ++t) {
+                long phys = table[t / bs];
+                if (phys < 0 || phys >= J->num_blocks) { J->bad++; continue; }
+                size_t row = (((size_t)phys * bs + t % bs) * Hkv + g) * D;
+                for (long d = 0; d < D; ++d) {
+                    kbuf[n * D + d] = load_elem(J->k_pool, row + d, J->dtype);
+                    vbuf[n * D + d] = load_elem(J->v_pool, row + d, J->dtype);
+                }
+                pos[n++] = t;
+            }
+            for (long i = 0; i < C; ++i) {
+                long p = J->seq_lens[b] - C + i;       /* query position */
+                long row_q = J->cu[b] + i;
+                for (long hh = 0; hh < group; ++hh) {
+                    long h = g * group + hh;
+                    double* o = J->out + ((size_t)row_q * Hq + h) * D;
+                    for (long d = 0; d < D; ++d) o[d] = 0.0;
+                    if (p < 0) continue;
+                    for (long d = 0; d < D; ++d)
+                        qv[d] = load_elem(J->q, ((size_t)row_q * Hq + h) * D + d, J->dtype);
+                    long m = 0;
+                    double mx = -INFINITY;
+                    for (long t = 0; t < n && pos[t] <= p; ++t, ++m) {
+                        double acc = 0.0;
+                        for (long d = 0; d < D; ++d) acc += qv[d] * kbuf[t * D + d];
+                        s[t] = J->scale * acc;
+                        if (s[t] > mx) mx = s[t];
+                    }
+                    if (m == 0) continue;
+                    double den = 0.0;
+                    for (long t = 0; t < m; ++t) { s[t] = exp(s[t] - mx); den += s[t]; }
+                    for (long t = 0; t < m; ++t) {
+                        double w = s[t] / den;
+                        for (long d = 0; d < D; ++d) o[d] += w * vbuf[t * D + d];
+                    }
+                }
+            }
+        }
+    }
+done:
+    free(kbuf); free(vbuf); free(s); free(pos); free(qv);
+    return NULL;
+}
+
+long oracle_prefill(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                    long num_blocks, long block_size, long num_kv_heads, long head_dim,
+                    const int32_t* cu_seqlens, const int32_t* block_tables, long max_blocks_per_seq,
+                    const int32_t* seq_lens, long batch, long num_q_heads, double scale,
+                    double* out, int num_threads) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 ||
+        head_dim <= 0 || batch < 0)
+        return -1;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > batch) num_threads = batch > 0 ? (int)batch : 1;
+    prefill_job* jobs = (prefill_job*)calloc((size_t)num_threads, sizeof(prefill_job));
+    pthread_t* tids = (pthread_t*)calloc((size_t)num_threads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return -1; }
+    for (int i = 0; i < num_threads; ++i) {
+        prefill_job* J = &jobs[i];
+        J->q = q; J->k_pool = k_pool; J->v_pool = v_pool; J->dtype = dtype;
+        J->num_blocks = num_blocks; J->block_size = block_size; J->num_kv_heads = num_kv_heads;
+        J->head_dim = head_dim; J->cu = cu_seqlens; J->block_tables = block_tables;
+        J->max_blocks_per_seq = max_blocks_per_seq; J->seq_lens = seq_lens;
+        J->num_q_heads = num_q_heads; J->scale = scale; J->out = out;
+        J->b_begin = batch * i / num_threads; J->b_end = batch * (i + 1) / num_threads;
+    }
+    if (num_threads == 1) prefill_worker(&jobs[0]);
+    else {
+        for (int i = 0; i < num_threads; ++i) pthread_create(&tids[i], NULL, prefill_worker, &jobs[i]);
+        for (int i = 0; i < num_threads; ++i) pthread_join(tids[i], NULL);
+    }
+    long bad = 0;
+    for (int i = 0; i < num_threads; ++i) {
+        if (jobs[i].bad < 0) { bad = -1; break; }
+        bad += jobs[i].bad;
+    }
+    free(jobs); free(tids);
+    return bad;
+}

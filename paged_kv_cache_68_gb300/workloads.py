@@ -62,10 +62,13 @@ class Workload:
     # sequences sharing prefix blocks: int32 [K, 3] (first member, members,
     # shared leading blocks), or None
     groups: Optional[np.ndarray] = None
+    # chunked prefill: int32 [B + 1] query boundaries in the flattened q /
+    # k_new / v_new / slot_mapping (None: one query per sequence)
+    cu_seqlens: Optional[np.ndarray] = None
 
     @property
     def batch(self) -> int:
-        return int(self.q.shape[0])
+        return int(self.seq_lens.shape[0])
 
     @property
     def elem_bytes(self) -> int:
@@ -95,7 +98,16 @@ class Workload:
         return self.attention_bytes() + self.append_bytes() + self.copy_bytes()
 
     def attention_flops(self) -> int:
-        return int(self.seq_lens.astype(np.int64).sum()) * self.num_q_heads * self.head_dim * 4
+        """QK and PV multiply-adds (x2) over every (query, visible token) pair."""
+        if self.cu_seqlens is None:
+            return int(self.seq_lens.astype(np.int64).sum()) * self.num_q_heads * self.head_dim * 4
+        pairs = 0
+        for b in range(self.batch):
+            C = int(self.cu_seqlens[b + 1] - self.cu_seqlens[b])
+            L = int(self.seq_lens[b])
+            # query i sees L - C + i + 1 tokens
+            pairs += C * (L - C + 1) + C * (C - 1) // 2
+        return pairs * self.num_q_heads * self.head_dim * 4
 
 
 # -- element helpers ---------------------------------------------------------
@@ -330,6 +342,79 @@ def long_context(seed: int = 0, batch: int = 8, lo: int = 32768, hi: int = 13107
     return build_step(f"long_context_bs{block_size}", seed, ctx, dtype="bf16", num_q_heads=32,
                       num_kv_heads=8, head_dim=128, block_size=block_size, rng=rng,
                       device=device)
+
+
+def chunked_prefill_step(name: str, seed: int, prefix_lens, chunk_lens, *, dtype: str,
+                         num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                         pool_factor: float = 1.5, scale: Optional[float] = None,
+                         rng: Optional[np.random.Generator] = None,
+                         device: Optional[str] = None) -> Workload:
+    """One chunked-prefill step: request b has prefix_lens[b] tokens cached
+    and a chunk of chunk_lens[b] new tokens (1 = a decode request).  The step
+    appends the chunk's K/V through its slots (blocks taken on demand, as
+    decode does) and attends each of its chunk_lens[b] queries causally over
+    the prefix and the chunk.  Draw order: placement permutation, cached K
+    rows, cached V rows, q, new K rows, new V rows."""
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    pre = np.asarray(prefix_lens, dtype=np.int64)
+    chk = np.asarray(chunk_lens, dtype=np.int64)
+    B, bs = pre.shape[0], block_size
+    need = int(sum(-(-int(pre[b] + chk[b]) // bs) for b in range(B)))
+    N = max(need, int(math.ceil(pool_factor * need)))
+    bm = BlockManager(N, bs, free_order=rng.permutation(N).tolist())
+    for b in range(B):
+        bm.allocate_prompt(b, int(pre[b]))
+    inner = (num_kv_heads, head_dim)
+    val = _values(seed, rng, dtype, device)
+    k_pool = val.nan((N, bs) + inner)
+    v_pool = val.nan((N, bs) + inner)
+    rows = np.concatenate([_token_rows(bm.tables[b], int(pre[b]), bs) for b in range(B)]
+                          + [np.zeros(0, np.int64)])
+    val.fill_rows(k_pool, rows)
+    val.fill_rows(v_pool, rows)
+    T = int(chk.sum())
+    q = val.randn((T, num_q_heads, head_dim))
+    k_new = val.randn((T,) + inner)
+    v_new = val.randn((T,) + inner)
+    slots = []
+    for b in range(B):
+        for _ in range(int(chk[b])):
+            slot, cow = bm.append_slot(b)
+            assert cow is None
+            slots.append(slot)
+    bm.check_invariant()
+    seq_lens = (pre + chk).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(chk)]).astype(np.int32)
+    w = Workload(
+        name=name, dtype=dtype, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=bs, num_blocks=N,
+        scale=scale if scale is not None else 1.0 / math.sqrt(head_dim),
+        k_pool=k_pool, v_pool=v_pool, q=q, k_new=k_new, v_new=v_new,
+        slot_mapping=np.asarray(slots, dtype=np.int64),
+        block_tables=_tables_array(bm, list(range(B)), None),
+        seq_lens=seq_lens, pairs=np.zeros((0, 2), np.int32), cu_seqlens=cu)
+    w.info = {"seed": seed, "tokens": int(seq_lens.sum()), "query_tokens": T,
+              "max_query_len": int(chk.max()) if B else 0}
+    return w
+
+
+def chunked_prefill(seed: int = 0, batch: int = 16, chunk: int = 256, max_prefix: int = 3840,
+                    decodes: int = 0, block_size: int = 16,
+                    device: Optional[str] = None) -> Workload:
+    """Chunked prefill, Llama-3-8B GQA shape (bf16, bs 16): ``batch`` requests
+    with a chunk of ``chunk`` prompt tokens each after a cached prefix of
+    U[0, max_prefix] tokens (the earlier chunks of the same prompt), plus
+    ``decodes`` decode requests (one query, lognormal context as the
+    Llama-3-8B step) packed into the same batch."""
+    rng = np.random.default_rng(seed)
+    pre = rng.integers(0, max_prefix, size=batch, endpoint=True)
+    chk = np.full(batch, chunk, np.int64)
+    if decodes:
+        pre = np.concatenate([pre, llama3_context_lens(rng, decodes)])
+        chk = np.concatenate([chk, np.ones(decodes, np.int64)])
+    return chunked_prefill_step("chunked_prefill", seed, pre, chk, dtype="bf16", num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, block_size=block_size, rng=rng,
+                                device=device)
 
 
 def shared_prefix(seed: int = 0, prompts: int = 32, prompt_len: int = 2000, n: int = 4,
