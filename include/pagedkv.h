@@ -83,6 +83,10 @@ typedef enum {
 #define KV_DEVERR_TIMEOUT      0x10 /* a pipeline wait gave up (work was skipped)    */
 #define KV_DEVERR_GROUP_RANGE  0x20 /* cascade: a group outside the batch, overlapping
                                        or out of order (its sharing is ignored)       */
+#define KV_DEVERR_QUERY_RANGE  0x40 /* prefill: cu_seqlens decreasing or past
+                                       num_tokens (the request is skipped), or a
+                                       request with more than max_query_len queries
+                                       (the queries past it are not computed)         */
 
 typedef struct kv_pool* kv_pool_t;
 
@@ -280,6 +284,49 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
                                          const int32_t* group_size,
                                          const int32_t* group_shared_blocks, int num_groups,
                                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * paged_attention_prefill -- paged (chunked) prefill attention: several query
+ * tokens per request, each attending causally to the request's cached tokens
+ * and to the chunk's earlier tokens, K and V read through the block table
+ * inside the kernel ("Part 3: single node", random-liu.github.io, ch. 13
+ * sec. 1-2: the new tokens of a batch are flattened into one stream with
+ * request boundaries cu_seqlens; a long prompt is processed one chunk per
+ * iteration and a chunk attends to the cached earlier chunks through the
+ * block table, as decode does).
+ *
+ * q, out: device [num_tokens, num_q_heads, head_dim] of the pool dtype; the
+ *   queries of request b are rows cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ * cu_seqlens: device int32 [batch + 1], non-decreasing, cu_seqlens[batch] <=
+ *   num_tokens.  C_b = cu_seqlens[b+1] - cu_seqlens[b] queries for request b.
+ * seq_lens: device int32 [batch]: L_b, the request's context length counted
+ *   after this chunk's own K/V rows were appended (kv_append first).  The
+ *   C_b queries are positions L_b - C_b .. L_b - 1, and query i sees
+ *   positions 0 .. L_b - C_b + i.  C_b = 1 is one decode query.  A query
+ *   whose position is negative (C_b > L_b) sees nothing and its output is 0.
+ * block_tables: device int32 [batch, max_blocks_per_seq], as for decode.
+ * max_query_len: an upper bound on every C_b (1 <= max_query_len <=
+ *   num_tokens); it sizes the grid.
+ * scale: > 0 and finite.  Arithmetic: fp32 scores and softmax on the tensor
+ *   cores (products of 16-bit inputs, fp32 accumulation; the probabilities
+ *   enter the second product as two 16-bit halves, so they keep fp32-level
+ *   accuracy); one rounding of each output to the pool dtype.
+ * Limits: 16-bit pools (KV_F16 or KV_BF16; not 8-bit pools), head_dim 128,
+ *   block_size a power of two in [8, 128], num_q_heads / num_kv_heads in
+ *   {1, 2, 4, 8}, batch <= 65535.  num_tokens = 0 is a no-op.
+ * Needs no workspace.  Output rows of queries that no request covers are not
+ *   written.
+ * Errors: KV_EINVAL (null, misaligned, num_kv_heads differing from the pool,
+ *   scale not > 0, max_query_len out of range), KV_EUNSUPPORTED, KV_ECUDA.
+ *   Device error bits: KV_DEVERR_QUERY_RANGE (malformed cu_seqlens, or
+ *   C_b > max_query_len), KV_DEVERR_BLOCK_RANGE, KV_DEVERR_SEQ_RANGE (L_b
+ *   larger than the table holds: clamped), KV_DEVERR_TIMEOUT.
+ */
+kv_status paged_attention_prefill(kv_pool_t pool, const void* q, void* out,
+                                  const int32_t* cu_seqlens, int num_tokens, int max_query_len,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* seq_lens, int batch, int num_q_heads,
+                                  float scale, int num_kv_heads, void* stream);
 
 /*
  * paged_attention_decode_noalloc -- paged_attention_decode without a

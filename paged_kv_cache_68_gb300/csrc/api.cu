@@ -70,6 +70,18 @@ constexpr size_t kMaxSmem = 227 * 1024;
 
 namespace pagedkv {
 
+bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base,
+                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                      bool swizzle128) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    return enc(map, dt, (cuuint32_t)rank, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 kv_status cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where,
                   cudaGetErrorString(e));

@@ -59,6 +59,28 @@ constexpr int kMaxGroups = 1024;   // cascade decode: groups per call
 // Record the text of a failed CUDA call for kv_last_cuda_error; returns KV_ECUDA.
 kv_status cuda_fail(cudaError_t e, const char* where);
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (element
+// strides 1, no interleave, optional 128-byte swizzle, 256-byte L2 fills).
+bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base,
+                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                      bool swizzle128);
+
+// Paged prefill: the tcgen05 kernel's launcher (one per query type).
+struct PrefillCall {
+    const void* q;
+    void* out;
+    const int32_t* cu_seqlens;
+    int num_tokens;
+    int max_query_len;
+    const int32_t* block_tables;
+    int max_blocks;
+    const int32_t* seq_lens;
+    int batch;
+    int num_q_heads;
+    float scale;
+};
+cudaError_t launch_prefill(const kv_pool& pool, const PrefillCall& call, cudaStream_t stream);
+
 // The split decode after a cascade prefix pass: the groups, and that pass's
 // states in the workspace; `plain_ws_bytes` is the part of the workspace the
 // split kernel itself uses (at its start).

@@ -9,7 +9,8 @@ The module-level functions carry the C names (``kv_pool_create``,
 ``kv_pool_create_quantized``,
 ``kv_append``, ``copy_blocks``, ``kv_swap_blocks``, ``paged_attention_workspace_size``,
 ``paged_attention_decode``, ``paged_attention_cascade_workspace_size``,
-``paged_attention_decode_cascade``, ``paged_attention_decode_noalloc``,
+``paged_attention_decode_cascade``, ``paged_attention_prefill``,
+``paged_attention_decode_noalloc``,
 ``kv_pool_get_error``, ``kv_pool_clear_error``, ``kv_pool_destroy``);
 ``KVPool`` bundles them for convenience.
 """
@@ -32,6 +33,7 @@ KV_DEVERR_PAIR_RANGE = 0x4
 KV_DEVERR_SEQ_RANGE = 0x8
 KV_DEVERR_TIMEOUT = 0x10
 KV_DEVERR_GROUP_RANGE = 0x20
+KV_DEVERR_QUERY_RANGE = 0x40
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 KV_FP8_E4M3, KV_INT8 = 3, 4
@@ -77,6 +79,7 @@ def load(build: bool = True) -> ctypes.CDLL:
             "paged_attention_cascade_workspace_size": ([P, I, I, I, ctypes.POINTER(S)], I),
             "paged_attention_decode_cascade": ([P, P, P, P, I, P, I, I, F, I, P, P, P, I, P, S, P], I),
             "kv_swap_blocks": ([P, P, P, P, P, I, P, I, I, P], I),
+            "paged_attention_prefill": ([P, P, P, P, I, I, P, I, P, I, I, F, I, P], I),
             "kv_pool_get_error": ([P, ctypes.POINTER(I)], I),
             "kv_pool_clear_error": ([P], I),
             "kv_strerror": ([I], ctypes.c_char_p),
@@ -237,6 +240,21 @@ def paged_attention_decode_cascade(handle, q, out, block_tables, seq_lens, scale
         _stream(stream)), "paged_attention_decode_cascade")
 
 
+def paged_attention_prefill(handle, q, out, cu_seqlens, max_query_len: int, block_tables,
+                            seq_lens, scale: float, num_kv_heads: int, dtype,
+                            stream=None) -> None:
+    """q, out [T, Hq, D]; cu_seqlens int32 [B + 1]; seq_lens int32 [B]
+    (context after the chunk's append); block_tables int32 [B, max_blocks]."""
+    t, hq, _ = q.shape
+    b = int(seq_lens.numel())
+    _check(load().paged_attention_prefill(
+        handle, _dev(q, "q", dtype), _dev(out, "out", dtype),
+        _dev(cu_seqlens, "cu_seqlens", torch.int32), int(t), int(max_query_len),
+        _dev(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), b, int(hq), float(scale), int(num_kv_heads),
+        _stream(stream)), "paged_attention_prefill")
+
+
 def kv_pool_get_error(handle) -> int:
     bits = ctypes.c_int()
     st = load().kv_pool_get_error(handle, ctypes.byref(bits))
@@ -345,6 +363,15 @@ class KVPool:
         paged_attention_decode_cascade(self.handle, q, out, block_tables, seq_lens, scale,
                                        self.num_kv_heads, cols[0], cols[1], cols[2], workspace,
                                        self.dtype, stream)
+        return out
+
+    def prefill(self, q, cu_seqlens, max_query_len: int, block_tables, seq_lens, scale: float,
+                out=None, stream=None) -> torch.Tensor:
+        """Chunked prefill attention of the flattened queries ``q`` [T, Hq, D]."""
+        if out is None:
+            out = torch.empty_like(q)
+        paged_attention_prefill(self.handle, q, out, cu_seqlens, max_query_len, block_tables,
+                                seq_lens, scale, self.num_kv_heads, self.dtype, stream)
         return out
 
     def get_error(self) -> int:

@@ -157,3 +157,49 @@ def assert_q8_pools_equal(got, want, what=""):
         else:
             ok = (g.view(np.uint32) == r.view(np.uint32)) | (np.isnan(g) & np.isnan(r))
             assert ok.all(), f"{what}: {name} differ at {np.flatnonzero(~ok.reshape(-1))[:5]}"
+
+
+# -- paged (chunked) prefill -----------------------------------------------------
+
+def gpu_prefill_step(w: wl.Workload, device="cuda", max_query_len=None, return_pools=True):
+    """kv_append of the chunks' K/V -> paged_attention_prefill through the C ABI.
+    Returns (k_pool, v_pool, out, error_bits) as raw host arrays."""
+    tv = lambda a: wl.value_to_torch(a, w.dtype, device)
+    k, v = tv(w.k_pool).clone(), tv(w.v_pool).clone()
+    q, kn, vn = tv(w.q), tv(w.k_new), tv(w.v_new)
+    slots = torch.from_numpy(w.slot_mapping).to(device)
+    tables = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device)
+    lens = torch.from_numpy(w.seq_lens).to(device)
+    cu = torch.from_numpy(np.ascontiguousarray(w.cu_seqlens, dtype=np.int32)).to(device)
+    mq = int(np.diff(w.cu_seqlens).max()) if max_query_len is None else max_query_len
+    pool = pagedkv.KVPool(k, v)
+    try:
+        pool.append(kn, vn, slots)
+        out = torch.zeros_like(q)
+        pool.prefill(q, cu, mq, tables, lens, w.scale, out=out)
+        torch.cuda.synchronize()
+        err = pool.get_error()
+    finally:
+        pool.close()
+    res = wl.value_to_numpy(out, w.dtype)
+    if not return_pools:
+        return None, None, res, err
+    return wl.value_to_numpy(k, w.dtype), wl.value_to_numpy(v, w.dtype), res, err
+
+
+def oracle_prefill_step(w: wl.Workload, requests=None):
+    """The same step on the C oracle.  Returns (k_pool, v_pool, out, rows):
+    `out` holds the rows of `requests` (every request if None), `rows` their
+    indices in the flattened query stream."""
+    h = wl.on_host(w)
+    k, v = h.k_pool.copy(), h.v_pool.copy()
+    assert c_oracle.append(k, v, h.k_new, h.v_new, h.slot_mapping, h.dtype) == 0
+    cu = np.asarray(h.cu_seqlens, dtype=np.int64)
+    reqs = np.arange(h.batch) if requests is None else np.asarray(requests)
+    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in reqs] + [np.zeros(0, np.int64)])
+    sub_cu = np.concatenate([[0], np.cumsum([cu[b + 1] - cu[b] for b in reqs])]).astype(np.int32)
+    out = c_oracle.prefill(np.ascontiguousarray(h.q[rows]), k, v, h.dtype, sub_cu,
+                           np.ascontiguousarray(h.block_tables[reqs]),
+                           np.ascontiguousarray(h.seq_lens[reqs]), h.scale, h.num_kv_heads,
+                           num_threads=ORACLE_THREADS)
+    return k, v, out, rows
