@@ -51,7 +51,12 @@ WORKLOAD_TEXT = {
                      "2000 tokens, n = 4 samples, 0-256 divergent tokens, CoW copies + append + attention",
     "long_context": "long-context split-KV decode: 32/8 heads, head_dim 128, bf16, batch 8, "
                     "context ~ U[32768, 131072], block_size 16",
+    "chunked_prefill": "chunked prefill step: Llama-3-8B GQA shape (32/8 heads, head_dim 128, bf16, "
+                       "block_size 16), 16 requests x 256-token chunks after cached prefixes of "
+                       "U[0, 3840] tokens, blocks scattered in a pool 1.5x the need, 1 layer, "
+                       "append of the chunks + causal paged prefill attention",
 }
+PREFILL_METRIC = "paged chunked-prefill attention: TFLOP/s (% of GB300 bf16 tensor peak), query tokens/s"
 
 
 # ------------------------------------------------------------------ helpers --
@@ -81,11 +86,15 @@ def parse_args(argv=None):
                          "blocks of this fraction of the sequences")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix workload: decode with the cascade entry point")
+    ap.add_argument("--decodes", type=int, default=0,
+                    help="chunked-prefill workload: decode requests packed into the batch")
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="chunked-prefill workload: tokens per chunk (default 256)")
     return ap.parse_args(argv)
 
 
 def make_workload(name: str, seed: int, device, placement: str = "random", batch=None,
-                  block_size=None, prompt_len=None):
+                  block_size=None, prompt_len=None, decodes=0, chunk=None):
     from paged_kv_cache_68_gb300 import workloads as wl
     kw = {} if batch is None else {"batch": batch}
     if name == "llama3_8b_gqa":
@@ -98,6 +107,10 @@ def make_workload(name: str, seed: int, device, placement: str = "random", batch
         if prompt_len is not None:
             kw["prompt_len"] = prompt_len
         return wl.shared_prefix(seed, device=device, **kw)
+    if name == "chunked_prefill":
+        if chunk is not None:
+            kw["chunk"] = chunk
+        return wl.chunked_prefill(seed, decodes=decodes, device=device, **kw)
     if name == "long_context":
         if block_size is not None:
             kw["block_size"] = block_size
@@ -131,22 +144,94 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    """SM clock and throttle reasons sampled while the timed region runs.
 
+    NVML (read-only queries through ctypes) every 2 ms on a background thread;
+    ``mark()`` takes one more sample synchronously (call it after the timed
+    work is enqueued, while the GPU runs it), so even a region of a few
+    milliseconds has samples.  Only samples between ``begin()`` and ``stop()``
+    count.  Falls back to ``nvidia-smi -lms 200`` when NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id: str):
-        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        import ctypes
+        import threading
+        self.samples, self.t0, self.proc, self.nvml = [], None, None, None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            assert lib.nvmlInit_v2() == 0
+            h = ctypes.c_void_p()
+            if gpu_id.startswith("GPU-"):
+                assert lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(h)) == 0
+            else:
+                assert lib.nvmlDeviceGetHandleByIndex_v2(int(gpu_id), ctypes.byref(h)) == 0
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))   # 1 = NVML_CLOCK_SM
+            self.nvml, self.h, self.reasons_fn, self.max_mhz = lib, h, reasons_fn, float(mx.value)
+            self.ctypes = ctypes
+            self.stop_ev = threading.Event()
+            self.lock = threading.Lock()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.nvml = None
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "200", "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
+            except OSError:
+                self.proc = None
+
+    def _read(self):
+        c = self.ctypes
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) != 0:
+            return None
+        self.reasons_fn(self.h, c.byref(rs))
+        return (time.perf_counter(), float(mhz.value), int(rs.value))
+
+    def _loop(self):
+        while not self.stop_ev.is_set():
+            r = self._read()
+            if r is not None:
+                with self.lock:
+                    self.samples.append(r)
+            time.sleep(0.002)
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def mark(self):
+        if self.nvml is not None:
+            r = self._read()
+            if r is not None:
+                with self.lock:
+                    self.samples.append(r)
 
     def stop(self):
+        t1 = time.perf_counter()
+        if self.nvml is not None:
+            self.stop_ev.set()
+            self.thread.join(timeout=2)
+            t0 = self.t0 if self.t0 is not None else 0.0
+            with self.lock:
+                inside = [s for s in self.samples if t0 <= s[0] <= t1]
+            reasons = set()
+            for _, _, bits in inside:
+                for bit, name in self.REASONS.items():
+                    if bits & bit:
+                        reasons.add(name)
+            sm = [s[1] for s in inside]
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -173,7 +258,7 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 def gpu_uuid(dev) -> str:
@@ -420,6 +505,7 @@ def run_ours(args):
     sampler = ClockSampler(gpu_uuid(dev))
     barrier()
     torch.cuda.synchronize()
+    sampler.begin()
     for i in range(K):
         flush.zero_()                                   # L2 flush, outside the events
         e = ev[i]
@@ -430,6 +516,7 @@ def run_ours(args):
         decode()
         e[2].record()
         e[3].record()
+    sampler.mark()                                      # the GPU is running the queued steps
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
@@ -535,6 +622,230 @@ def run_ours(args):
     }
 
 
+# ------------------------------------------------------- chunked prefill --
+
+def measured_tensor_peak():
+    """Dense bf16 tensor peak: the burst figure (a kernel timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def oracle_prefill_sample(host_w, reqs, threads):
+    """One oracle prefill step (append + attention) restricted to requests
+    `reqs`; returns (seconds, algorithmic flops of the sample)."""
+    import numpy as np
+    from oracle import c_oracle
+    cu = host_w.cu_seqlens.astype(np.int64)
+    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in reqs])
+    sub_cu = np.concatenate([[0], np.cumsum([cu[b + 1] - cu[b] for b in reqs])]).astype(np.int32)
+    k, v = host_w.k_pool, host_w.v_pool          # appends are idempotent
+    t0 = time.perf_counter()
+    c_oracle.append(k, v, host_w.k_new[rows], host_w.v_new[rows], host_w.slot_mapping[rows],
+                    host_w.dtype)
+    c_oracle.prefill(np.ascontiguousarray(host_w.q[rows]), k, v, host_w.dtype, sub_cu,
+                     np.ascontiguousarray(host_w.block_tables[reqs]),
+                     np.ascontiguousarray(host_w.seq_lens[reqs]), host_w.scale,
+                     host_w.num_kv_heads, num_threads=threads)
+    dt = time.perf_counter() - t0
+    sub = copy.copy(host_w)
+    sub.cu_seqlens, sub.seq_lens = sub_cu, host_w.seq_lens[reqs]
+    return dt, sub.attention_flops()
+
+
+def pick_prefill_sample(host_w, budget_s, threads):
+    """Requests (a prefix of a fixed shuffle) whose oracle step takes about budget_s."""
+    import numpy as np
+    order = np.random.default_rng(1234).permutation(host_w.batch)
+    n = 1
+    dt, _ = oracle_prefill_sample(host_w, order[:n], threads)
+    if dt < budget_s and n < host_w.batch:
+        n = int(min(host_w.batch, max(n, n * budget_s / max(dt, 1e-3))))
+    return np.sort(order[:n])
+
+
+def run_prefill(args):
+    """kv_append of the chunks -> paged_attention_prefill, inputs resident in
+    HBM; the roofline is the tensor pipe (algorithmic QK and PV flops)."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_68_gb300 import pagedkv
+    from paged_kv_cache_68_gb300 import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pagedkv.load()
+    w = make_workload(args.workload, args.seed, dev, batch=args.batch, decodes=args.decodes,
+                      chunk=args.chunk)
+    tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
+    srcs = {"q": tv(w.q), "k_new": tv(w.k_new), "v_new": tv(w.v_new),
+            "slots": torch.from_numpy(w.slot_mapping).to(dev),
+            "tables": torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev),
+            "lens": torch.from_numpy(w.seq_lens).to(dev),
+            "cu": torch.from_numpy(np.ascontiguousarray(w.cu_seqlens, dtype=np.int32)).to(dev)}
+    offs, total = {}, 0
+    for n, t in srcs.items():
+        offs[n] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    dev_in = torch.empty(total, dtype=torch.uint8, device=dev)
+    view = {}
+    for n, t in srcs.items():
+        nb = t.numel() * t.element_size()
+        view[n] = dev_in[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+        view[n].copy_(t)
+    host_in = dev_in.cpu().pin_memory()
+    pool = pagedkv.KVPool(w.k_pool, w.v_pool)
+    out = torch.empty_like(view["q"])
+    maxq = int(np.diff(w.cu_seqlens).max())
+
+    def append():
+        pool.append(view["k_new"], view["v_new"], view["slots"])
+
+    def prefill():
+        pool.prefill(view["q"], view["cu"], maxq, view["tables"], view["lens"], w.scale, out=out)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        append()
+        prefill()
+    torch.cuda.synchronize()
+    assert pool.get_error() == 0, "device error word set during warm-up"
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid(dev))
+    barrier()
+    torch.cuda.synchronize()
+    sampler.begin()
+    for i in range(K):
+        flush.zero_()                                   # L2 flush, outside the events
+        e = ev[i]
+        e[0].record()
+        append()
+        e[1].record()
+        prefill()
+        e[2].record()
+    sampler.mark()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+    pf_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    assert pool.get_error() == 0, "device error word set during the timed steps"
+
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    KE = max(1, min(args.e2e_steps, K))
+    eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(KE):
+        flush.zero_()
+        eve[i][0].record()
+        dev_in.copy_(host_in, non_blocking=True)
+        append()
+        prefill()
+        out_host.copy_(out, non_blocking=True)
+        eve[i][1].record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eve) / KE
+
+    flops = w.attention_flops()
+    max_step_ms, total_flops = reduce_max_sum(step_ms, flops)
+    max_pf_ms, _ = reduce_max_sum(pf_ms, flops)
+    max_e2e_ms, _ = reduce_max_sum(e2e_ms, flops)
+    qtok = int(w.info["query_tokens"]) * world
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (pf_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_w = wl.on_host(w)
+        threads = os.cpu_count() or 1
+        reqs = pick_prefill_sample(host_w, 10.0, threads)
+        dt, fl, passes = 0.0, 0, 0
+        while passes < 2 or dt < 5.0:
+            t, f = oracle_prefill_sample(host_w, reqs, threads)
+            dt, fl, passes = dt + t, fl + f, passes + 1
+        cpu = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{len(reqs)} of {w.batch} requests of the same step (append + causal "
+                         f"prefill attention, fp64 C oracle), {passes} passes, {dt:.1f} s"}
+    pool.close()
+    if rank != 0:
+        return None
+    return {
+        "metric": PREFILL_METRIC, "value": round(total_flops / (max_step_ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(max_step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload]
+                   + ("" if args.batch is None else f" (requests overridden to {args.batch})")
+                   + ("" if args.chunk is None else f" (chunk {args.chunk})")
+                   + ("" if not args.decodes else f", + {args.decodes} decode requests"),
+                   "seed": args.seed, "global_batch": w.batch * world,
+                   "query_tokens_per_replica": int(w.info["query_tokens"]),
+                   "context_tokens_per_replica": int(w.seq_lens.sum()),
+                   "attention_flops_per_replica": flops,
+                   "l2": "flushed (512 MB write) between timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "query_tokens_per_s": round(qtok / (max_step_ms * 1e-3), 1),
+        "attention_tflops": round(total_flops / (max_pf_ms * 1e-3) / 1e12, 2),
+        "roofline": {"bound": "tensor",
+                     "kernel": "paged_prefill (tcgen05; the whole prefill call, one kernel)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind} (bf16 burst)",
+                     "traffic": None, "algorithmic_flops": flops},
+        "e2e": {"value": round(total_flops / (max_e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(max_e2e_ms, 5),
+                "h2d_bytes_per_step": int(host_in.numel()),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+        "clocks": clocks,
+        "gpu_launches": 2 * K,
+        "cpu_baseline": cpu,
+    }
+
+
+def run_prefill_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    import torch
+
+    from oracle import c_oracle
+    from paged_kv_cache_68_gb300 import workloads as wl
+    c_oracle.build()
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    w = wl.on_host(make_workload(args.workload, args.seed, dev, batch=args.batch,
+                                 decodes=args.decodes, chunk=args.chunk))
+    threads = os.cpu_count() or 1
+    per_step = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    reqs = pick_prefill_sample(w, per_step, threads)
+    for _ in range(args.warmup):
+        oracle_prefill_sample(w, reqs, threads)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        dt, f = oracle_prefill_sample(w, reqs, threads)
+        tot_t, tot_f = tot_t + dt, tot_f + f
+    value = tot_f / tot_t / 1e12
+    sample = (f"{len(reqs)} of {w.batch} requests per step (append + causal prefill attention, "
+              f"fp64 C oracle), {args.steps} steps")
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+        "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 # -------------------------------------------------------- reference arm --
 
 def run_reference(args):
@@ -584,7 +895,10 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.workload == "chunked_prefill":
+        res = run_prefill_reference(args) if args.impl == "reference" else run_prefill(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

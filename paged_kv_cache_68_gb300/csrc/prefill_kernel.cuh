@@ -22,14 +22,20 @@
 //   S  = Q K^T      tcgen05.mma, A = Q (smem), B = K tile (smem), D = TMEM
 //   P  = exp2(S * scale * log2 e - m)            (softmax warps, fp32)
 //   O += P V        tcgen05.mma, A = P (TMEM), B = V tile (smem), D = TMEM
-// P is stored in TMEM as 16-bit hi + lo halves (P = hi + lo to 2^-17
-// relative) and multiplied twice, so the result keeps fp32-level accuracy.
+// P overwrites S in TMEM as 16-bit hi + lo halves (P = hi + lo to 2^-16
+// relative) and is multiplied twice, so the result keeps fp32-level accuracy.
 // The running maximum is updated lazily: O and the sum are rescaled only when
 // a row's maximum grows by more than 2^8, so P stays below 256.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Two CTAs share an SM (96 KB of shared memory and 256 TMEM columns each):
+// one CTA's softmax runs while the other's products occupy the tensor pipe,
+// which hides the serial S -> softmax -> PV chain of each tile.
+//
+// Warp roles (192 threads):
 //   warps 0-3  softmax and epilogue; thread r owns row r (TMEM lane r);
-//   warp 4     TMA producer: Q once, then K and V tiles into a 2-stage ring;
+//   warp 4     TMA producer: Q once, then the K and V tiles (one buffer each:
+//              K_{j+1} lands while tile j's softmax and PV run, V_{j+1} while
+//              S_{j+1} and its softmax run);
 //   warp 5     TMEM allocation and the single MMA-issuing thread.
 // Every mbarrier wait is bounded; a wait that gives up sets KV_DEVERR_TIMEOUT,
 // raises the CTA's abort flag, and the CTA drains its copies and MMAs, frees
@@ -50,25 +56,24 @@ using dec::FULL;
 constexpr int D = 128;            // head_dim
 constexpr int BM = 128;           // rows of a tile
 constexpr int BN = 128;           // tokens of a KV tile
-constexpr int STAGES = 2;         // K/V ring depth
 constexpr int NSOFT = 4;          // softmax warps = TMEM lane quadrants
 constexpr int WARP_TMA = 4, WARP_MMA = 5;
 constexpr int NTHREADS = 6 * 32;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_O = 128, COL_PH = 256, COL_PL = 320;
+constexpr int CTAS_PER_SM = 2;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t COL_S = 0, COL_O = 128;    // P (hi, then lo) overwrites S
+constexpr uint32_t COL_PH = COL_S, COL_PL = COL_S + 64;
 constexpr float kRescaleLog2 = 8.f;   // lazy rescale threshold (log2 units)
 
 constexpr uint32_t HALF_BYTES = 128u * 128u;    // 128 rows x 128 B (64 dims)
 constexpr uint32_t TILE_BYTES = 2u * HALF_BYTES;
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_RING = TILE_BYTES;
-constexpr uint32_t STAGE_BYTES = 2u * TILE_BYTES;  // K tile then V tile
-constexpr uint32_t OFF_BAR = OFF_RING + STAGES * STAGE_BYTES;
-// barriers (8 B each): q_full, k_full[S], v_full[S], kv_empty[S], s_full,
-// s_free, p_full, o_full, drain; then the TMEM address and the abort flag
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_VF = BAR_KF + STAGES, BAR_KE = BAR_VF + STAGES,
-              BAR_SF = BAR_KE + STAGES, BAR_SR = BAR_SF + 1, BAR_PF = BAR_SR + 1,
-              BAR_OF = BAR_PF + 1, BAR_DR = BAR_OF + 1, NBARS = BAR_DR + 1;
+constexpr uint32_t OFF_K = TILE_BYTES;
+constexpr uint32_t OFF_V = 2u * TILE_BYTES;
+constexpr uint32_t OFF_BAR = 3u * TILE_BYTES;
+// barriers (8 B each), then the TMEM address and the abort flag
+constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 2, BAR_VF = 3, BAR_VE = 4, BAR_SF = 5,
+              BAR_PF = 6, BAR_OF = 7, BAR_DR = 8, NBARS = 9;
 constexpr uint32_t OFF_TMEM = OFF_BAR + 8u * NBARS;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4u;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4u + 1024u;   // + slack to align the base to 1 KB
@@ -157,6 +162,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24)
         : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 PKV_W8(0)
+                 : "memory");
+}
 #undef PKV_R8
 #undef PKV_W8
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -180,6 +191,16 @@ template <> struct H16<__nv_bfloat16> {
     __device__ static __forceinline__ float high(uint32_t w) {
         return __uint_as_float(w & 0xffff0000u);
     }
+    // p = hi + lo: hi keeps the top 16 bits of each fp32 (truncation, exact
+    // remainder), lo is the remainder rounded to bf16 (|error| <= 2^-16 p)
+    __device__ static __forceinline__ void split(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+        hi = __byte_perm(b0, b1, 0x7632);
+        const float2 r = __ffma2_rn(make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                                __uint_as_float(b1 & 0xffff0000u)),
+                                    make_float2(-1.f, -1.f), make_float2(p0, p1));
+        lo = pack(r.x, r.y);
+    }
 };
 template <> struct H16<__half> {
     static constexpr uint32_t kFmt = 0;
@@ -194,12 +215,24 @@ template <> struct H16<__half> {
     __device__ static __forceinline__ float high(uint32_t w) {
         return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
     }
+    // p = hi + lo: hi rounded to f16, lo the remainder rounded to f16
+    __device__ static __forceinline__ void split(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+        hi = pack(p0, p1);
+        lo = pack(p0 - low(hi), p1 - high(hi));
+    }
 };
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // Bounded wait; on expiry (or when another role already gave up) raise the
 // abort flag and return false.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, int* err) {
+    if (dec::mbar_try(bar, parity)) return true;
     if (*abort_flag) return false;
     if (dec::mbar_wait(bar, parity)) return true;
     *abort_flag = 1;
@@ -208,7 +241,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 template <typename T, int G>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     paged_prefill(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
@@ -249,17 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // -- set-up: barriers, TMEM ----------------------------------------------
     if (tid == 0) {
-        dec::mbar_init(bar(BAR_Q), 1);
-        for (int s = 0; s < STAGES; ++s) {
-            dec::mbar_init(bar(BAR_KF + s), 1);
-            dec::mbar_init(bar(BAR_VF + s), 1);
-            dec::mbar_init(bar(BAR_KE + s), 1);
-        }
-        dec::mbar_init(bar(BAR_SF), 1);
-        dec::mbar_init(bar(BAR_SR), NSOFT);
-        dec::mbar_init(bar(BAR_PF), NSOFT);
-        dec::mbar_init(bar(BAR_OF), 1);
-        dec::mbar_init(bar(BAR_DR), 1);
+        for (int i = 0; i < NBARS; ++i) dec::mbar_init(bar(i), i == BAR_PF ? NSOFT : 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -279,7 +302,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ------------------------------------------------------ producer ----
         const int nb_tile = BN / bs;               // pool blocks per KV tile (<= 16)
         const uint32_t blk_bytes = (uint32_t)bs * 128u;   // one block, one 64-dim half
-        int issued = 0;
+        int issued_k = 0, issued_v = 0;
         if (ntiles > 0) {
             if (lane == 0) {
                 dec::mbar_arrive_tx(bar(BAR_Q), TILE_BYTES);
@@ -288,49 +311,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                  bar(BAR_Q));
             }
             const int32_t* table = p.block_tables + (size_t)b * p.max_blocks;
-            for (int j = 0; j < ntiles; ++j) {
-                const int s = j % STAGES, ph = j / STAGES;
-                bool ok = true;
-                if (lane == 0 && ph > 0)
-                    ok = wait_or_abort(bar(BAR_KE + s), (ph - 1) & 1, abort_flag, p.err);
-                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
+            // one KV tile into one buffer: the lanes' blocks, bytes counted first
+            auto load_tile = [&](int j, int full, uint32_t dst, const CUtensorMap* map) {
                 const int lb = j * nb_tile + lane;  // logical block of this lane
                 int id = -1;
                 bool load = false;
                 if (lane < nb_tile && lb * bs < L) {
                     id = table[lb];
                     load = id >= 0 && id < p.num_blocks;
-                    if (!load) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                    if (!load && map == &tmap_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
                 }
                 const unsigned mask = __ballot_sync(FULL, load);
-                const uint32_t bytes = (uint32_t)__popc(mask) * 2u * blk_bytes;
-                if (lane == 0) {
-                    dec::mbar_arrive_tx(bar(BAR_KF + s), bytes);
-                    dec::mbar_arrive_tx(bar(BAR_VF + s), bytes);
-                }
+                if (lane == 0) dec::mbar_arrive_tx(bar(full), (uint32_t)__popc(mask) * 2u * blk_bytes);
                 __syncwarp();
                 if (load) {
-                    const uint32_t kd = sbase + OFF_RING + (uint32_t)s * STAGE_BYTES +
-                                        (uint32_t)lane * blk_bytes;
-                    const uint32_t vd = kd + TILE_BYTES;
-                    const int row = id * bs;
-                    dec::tma_load_3d(kd, &tmap_k, 0, g, row, bar(BAR_KF + s));
-                    dec::tma_load_3d(kd + HALF_BYTES, &tmap_k, 64, g, row, bar(BAR_KF + s));
-                    dec::tma_load_3d(vd, &tmap_v, 0, g, row, bar(BAR_VF + s));
-                    dec::tma_load_3d(vd + HALF_BYTES, &tmap_v, 64, g, row, bar(BAR_VF + s));
+                    const uint32_t d = dst + (uint32_t)lane * blk_bytes;
+                    dec::tma_load_3d(d, map, 0, g, id * bs, bar(full));
+                    dec::tma_load_3d(d + HALF_BYTES, map, 64, g, id * bs, bar(full));
                 }
-                issued = j + 1;
+            };
+            // K_j needs S_{j-1} done (k_empty), V_j needs PV_{j-1} done (v_empty);
+            // K runs one tile ahead of V
+            for (int j = 0; j < ntiles; ++j) {
+                bool ok = true;
+                if (lane == 0 && j > 0)
+                    ok = wait_or_abort(bar(BAR_KE), (j - 1) & 1, abort_flag, p.err);
+                if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
+                load_tile(j, BAR_KF, sbase + OFF_K, &tmap_k);
+                issued_k = j + 1;
+                if (lane == 0 && j > 0)
+                    ok = wait_or_abort(bar(BAR_VE), (j - 1) & 1, abort_flag, p.err);
+                if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
+                load_tile(j, BAR_VF, sbase + OFF_V, &tmap_v);
+                issued_v = j + 1;
             }
             // Drain: no copy may still be landing in shared memory at exit.
             if (lane == 0) {
-                if (!dec::mbar_wait(bar(BAR_Q), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
-                for (int j = max(0, issued - STAGES); j < issued; ++j) {
-                    const int s = j % STAGES, par = (j / STAGES) & 1;
-                    if (!dec::mbar_wait(bar(BAR_KF + s), par) ||
-                        !dec::mbar_wait(bar(BAR_VF + s), par))
-                        atomicOr(p.err, KV_DEVERR_TIMEOUT);
-                }
+                bool ok = dec::mbar_wait(bar(BAR_Q), 0);
+                if (issued_k > 0) ok &= dec::mbar_wait(bar(BAR_KF), (issued_k - 1) & 1);
+                if (issued_v > 0) ok &= dec::mbar_wait(bar(BAR_VF), (issued_v - 1) & 1);
+                if (!ok) atomicOr(p.err, KV_DEVERR_TIMEOUT);
             }
         }
     } else if (warp == WARP_MMA) {
@@ -339,35 +359,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t fmt = H16<T>::kFmt;
             constexpr uint32_t id_s = idesc_f16(fmt, 0, BM, BN);   // S = Q K^T
             constexpr uint32_t id_pv = idesc_f16(fmt, 1, BM, D);   // O += P V (V MN-major)
-            const uint32_t q_addr = sbase + OFF_Q;
+            const uint32_t q_addr = sbase + OFF_Q, k_addr = sbase + OFF_K, v_addr = sbase + OFF_V;
             bool ok = wait_or_abort(bar(BAR_Q), 0, abort_flag, p.err);
-            int done_pv = 0;                       // PV products issued
-            auto pv = [&](int jj) -> bool {
-                const int s = jj % STAGES, par = (jj / STAGES) & 1;
-                if (!wait_or_abort(bar(BAR_PF), jj & 1, abort_flag, p.err)) return false;
-                if (!wait_or_abort(bar(BAR_VF + s), par, abort_flag, p.err)) return false;
-                tc_fence_after();
-                const uint32_t v_addr = sbase + OFF_RING + (uint32_t)s * STAGE_BYTES + TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 tokens = two 8-row swizzle atoms; the two 64-dim halves
-                    // are HALF_BYTES apart (leading byte offset)
-                    const uint64_t vdesc = sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF_BYTES, 1024u);
-                    mma_ts(tmem + COL_O, tmem + COL_PH + (uint32_t)kk * 8u, vdesc, id_pv,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tmem + COL_O, tmem + COL_PL + (uint32_t)kk * 8u, vdesc, id_pv, 1u);
-                }
-                mma_commit(bar(BAR_KE + s));
-                mma_commit(bar(BAR_OF));
-                done_pv = jj + 1;
-                return true;
-            };
             for (int j = 0; ok && j < ntiles; ++j) {
-                const int s = j % STAGES, par = (j / STAGES) & 1;
-                if (!wait_or_abort(bar(BAR_KF + s), par, abort_flag, p.err)) break;
-                if (j > 0 && !wait_or_abort(bar(BAR_SR), (j - 1) & 1, abort_flag, p.err)) break;
+                const uint32_t par = j & 1;
+                // S_j overwrites P_{j-1}: PV_{j-1} must have finished reading it
+                if (j > 0 && !wait_or_abort(bar(BAR_OF), par ^ 1u, abort_flag, p.err)) break;
+                if (!wait_or_abort(bar(BAR_KF), par, abort_flag, p.err)) break;
                 tc_fence_after();
-                const uint32_t k_addr = sbase + OFF_RING + (uint32_t)s * STAGE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // 16 dims = 32 bytes inside a 128-byte swizzled row
@@ -375,10 +374,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     mma_ss(tmem + COL_S, sdesc_sw128(q_addr + off, 16u, 1024u),
                            sdesc_sw128(k_addr + off, 16u, 1024u), id_s, kk > 0 ? 1u : 0u);
                 }
+                mma_commit(bar(BAR_KE));
                 mma_commit(bar(BAR_SF));
-                if (j > 0 && !pv(j - 1)) break;
+                if (!wait_or_abort(bar(BAR_PF), par, abort_flag, p.err)) break;
+                if (!wait_or_abort(bar(BAR_VF), par, abort_flag, p.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    // 16 tokens = two 8-row swizzle atoms; the two 64-dim halves
+                    // are HALF_BYTES apart (leading byte offset)
+                    const uint64_t vdesc = sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF_BYTES, 1024u);
+                    mma_ts(tmem + COL_O, tmem + COL_PH + (uint32_t)kk * 8u, vdesc, id_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + COL_O, tmem + COL_PL + (uint32_t)kk * 8u, vdesc, id_pv, 1u);
+                }
+                mma_commit(bar(BAR_VE));
+                mma_commit(bar(BAR_OF));
             }
-            if (ok && *abort_flag == 0 && done_pv == ntiles - 1) pv(ntiles - 1);
             // Drain: every MMA issued has completed before TMEM is freed.
             mma_commit(bar(BAR_DR));
             if (!dec::mbar_wait(bar(BAR_DR), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
@@ -392,7 +404,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int lim = valid ? P0 + qi : -1;      // last visible position
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         const float qs = p.qscale;
-        float m = -CUDART_INF_F, l = 0.f;
+        float m = -CUDART_INF_F;
+        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // partial row sums
         bool ok = true;
         // tcgen05.ld / st are warp-collective: every wait's outcome is made
         // uniform across the warp
@@ -400,17 +413,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
         };
         for (int j = 0; j < ntiles; ++j) {
-            const int s = j % STAGES;
             const int t0 = j * BN;
+            // S_j complete (and with it PV_{j-1}: the commit covers every
+            // earlier product)
             if (!wait_warp(bar(BAR_SF), j & 1)) { ok = false; break; }
             tc_fence_after();
             uint32_t sv[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(trow + COL_S + 32u * c, sv[c]);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) dec::mbar_arrive(bar(BAR_SR));
             // causal / length mask: tokens past `lim` do not exist for this row
             if (t0 + BN - 1 > lim) {
 #pragma unroll
@@ -419,11 +430,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int e = 0; e < 32; ++e)
                         if (t0 + 32 * c + e > lim) sv[c][e] = __float_as_uint(-CUDART_INF_F);
             }
-            float mx = -CUDART_INF_F;
+            // row maximum: four independent chains of three-input maxima
+            float mx4[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int i = 0; i < 4; ++i)
+                mx4[i] = fmaxf(__uint_as_float(sv[i][0]), __uint_as_float(sv[i][1]));
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 2; e < 32; e += 2)
+                    mx4[i] = max3(mx4[i], __uint_as_float(sv[i][e]), __uint_as_float(sv[i][e + 1]));
+            const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
             const float m_new = fmaxf(m, mx * qs);
             float alpha = 1.f;
             const bool grow = m_new > m + kRescaleLog2;   // false while both are -inf
@@ -432,29 +449,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 m = m_new;
             }
             const float mu = m == -CUDART_INF_F ? 0.f : m;
-            l *= alpha;
-            // P = hi + lo, packed in pairs (token 2i in the low half)
-            uint32_t ph[64], pl[64];
+            l2[0] = __fmul2_rn(l2[0], make_float2(alpha, alpha));
+            l2[1] = __fmul2_rn(l2[1], make_float2(alpha, alpha));
+            // P = hi + lo over S's columns (S was read in full above), 16
+            // tokens at a time
+            const float2 qs2 = make_float2(qs, qs), nmu2 = make_float2(-mu, -mu);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 8; ++c) {
+                uint32_t ph[8], pl[8];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = dec::fast_exp2(fmaf(__uint_as_float(sv[c][e]), qs, -mu));
-                    const float p1 = dec::fast_exp2(fmaf(__uint_as_float(sv[c][e + 1]), qs, -mu));
-                    l += p0 + p1;
-                    const uint32_t h = H16<T>::pack(p0, p1);
-                    ph[16 * c + e / 2] = h;
-                    pl[16 * c + e / 2] = H16<T>::pack(p0 - H16<T>::low(h), p1 - H16<T>::high(h));
+                for (int e = 0; e < 16; e += 2) {
+                    const uint32_t* sc = sv[c >> 1] + 16 * (c & 1);
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(sc[e]), __uint_as_float(sc[e + 1])), qs2, nmu2);
+                    const float2 pp = make_float2(dec::fast_exp2(x.x), dec::fast_exp2(x.y));
+                    l2[(e >> 1) & 1] = __fadd2_rn(l2[(e >> 1) & 1], pp);
+                    H16<T>::split(pp.x, pp.y, ph[e / 2], pl[e / 2]);
                 }
+                tmem_st8(trow + COL_PH + 8u * c, ph);
+                tmem_st8(trow + COL_PL + 8u * c, pl);
+            }
+            // O was last written by PV_{j-1}; rescale it when any row's maximum grew
+            // (after P, so S's registers are free)
+            if (j > 0 && __any_sync(FULL, grow)) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(trow + COL_O + 32u * c, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(trow + COL_O + 32u * c, ov);
+                }
+            }
             // the last tile: zero V rows past the sequence end (P is 0 there,
             // but 0 x NaN from an unwritten row would poison the product)
             if (t0 + BN > L) {
-                if (!wait_warp(bar(BAR_VF + s), (j / STAGES) & 1)) {
-                    ok = false;
-                    break;
-                }
+                if (!wait_warp(bar(BAR_VF), j & 1)) { ok = false; break; }
                 const int r0 = max(L - t0, 0);
-                unsigned char* vt = smem + OFF_RING + (uint32_t)s * STAGE_BYTES + TILE_BYTES;
+                unsigned char* vt = smem + OFF_V;
                 const int nchunks = (BN - r0) * 16;     // 16-byte chunks in both halves
                 for (int i = tid; i < nchunks; i += NSOFT * 32) {
                     const int row = r0 + (i >> 4), ch = i & 15;
@@ -462,32 +496,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 dec::fence_proxy_async();
-            }
-            if (j > 0) {
-                if (!wait_warp(bar(BAR_OF), (j - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                if (__any_sync(FULL, grow)) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(trow + COL_O + 32u * c, ov);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(trow + COL_O + 32u * c, ov);
-                    }
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t w[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = ph[32 * c + e];
-                tmem_st32(trow + COL_PH + 32u * c, w);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pl[32 * c + e];
-                tmem_st32(trow + COL_PL + 32u * c, w);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -498,6 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = __all_sync(FULL, ok);
         const bool have_o = ok && ntiles > 0 && wait_warp(bar(BAR_OF), (ntiles - 1) & 1);
         if (ntiles > 0) tc_fence_after();
+        const float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
         const float inv = l > 0.f ? 1.f / l : 0.f;
         T* orow = static_cast<T*>(p.out) +
                   ((size_t)(cu0 + q0 + qi) * p.num_q_heads + (size_t)g * G + hh) * D;
