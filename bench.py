@@ -40,6 +40,8 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_decode_split_llama3_8b_gqa.md")
 DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "decode_kernel.cuh")
+PREFILL_SUMMARY = os.path.join(ROOT, "profiles", "paged_prefill_chunked_llama3_8b.md")
+PREFILL_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "prefill_kernel.cuh")
 
 WORKLOAD_TEXT = {
     "llama3_8b_gqa": "Llama-3-8B-shaped GQA decode step: 32 query / 8 KV heads, head_dim 128, bf16, "
@@ -128,12 +130,14 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the split kernel from the committed ncu summary,
-    if it was taken on the current kernel source (else None)."""
+def profiled_traffic(summary=None, source=None):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if the
+    counters were taken on the current kernel source (else None)."""
+    summary = summary or PROFILE_SUMMARY
+    source = source or DECODE_SOURCE
     try:
-        text = open(PROFILE_SUMMARY).read()
-        sha = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
+        text = open(summary).read()
+        sha = hashlib.sha256(open(source, "rb").read()).hexdigest()
     except OSError:
         return None
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
@@ -610,7 +614,11 @@ def run_ours(args):
                                 "paged_decode_split (the whole decode call: one kernel, merges included)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": None if (cascade or q8 is not None) else profiled_traffic(),
+                     "traffic": (profiled_traffic()
+                                 if (not cascade and q8 is None and args.workload == "llama3_8b_gqa"
+                                     and args.batch is None and args.seed == 0
+                                     and args.placement == "random") else None),
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
                      "algorithmic_bytes": roof_bytes},
         "e2e": {"value": round(total_bytes / (max_e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(max_e2e_ms, 5), "h2d_bytes_per_step": h2d,
@@ -799,7 +807,11 @@ def run_prefill(args):
                      "kernel": "paged_prefill (tcgen05; the whole prefill call, one kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind} (bf16 burst)",
-                     "traffic": None, "algorithmic_flops": flops},
+                     "traffic": (profiled_traffic(PREFILL_SUMMARY, PREFILL_SOURCE)
+                                 if args.batch is None and args.chunk is None and not args.decodes
+                                 and args.seed == 0 else None),
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
+                     "algorithmic_flops": flops},
         "e2e": {"value": round(total_flops / (max_e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(max_e2e_ms, 5),
                 "h2d_bytes_per_step": int(host_in.numel()),
