@@ -22,24 +22,31 @@
 //   S  = Q K^T      tcgen05.mma, A = Q (smem), B = K tile (smem), D = TMEM
 //   P  = exp2(S * scale * log2 e - m)            (softmax warps, fp32)
 //   O += P V        tcgen05.mma, A = P (TMEM), B = V tile (smem), D = TMEM
-// P overwrites S in TMEM as 16-bit hi + lo halves (P = hi + lo to 2^-16
-// relative) and is multiplied twice, so the result keeps fp32-level accuracy.
+// P is stored in TMEM as 16-bit hi + lo halves (P = hi + lo to 2^-16
+// relative) and multiplied twice, so the result keeps fp32-level accuracy.
 // The running maximum is updated lazily: O and the sum are rescaled only when
 // a row's maximum grows by more than 2^8, so P stays below 256.
 //
-// Two CTAs share an SM (96 KB of shared memory and 256 TMEM columns each):
-// one CTA's softmax runs while the other's products occupy the tensor pipe,
-// which hides the serial S -> softmax -> PV chain of each tile.
+// Overlap.  S, P and O have separate TMEM columns (384 of 512), so S_{j+1} is
+// computed while tile j's softmax runs, and tile j+1's softmax (maximum and
+// exponentials) while PV_j runs; only the store of P_{j+1} waits for PV_j.
+// K tiles come through a three-stage ring released as soon as S_j is done,
+// V tiles through a two-stage ring released after PV_j, so each load has one
+// to two tiles of lead.  One CTA per SM (196 KB of shared memory).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax and epilogue; thread r owns row r (TMEM lane r);
-//   warp 4     TMA producer: Q once, then the K and V tiles (one buffer each:
-//              K_{j+1} lands while tile j's softmax and PV run, V_{j+1} while
-//              S_{j+1} and its softmax run);
-//   warp 5     TMEM allocation and the single MMA-issuing thread.
+// Warp roles (352 threads):
+//   warps 0-7  softmax and epilogue, two warpgroups: thread (w, lane) owns row
+//              32 (w % 4) + lane (its TMEM lane) and the 64 columns starting
+//              at 64 (w / 4); the two halves of a row exchange their maxima
+//              and sums through shared memory (a named barrier per pair);
+//   warp 8     TMA producer of Q (once) and the K tiles;
+//   warp 9     TMEM allocation and the MMA issue (one elected lane);
+//   warp 10    TMA producer of the V tiles (so K loads never queue behind a
+//              V buffer that PV still holds).
 // Every mbarrier wait is bounded; a wait that gives up sets KV_DEVERR_TIMEOUT,
 // raises the CTA's abort flag, and the CTA drains its copies and MMAs, frees
-// TMEM and exits.
+// TMEM and exits (the softmax pairs keep meeting at their named barriers, so
+// none of them can be left waiting there).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -56,25 +63,30 @@ using dec::FULL;
 constexpr int D = 128;            // head_dim
 constexpr int BM = 128;           // rows of a tile
 constexpr int BN = 128;           // tokens of a KV tile
-constexpr int NSOFT = 4;          // softmax warps = TMEM lane quadrants
-constexpr int WARP_TMA = 4, WARP_MMA = 5;
-constexpr int NTHREADS = 6 * 32;
-constexpr int CTAS_PER_SM = 2;
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_O = 128;    // P (hi, then lo) overwrites S
-constexpr uint32_t COL_PH = COL_S, COL_PL = COL_S + 64;
+constexpr int KST = 3, VST = 2;   // K and V ring depths
+constexpr int NSOFT = 8;          // softmax warps: two per TMEM lane quadrant
+constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_TMAV = 10;
+constexpr int NTHREADS = 11 * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_O = 128, COL_PH = 256, COL_PL = 320;
 constexpr float kRescaleLog2 = 8.f;   // lazy rescale threshold (log2 units)
 
 constexpr uint32_t HALF_BYTES = 128u * 128u;    // 128 rows x 128 B (64 dims)
 constexpr uint32_t TILE_BYTES = 2u * HALF_BYTES;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = TILE_BYTES;
-constexpr uint32_t OFF_V = 2u * TILE_BYTES;
-constexpr uint32_t OFF_BAR = 3u * TILE_BYTES;
-// barriers (8 B each), then the TMEM address and the abort flag
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 2, BAR_VF = 3, BAR_VE = 4, BAR_SF = 5,
-              BAR_PF = 6, BAR_OF = 7, BAR_DR = 8, NBARS = 9;
-constexpr uint32_t OFF_TMEM = OFF_BAR + 8u * NBARS;
+constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
+// barriers (8 B each): q_full, k_full[KST], k_empty[KST], v_full[VST],
+// v_empty[VST], s_full, s_free, p_full, o_full, drain
+constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = BAR_KF + KST, BAR_VF = BAR_KE + KST,
+              BAR_VE = BAR_VF + VST, BAR_SF = BAR_VE + VST, BAR_SR = BAR_SF + 1,
+              BAR_PF = BAR_SR + 1, BAR_OF = BAR_PF + 1, BAR_DR = BAR_OF + 1, NBARS = BAR_DR + 1;
+// row maxima of the two halves, double-buffered by tile parity: [2][2][128]
+// floats; then the halves' row sums [2][128]
+constexpr uint32_t OFF_RED = OFF_BAR + 8u * NBARS;
+constexpr uint32_t OFF_LRED = OFF_RED + 4u * 2u * 2u * BM;
+constexpr uint32_t OFF_TMEM = OFF_LRED + 4u * 2u * BM;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4u;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4u + 1024u;   // + slack to align the base to 1 KB
 
@@ -162,12 +174,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24)
         : "memory");
 }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
-                     taddr),
-                 PKV_W8(0)
-                 : "memory");
-}
 #undef PKV_R8
 #undef PKV_W8
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -228,6 +234,19 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
+// One lane of the (fully active) warp is elected.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile("{ .reg .pred p; elect.sync _|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(pred));
+    return pred != 0;
+}
+
+// Named barrier for the two softmax warps of one TMEM lane quadrant (ids 1-4;
+// 0 is __syncthreads).
+__device__ __forceinline__ void pair_sync(int quadrant) {
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + quadrant) : "memory");
+}
+
 // Bounded wait; on expiry (or when another role already gave up) raise the
 // abort flag and return false.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -241,7 +260,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 template <typename T, int G>
-__global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
+__global__ void __launch_bounds__(NTHREADS, 1)
     paged_prefill(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
@@ -282,7 +301,8 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
 
     // -- set-up: barriers, TMEM ----------------------------------------------
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) dec::mbar_init(bar(i), i == BAR_PF ? NSOFT : 1);
+        for (int i = 0; i < NBARS; ++i)
+            dec::mbar_init(bar(i), (i == BAR_SR || i == BAR_PF) ? NSOFT : 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -298,149 +318,189 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == WARP_TMA) {
-        // ------------------------------------------------------ producer ----
+    if (warp == WARP_TMA || warp == WARP_TMAV) {
+        // ----------------------------------------------------- producers ----
+        const bool is_k = warp == WARP_TMA;
+        const int nst = is_k ? KST : VST;
+        const int full0 = is_k ? BAR_KF : BAR_VF, empty0 = is_k ? BAR_KE : BAR_VE;
+        const uint32_t buf0 = sbase + (is_k ? OFF_K : OFF_V);
+        const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
         const int nb_tile = BN / bs;               // pool blocks per KV tile (<= 16)
         const uint32_t blk_bytes = (uint32_t)bs * 128u;   // one block, one 64-dim half
-        int issued_k = 0, issued_v = 0;
         if (ntiles > 0) {
-            if (lane == 0) {
+            if (is_k && lane == 0) {
                 dec::mbar_arrive_tx(bar(BAR_Q), TILE_BYTES);
                 dec::tma_load_3d(sbase + OFF_Q, &tmap_q, 0, g * G, cu0 + q0, bar(BAR_Q));
                 dec::tma_load_3d(sbase + OFF_Q + HALF_BYTES, &tmap_q, 64, g * G, cu0 + q0,
                                  bar(BAR_Q));
             }
             const int32_t* table = p.block_tables + (size_t)b * p.max_blocks;
-            // one KV tile into one buffer: the lanes' blocks, bytes counted first
-            auto load_tile = [&](int j, int full, uint32_t dst, const CUtensorMap* map) {
+            int issued = 0;
+            for (int j = 0; j < ntiles; ++j) {
+                const int slot = j % nst;
+                bool ok = true;
+                // tile j reuses the buffer of tile j - nst: freed when S (K) or
+                // PV (V) of that tile is done
+                if (lane == 0 && j >= nst)
+                    ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err);
+                if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
                 const int lb = j * nb_tile + lane;  // logical block of this lane
                 int id = -1;
                 bool load = false;
                 if (lane < nb_tile && lb * bs < L) {
                     id = table[lb];
                     load = id >= 0 && id < p.num_blocks;
-                    if (!load && map == &tmap_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                    if (!load && is_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
                 }
                 const unsigned mask = __ballot_sync(FULL, load);
-                if (lane == 0) dec::mbar_arrive_tx(bar(full), (uint32_t)__popc(mask) * 2u * blk_bytes);
+                if (lane == 0)
+                    dec::mbar_arrive_tx(bar(full0 + slot), (uint32_t)__popc(mask) * 2u * blk_bytes);
                 __syncwarp();
                 if (load) {
-                    const uint32_t d = dst + (uint32_t)lane * blk_bytes;
-                    dec::tma_load_3d(d, map, 0, g, id * bs, bar(full));
-                    dec::tma_load_3d(d + HALF_BYTES, map, 64, g, id * bs, bar(full));
+                    const uint32_t d = buf0 + (uint32_t)slot * TILE_BYTES + (uint32_t)lane * blk_bytes;
+                    dec::tma_load_3d(d, map, 0, g, id * bs, bar(full0 + slot));
+                    dec::tma_load_3d(d + HALF_BYTES, map, 64, g, id * bs, bar(full0 + slot));
                 }
-            };
-            // K_j needs S_{j-1} done (k_empty), V_j needs PV_{j-1} done (v_empty);
-            // K runs one tile ahead of V
-            for (int j = 0; j < ntiles; ++j) {
-                bool ok = true;
-                if (lane == 0 && j > 0)
-                    ok = wait_or_abort(bar(BAR_KE), (j - 1) & 1, abort_flag, p.err);
-                if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
-                load_tile(j, BAR_KF, sbase + OFF_K, &tmap_k);
-                issued_k = j + 1;
-                if (lane == 0 && j > 0)
-                    ok = wait_or_abort(bar(BAR_VE), (j - 1) & 1, abort_flag, p.err);
-                if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
-                load_tile(j, BAR_VF, sbase + OFF_V, &tmap_v);
-                issued_v = j + 1;
+                issued = j + 1;
             }
             // Drain: no copy may still be landing in shared memory at exit.
             if (lane == 0) {
-                bool ok = dec::mbar_wait(bar(BAR_Q), 0);
-                if (issued_k > 0) ok &= dec::mbar_wait(bar(BAR_KF), (issued_k - 1) & 1);
-                if (issued_v > 0) ok &= dec::mbar_wait(bar(BAR_VF), (issued_v - 1) & 1);
+                bool ok = !is_k || dec::mbar_wait(bar(BAR_Q), 0);
+                for (int j = max(0, issued - nst); j < issued; ++j)
+                    ok &= dec::mbar_wait(bar(full0 + j % nst), (j / nst) & 1);
                 if (!ok) atomicOr(p.err, KV_DEVERR_TIMEOUT);
             }
         }
     } else if (warp == WARP_MMA) {
         // ----------------------------------------------------------- MMA ----
-        if (ntiles > 0 && lane == 0) {
+        // The whole warp runs the loop (waits included) so every operand is
+        // warp-uniform; one elected lane issues each tcgen05 instruction.
+        if (ntiles > 0) {
             constexpr uint32_t fmt = H16<T>::kFmt;
             constexpr uint32_t id_s = idesc_f16(fmt, 0, BM, BN);   // S = Q K^T
             constexpr uint32_t id_pv = idesc_f16(fmt, 1, BM, D);   // O += P V (V MN-major)
-            const uint32_t q_addr = sbase + OFF_Q, k_addr = sbase + OFF_K, v_addr = sbase + OFF_V;
-            bool ok = wait_or_abort(bar(BAR_Q), 0, abort_flag, p.err);
+            const uint32_t tm = __shfl_sync(FULL, tmem, 0);
+            // base descriptors; a K step adds (byte offset >> 4) to the start field
+            const uint64_t dq = sdesc_sw128(sbase + OFF_Q, 16u, 1024u);
+            const uint64_t dk = sdesc_sw128(sbase + OFF_K, 16u, 1024u);
+            const uint64_t dv = sdesc_sw128(sbase + OFF_V, HALF_BYTES, 1024u);
+            auto wait_all = [&](uint32_t bb, uint32_t parity) {
+                return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
+            };
+            bool ok = wait_all(bar(BAR_Q), 0);
+            int done_pv = 0;                       // PV products issued
+            auto pv = [&](int jj) -> bool {
+                const int s = jj % VST;
+                if (!wait_all(bar(BAR_PF), jj & 1)) return false;
+                if (!wait_all(bar(BAR_VF + s), (jj / VST) & 1)) return false;
+                tc_fence_after();
+                const uint64_t vs = dv + (uint64_t)((uint32_t)s * (TILE_BYTES >> 4));
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // 16 tokens = two 8-row swizzle atoms (2 KB); the two
+                        // 64-dim halves are HALF_BYTES apart (leading byte offset)
+                        const uint64_t vdesc = vs + (uint64_t)(kk * (2048 >> 4));
+                        mma_ts(tm + COL_O, tm + COL_PH + (uint32_t)kk * 8u, vdesc, id_pv,
+                               (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_ts(tm + COL_O, tm + COL_PL + (uint32_t)kk * 8u, vdesc, id_pv, 1u);
+                    }
+                    mma_commit(bar(BAR_VE + s));
+                    mma_commit(bar(BAR_OF));
+                }
+                __syncwarp();
+                done_pv = jj + 1;
+                return true;
+            };
             for (int j = 0; ok && j < ntiles; ++j) {
-                const uint32_t par = j & 1;
-                // S_j overwrites P_{j-1}: PV_{j-1} must have finished reading it
-                if (j > 0 && !wait_or_abort(bar(BAR_OF), par ^ 1u, abort_flag, p.err)) break;
-                if (!wait_or_abort(bar(BAR_KF), par, abort_flag, p.err)) break;
+                const int s = j % KST;
+                if (!wait_all(bar(BAR_KF + s), (j / KST) & 1)) break;
+                // S_j overwrites S_{j-1}: the softmax must have read it
+                if (j > 0 && !wait_all(bar(BAR_SR), (j - 1) & 1)) break;
                 tc_fence_after();
+                const uint64_t ks = dk + (uint64_t)((uint32_t)s * (TILE_BYTES >> 4));
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    // 16 dims = 32 bytes inside a 128-byte swizzled row
-                    const uint32_t off = (uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + COL_S, sdesc_sw128(q_addr + off, 16u, 1024u),
-                           sdesc_sw128(k_addr + off, 16u, 1024u), id_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        // 16 dims = 32 bytes inside a 128-byte swizzled row
+                        const uint32_t off = ((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4;
+                        mma_ss(tm + COL_S, dq + off, ks + off, id_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(BAR_KE + s));
+                    mma_commit(bar(BAR_SF));
                 }
-                mma_commit(bar(BAR_KE));
-                mma_commit(bar(BAR_SF));
-                if (!wait_or_abort(bar(BAR_PF), par, abort_flag, p.err)) break;
-                if (!wait_or_abort(bar(BAR_VF), par, abort_flag, p.err)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 tokens = two 8-row swizzle atoms; the two 64-dim halves
-                    // are HALF_BYTES apart (leading byte offset)
-                    const uint64_t vdesc = sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF_BYTES, 1024u);
-                    mma_ts(tmem + COL_O, tmem + COL_PH + (uint32_t)kk * 8u, vdesc, id_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tmem + COL_O, tmem + COL_PL + (uint32_t)kk * 8u, vdesc, id_pv, 1u);
-                }
-                mma_commit(bar(BAR_VE));
-                mma_commit(bar(BAR_OF));
+                __syncwarp();
+                if (j > 0 && !pv(j - 1)) break;
             }
+            if (ok && *abort_flag == 0 && done_pv == ntiles - 1) pv(ntiles - 1);
             // Drain: every MMA issued has completed before TMEM is freed.
-            mma_commit(bar(BAR_DR));
-            if (!dec::mbar_wait(bar(BAR_DR), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
+            if (elect_one()) mma_commit(bar(BAR_DR));
+            __syncwarp();
+            if (!wait_all(bar(BAR_DR), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
         }
         __syncwarp();
     } else {
         // ---------------------------------------------- softmax, epilogue ----
-        const int r = tid;                         // row = TMEM lane
+        const int qd = warp & 3, half = warp >> 2;
+        const int r = 32 * qd + lane;              // row = TMEM lane
         const int qi = r / G, hh = r % G;
         const bool valid = qi < nq;
         const int lim = valid ? P0 + qi : -1;      // last visible position
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
+        const uint32_t cs = COL_S + 64u * half;    // this half's S columns
+        float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [2][2][BM]
+        float* lred = reinterpret_cast<float*>(smem + OFF_LRED);   // [2][BM]
         const float qs = p.qscale;
         float m = -CUDART_INF_F;
         float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // partial row sums
         bool ok = true;
         // tcgen05.ld / st are warp-collective: every wait's outcome is made
-        // uniform across the warp
+        // uniform across the warp.  After a failed wait the warp keeps meeting
+        // its partner at the named barriers but touches neither TMEM nor the
+        // pipeline barriers again.
         auto wait_warp = [&](uint32_t bb, uint32_t parity) {
             return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
         };
         for (int j = 0; j < ntiles; ++j) {
-            const int t0 = j * BN;
-            // S_j complete (and with it PV_{j-1}: the commit covers every
-            // earlier product)
-            if (!wait_warp(bar(BAR_SF), j & 1)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t sv[4][32];
+            const int t0 = j * BN + 64 * half;     // first token of this half
+            uint32_t sv[2][32];
+            if (ok) ok = wait_warp(bar(BAR_SF), j & 1);
+            if (ok) {
+                tc_fence_after();
+                tmem_ld32(trow + cs, sv[0]);
+                tmem_ld32(trow + cs + 32u, sv[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) dec::mbar_arrive(bar(BAR_SR));   // S may be overwritten
+            } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(trow + COL_S + 32u * c, sv[c]);
-            tmem_wait_ld();
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sv[c][e] = __float_as_uint(-CUDART_INF_F);
+            }
             // causal / length mask: tokens past `lim` do not exist for this row
-            if (t0 + BN - 1 > lim) {
+            if (t0 + 63 > lim) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         if (t0 + 32 * c + e > lim) sv[c][e] = __float_as_uint(-CUDART_INF_F);
             }
-            // row maximum: four independent chains of three-input maxima
-            float mx4[4];
+            float mx2[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                mx4[i] = fmaxf(__uint_as_float(sv[i][0]), __uint_as_float(sv[i][1]));
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int c = 0; c < 2; ++c) {
+                mx2[c] = fmaxf(__uint_as_float(sv[c][0]), __uint_as_float(sv[c][1]));
 #pragma unroll
                 for (int e = 2; e < 32; e += 2)
-                    mx4[i] = max3(mx4[i], __uint_as_float(sv[i][e]), __uint_as_float(sv[i][e + 1]));
-            const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                    mx2[c] = max3(mx2[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            }
+            // the row maximum over both halves (buffer by tile parity: the
+            // partner has read this buffer before either reaches the next sync)
+            float* rb = red + (j & 1) * 2 * BM;
+            rb[half * BM + r] = fmaxf(mx2[0], mx2[1]);
+            pair_sync(qd);
+            const float mx = fmaxf(rb[r], rb[BM + r]);
             const float m_new = fmaxf(m, mx * qs);
             float alpha = 1.f;
             const bool grow = m_new > m + kRescaleLog2;   // false while both are -inf
@@ -451,73 +511,85 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
             const float mu = m == -CUDART_INF_F ? 0.f : m;
             l2[0] = __fmul2_rn(l2[0], make_float2(alpha, alpha));
             l2[1] = __fmul2_rn(l2[1], make_float2(alpha, alpha));
-            // P = hi + lo over S's columns (S was read in full above), 16
-            // tokens at a time
+            // P = hi + lo of this half's 64 tokens, in registers until PV_{j-1}
+            // has finished with the P columns
             const float2 qs2 = make_float2(qs, qs), nmu2 = make_float2(-mu, -mu);
+            uint32_t ph[32], pl[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t ph[8], pl[8];
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    const uint32_t* sc = sv[c >> 1] + 16 * (c & 1);
+                for (int e = 0; e < 32; e += 2) {
                     const float2 x = __ffma2_rn(
-                        make_float2(__uint_as_float(sc[e]), __uint_as_float(sc[e + 1])), qs2, nmu2);
+                        make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), qs2,
+                        nmu2);
                     const float2 pp = make_float2(dec::fast_exp2(x.x), dec::fast_exp2(x.y));
                     l2[(e >> 1) & 1] = __fadd2_rn(l2[(e >> 1) & 1], pp);
-                    H16<T>::split(pp.x, pp.y, ph[e / 2], pl[e / 2]);
+                    H16<T>::split(pp.x, pp.y, ph[16 * c + e / 2], pl[16 * c + e / 2]);
                 }
-                tmem_st8(trow + COL_PH + 8u * c, ph);
-                tmem_st8(trow + COL_PL + 8u * c, pl);
-            }
-            // O was last written by PV_{j-1}; rescale it when any row's maximum grew
-            // (after P, so S's registers are free)
-            if (j > 0 && __any_sync(FULL, grow)) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(trow + COL_O + 32u * c, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(trow + COL_O + 32u * c, ov);
-                }
-            }
             // the last tile: zero V rows past the sequence end (P is 0 there,
             // but 0 x NaN from an unwritten row would poison the product)
-            if (t0 + BN > L) {
-                if (!wait_warp(bar(BAR_VF), j & 1)) { ok = false; break; }
-                const int r0 = max(L - t0, 0);
-                unsigned char* vt = smem + OFF_V;
-                const int nchunks = (BN - r0) * 16;     // 16-byte chunks in both halves
-                for (int i = tid; i < nchunks; i += NSOFT * 32) {
-                    const int row = r0 + (i >> 4), ch = i & 15;
-                    *reinterpret_cast<uint4*>(vt + (ch >> 3) * HALF_BYTES + row * 128 + (ch & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+            if (ok && j * BN + BN > L) {
+                ok = wait_warp(bar(BAR_VF + j % VST), (j / VST) & 1);
+                if (ok) {
+                    const int r0 = max(L - j * BN, 0);
+                    unsigned char* vt = smem + OFF_V + (uint32_t)(j % VST) * TILE_BYTES;
+                    const int nchunks = (BN - r0) * 16;     // 16-byte chunks in both halves
+                    for (int i = tid; i < nchunks; i += NSOFT * 32) {
+                        const int row = r0 + (i >> 4), ch = i & 15;
+                        *reinterpret_cast<uint4*>(vt + (ch >> 3) * HALF_BYTES + row * 128 +
+                                                  (ch & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    dec::fence_proxy_async();
                 }
-                dec::fence_proxy_async();
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) dec::mbar_arrive(bar(BAR_PF));
+            // PV_{j-1} done: the P columns are free and O holds tile j-1's sum;
+            // rescale this half's O columns when any row's maximum grew
+            if (ok && j > 0) {
+                ok = wait_warp(bar(BAR_OF), (j - 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    if (__any_sync(FULL, grow)) {
+#pragma unroll 1
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t ov[32];
+                            const uint32_t col = COL_O + 64u * half + 32u * c;
+                            tmem_ld32(trow + col, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tmem_st32(trow + col, ov);
+                        }
+                    }
+                }
+            }
+            if (ok) {
+                tmem_st32(trow + COL_PH + 32u * half, ph);
+                tmem_st32(trow + COL_PL + 32u * half, pl);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) dec::mbar_arrive(bar(BAR_PF));
+            }
         }
         // -- epilogue: out = O / l, rounded once to the output type ----------
-        ok = __all_sync(FULL, ok);
         const bool have_o = ok && ntiles > 0 && wait_warp(bar(BAR_OF), (ntiles - 1) & 1);
-        if (ntiles > 0) tc_fence_after();
-        const float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+        if (have_o) tc_fence_after();
+        lred[half * BM + r] = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+        pair_sync(qd);
+        const float l = lred[r] + lred[BM + r];
+        const bool done = __all_sync(FULL, have_o || (ok && ntiles == 0));
         const float inv = l > 0.f ? 1.f / l : 0.f;
         T* orow = static_cast<T*>(p.out) +
-                  ((size_t)(cu0 + q0 + qi) * p.num_q_heads + (size_t)g * G + hh) * D;
+                  ((size_t)(cu0 + q0 + qi) * p.num_q_heads + (size_t)g * G + hh) * D + 64 * half;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t ov[32];
             if (have_o) {
-                tmem_ld32(trow + COL_O + 32u * c, ov);
+                tmem_ld32(trow + COL_O + 64u * half + 32u * c, ov);
                 tmem_wait_ld();
             }
-            if (valid && (have_o || (ok && ntiles == 0))) {
+            if (valid && done) {
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
