@@ -20,6 +20,22 @@ cudaError_t launch_typed(const kv_pool& pool, const PrefillCall& c, cudaStream_t
     if (!encode_tiled_map(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(c.q), dims,
                           strides, box, true))
         return cudaErrorInvalidValue;
+    // K/V boxes of min(bs, BN) rows: the pool's swizzled maps (box = one
+    // block) when a block fits a KV tile, else maps with BN-row boxes
+    const CUtensorMap* mk = &pool.tmap_k_swz;
+    const CUtensorMap* mv = &pool.tmap_v_swz;
+    CUtensorMap tk, tv;
+    if (pool.block_size > BN) {
+        const cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)pool.num_kv_heads,
+                                     (cuuint64_t)pool.num_blocks * (cuuint64_t)pool.block_size};
+        const cuuint64_t kstr[2] = {(cuuint64_t)D * 2u, (cuuint64_t)pool.num_kv_heads * D * 2u};
+        const cuuint32_t kbox[3] = {64u, 1u, (cuuint32_t)BN};
+        if (!encode_tiled_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, pool.k, kdims, kstr, kbox, true) ||
+            !encode_tiled_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, pool.v, kdims, kstr, kbox, true))
+            return cudaErrorInvalidValue;
+        mk = &tk;
+        mv = &tv;
+    }
     auto kern = paged_prefill<T, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
@@ -38,10 +54,12 @@ cudaError_t launch_typed(const kv_pool& pool, const PrefillCall& c, cudaStream_t
     p.num_blocks = pool.num_blocks;
     p.bs = pool.block_size;
     p.max_q = c.max_query_len;
+    p.box_rows = pool.block_size < BN ? pool.block_size : BN;
     p.qscale = c.scale * 1.4426950408889634f;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((c.max_query_len + QT - 1) / QT), (unsigned)pool.num_kv_heads,
-                       (unsigned)c.batch);
+    // one CTA per pair of query tiles
+    cfg.gridDim = dim3((unsigned)((c.max_query_len + 2 * QT - 1) / (2 * QT)),
+                       (unsigned)pool.num_kv_heads, (unsigned)c.batch);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
@@ -50,7 +68,7 @@ cudaError_t launch_typed(const kv_pool& pool, const PrefillCall& c, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmap_q, pool.tmap_k_swz, pool.tmap_v_swz, p);
+    return cudaLaunchKernelEx(&cfg, kern, tmap_q, *mk, *mv, p);
 }
 
 template <typename T>

@@ -13,12 +13,14 @@
 // C_b = 1 is a decode request.  Softmax is computed block-wise with a running
 // maximum and sum ("Lecture 24", semidirectx.com CMU 11-868 notes, sec. 3.2).
 //
-// Tiling.  One CTA computes one tile of BM = 128 rows: QT = 128 / G
-// consecutive queries of one request times the G query heads that share one
-// KV head (row = query * G + head), so each K/V tile is read once for the
-// whole GQA group.  The CTA walks the request's tokens in KV tiles of BN = 128
-// (BN / bs pool blocks, each fetched by TMA through the block table), up to
-// the last position its queries can see.
+// Tiling.  A query tile is BM = 128 rows: QT = 128 / G consecutive queries
+// of one request times the G query heads that share one KV head (row =
+// query * G + head), so each K/V tile is read once for the whole GQA group.
+// One CTA runs two query tiles of the same request and KV head ("streams" A
+// and B: query tiles 2t and 2t+1) over shared K/V tiles of BN = 64 tokens
+// (BN / bs pool blocks, or half a block for bs = 128, fetched by TMA through
+// the block table), up to the last position the later tile can see.  Per
+// stream and KV tile:
 //   S  = Q K^T      tcgen05.mma, A = Q (smem), B = K tile (smem), D = TMEM
 //   P  = exp2(S * scale * log2 e - m)            (softmax warps, fp32)
 //   O += P V        tcgen05.mma, A = P (TMEM), B = V tile (smem), D = TMEM
@@ -27,26 +29,27 @@
 // The running maximum is updated lazily: O and the sum are rescaled only when
 // a row's maximum grows by more than 2^8, so P stays below 256.
 //
-// Overlap.  S, P and O have separate TMEM columns (384 of 512), so S_{j+1} is
-// computed while tile j's softmax runs, and tile j+1's softmax (maximum and
-// exponentials) while PV_j runs; only the store of P_{j+1} waits for PV_j.
-// K tiles come through a three-stage ring released as soon as S_j is done,
-// V tiles through a two-stage ring released after PV_j, so each load has one
-// to two tiles of lead.  One CTA per SM (196 KB of shared memory).
+// Overlap.  Each stream has its own S (64 TMEM columns), P (64) and O (128):
+// S_{j+1} is computed while tile j's softmax runs, and tile j+1's softmax
+// while PV_j runs.  The two streams' softmax warps share every SM
+// sub-partition (a warp may only read the TMEM lanes of its own
+// sub-partition, so all warps there work on the same 32 rows of a tile); with
+// two streams, one stream's exponentials (the ex2 unit is the softmax's
+// floor) overlap the other's loads, reductions and stores.
 //
-// Warp roles (352 threads):
-//   warps 0-7  softmax and epilogue, two warpgroups: thread (w, lane) owns row
-//              32 (w % 4) + lane (its TMEM lane) and the 64 columns starting
-//              at 64 (w / 4); the two halves of a row exchange their maxima
-//              and sums through shared memory (a named barrier per pair);
-//   warp 8     TMA producer of Q (once) and the K tiles;
-//   warp 9     TMEM allocation and the MMA issue (one elected lane);
-//   warp 10    TMA producer of the V tiles (so K loads never queue behind a
-//              V buffer that PV still holds).
+// Warp roles (384 threads, one CTA per SM):
+//   warps 0-7  softmax and epilogue, warps 4X..4X+3 for stream X: thread
+//              (w, lane) owns row 32 (w % 4) + lane of its stream's tile (its
+//              TMEM lane), all 64 columns of each KV tile;
+//   warp 8     TMA producer of the two Q tiles (once) and the K tiles
+//              (4-stage ring, released when both streams' S are done);
+//   warp 9     TMA producer of the V tiles (3-stage ring, released when both
+//              streams' PV are done);
+//   warps 10, 11 the MMA issue of stream A and of stream B (one elected
+//              lane each; warp 10 also allocates and frees TMEM).
 // Every mbarrier wait is bounded; a wait that gives up sets KV_DEVERR_TIMEOUT,
 // raises the CTA's abort flag, and the CTA drains its copies and MMAs, frees
-// TMEM and exits (the softmax pairs keep meeting at their named barriers, so
-// none of them can be left waiting there).
+// TMEM and exits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -61,32 +64,32 @@ namespace pf {
 using dec::FULL;
 
 constexpr int D = 128;            // head_dim
-constexpr int BM = 128;           // rows of a tile
-constexpr int BN = 128;           // tokens of a KV tile
-constexpr int KST = 3, VST = 2;   // K and V ring depths
-constexpr int NSOFT = 8;          // softmax warps: two per TMEM lane quadrant
-constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_TMAV = 10;
-constexpr int NTHREADS = 11 * 32;
+constexpr int BM = 128;           // rows of a query tile
+constexpr int BN = 64;            // tokens of a KV tile
+constexpr int KST = 4, VST = 3;   // K and V ring depths
+constexpr int NSOFT = 4;          // softmax warps per stream: one per TMEM lane quadrant
+constexpr int WARP_TMAK = 2 * NSOFT, WARP_TMAV = WARP_TMAK + 1, WARP_MMA = WARP_TMAK + 2;
+constexpr int NTHREADS = (2 * NSOFT + 4) * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_O = 128, COL_PH = 256, COL_PL = 320;
+// per stream X: base 256 X; S, then P hi, P lo, then O
+constexpr uint32_t COL_S = 0, COL_PH = 64, COL_PL = 96, COL_O = 128, COL_STREAM = 256;
 constexpr float kRescaleLog2 = 8.f;   // lazy rescale threshold (log2 units)
 
-constexpr uint32_t HALF_BYTES = 128u * 128u;    // 128 rows x 128 B (64 dims)
-constexpr uint32_t TILE_BYTES = 2u * HALF_BYTES;
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = TILE_BYTES;
-constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_V + VST * TILE_BYTES;
+constexpr uint32_t QHALF = 128u * 128u;          // Q: 128 rows x 128 B (64 dims)
+constexpr uint32_t QTILE = 2u * QHALF;
+constexpr uint32_t KVHALF = (uint32_t)BN * 128u; // K/V: 64 rows x 128 B
+constexpr uint32_t KVTILE = 2u * KVHALF;
+constexpr uint32_t OFF_Q = 0;                    // two query tiles
+constexpr uint32_t OFF_K = 2u * QTILE;
+constexpr uint32_t OFF_V = OFF_K + KST * KVTILE;
+constexpr uint32_t OFF_BAR = OFF_V + VST * KVTILE;
 // barriers (8 B each): q_full, k_full[KST], k_empty[KST], v_full[VST],
-// v_empty[VST], s_full, s_free, p_full, o_full, drain
+// v_empty[VST], then per stream: s_full, s_free, p_full, o_full, drain
 constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = BAR_KF + KST, BAR_VF = BAR_KE + KST,
-              BAR_VE = BAR_VF + VST, BAR_SF = BAR_VE + VST, BAR_SR = BAR_SF + 1,
-              BAR_PF = BAR_SR + 1, BAR_OF = BAR_PF + 1, BAR_DR = BAR_OF + 1, NBARS = BAR_DR + 1;
-// row maxima of the two halves, double-buffered by tile parity: [2][2][128]
-// floats; then the halves' row sums [2][128]
-constexpr uint32_t OFF_RED = OFF_BAR + 8u * NBARS;
-constexpr uint32_t OFF_LRED = OFF_RED + 4u * 2u * 2u * BM;
-constexpr uint32_t OFF_TMEM = OFF_LRED + 4u * 2u * BM;
+              BAR_VE = BAR_VF + VST, BAR_STREAM = BAR_VE + VST;
+constexpr int SB_SF = 0, SB_SR = 1, SB_PF = 2, SB_OF = 3, SB_DR = 4, SB_N = 5;
+constexpr int NBARS = BAR_STREAM + 2 * SB_N;
+constexpr uint32_t OFF_TMEM = OFF_BAR + 8u * NBARS;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4u;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4u + 1024u;   // + slack to align the base to 1 KB
 
@@ -104,6 +107,7 @@ struct Params {
     int num_blocks;
     int bs;
     int max_q;                    // the largest C_b the grid covers
+    int box_rows;                 // rows of one K/V box: min(bs, BN)
     float qscale;                 // scale * log2(e), > 0
 };
 
@@ -159,6 +163,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                   "r"(v[i + 4]), "r"(v[i + 5]), "r"(v[i + 6]), "r"(v[i + 7])
 
 // 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        PKV_W8(0), PKV_W8(8)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -241,11 +252,6 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
-// Named barrier for the two softmax warps of one TMEM lane quadrant (ids 1-4;
-// 0 is __syncthreads).
-__device__ __forceinline__ void pair_sync(int quadrant) {
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + quadrant) : "memory");
-}
 
 // Bounded wait; on expiry (or when another role already gave up) raise the
 // abort flag and return false.
@@ -270,18 +276,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = dec::smem_u32(smem);
     auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
+    auto sbar = [&](int x, int i) { return bar(BAR_STREAM + x * SB_N + i); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, g = blockIdx.y;
-    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;   // later query tiles (more work) first
+    const int pt = (int)gridDim.x - 1 - (int)blockIdx.x;   // later tile pairs (more work) first
     const int bs = p.bs;
 
     dec::pdl_launch_dependents();
     dec::pdl_wait();                              // inputs of earlier kernels are visible
 
-    // -- the tile's queries and the tokens they see --------------------------
+    // -- the two tiles' queries and the tokens they see ----------------------
     int cu0 = p.cu_seqlens[b], cu1 = p.cu_seqlens[b + 1];
     int L = p.seq_lens[b];
     int C = cu1 - cu0;
@@ -290,19 +297,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int cap = p.max_blocks * bs;
     const bool bad_len = L > cap;
     L = max(0, min(L, cap));
-    if (tid == 0 && qt == 0 && (bad_q || C > p.max_q)) atomicOr(p.err, KV_DEVERR_QUERY_RANGE);
-    if (tid == 0 && qt == 0 && g == 0 && bad_len) atomicOr(p.err, KV_DEVERR_SEQ_RANGE);
-    const int q0 = qt * QT;
-    const int nq = min(QT, min(C, p.max_q) - q0);  // valid queries of this tile
-    if (nq <= 0) return;                           // whole CTA, before any barrier
-    const int P0 = L - C + q0;                     // position of the tile's first query
-    const int Pmax = P0 + nq - 1;                  // and of its last (<= L - 1)
+    if (tid == 0 && pt == 0 && (bad_q || C > p.max_q)) atomicOr(p.err, KV_DEVERR_QUERY_RANGE);
+    if (tid == 0 && pt == 0 && g == 0 && bad_len) atomicOr(p.err, KV_DEVERR_SEQ_RANGE);
+    const int Cq = min(C, p.max_q);
+    const int q0 = 2 * pt * QT;                    // first query of stream A
+    const int nqa = min(QT, Cq - q0), nqb = min(QT, Cq - q0 - QT);
+    if (nqa <= 0) return;                          // whole CTA, before any barrier
+    const int nstreams = nqb > 0 ? 2 : 1;
+    const int P0 = L - C + q0;                     // position of stream A's first query
+    const int Pmax = P0 + (nstreams == 2 ? QT + nqb : nqa) - 1;   // the last query's (<= L - 1)
+    // every active stream walks all tiles (rows past their own limit are
+    // masked), so each K/V tile has exactly `nstreams` consumers
     const int ntiles = Pmax >= 0 ? Pmax / BN + 1 : 0;
 
     // -- set-up: barriers, TMEM ----------------------------------------------
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i)
-            dec::mbar_init(bar(i), (i == BAR_SR || i == BAR_PF) ? NSOFT : 1);
+        for (int i = 0; i < NBARS; ++i) {
+            uint32_t count = 1;
+            if ((i >= BAR_KE && i < BAR_KE + KST) || (i >= BAR_VE && i < BAR_VE + VST))
+                count = (uint32_t)nstreams;
+            if (i >= BAR_STREAM && ((i - BAR_STREAM) % SB_N == SB_SR || (i - BAR_STREAM) % SB_N == SB_PF))
+                count = NSOFT;
+            dec::mbar_init(bar(i), count);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -318,48 +335,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == WARP_TMA || warp == WARP_TMAV) {
+    if (warp == WARP_TMAK || warp == WARP_TMAV) {
         // ----------------------------------------------------- producers ----
-        const bool is_k = warp == WARP_TMA;
+        const bool is_k = warp == WARP_TMAK;
         const int nst = is_k ? KST : VST;
         const int full0 = is_k ? BAR_KF : BAR_VF, empty0 = is_k ? BAR_KE : BAR_VE;
         const uint32_t buf0 = sbase + (is_k ? OFF_K : OFF_V);
         const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-        const int nb_tile = BN / bs;               // pool blocks per KV tile (<= 16)
-        const uint32_t blk_bytes = (uint32_t)bs * 128u;   // one block, one 64-dim half
+        const int R = p.box_rows;                  // rows per box: min(bs, BN)
+        const int nbox = BN / R;                   // boxes per KV tile (<= 8)
+        const uint32_t box_bytes = (uint32_t)R * 128u;   // one box, one 64-dim half
         if (ntiles > 0) {
             if (is_k && lane == 0) {
-                dec::mbar_arrive_tx(bar(BAR_Q), TILE_BYTES);
-                dec::tma_load_3d(sbase + OFF_Q, &tmap_q, 0, g * G, cu0 + q0, bar(BAR_Q));
-                dec::tma_load_3d(sbase + OFF_Q + HALF_BYTES, &tmap_q, 64, g * G, cu0 + q0,
-                                 bar(BAR_Q));
+                dec::mbar_arrive_tx(bar(BAR_Q), (uint32_t)nstreams * QTILE);
+                for (int x = 0; x < nstreams; ++x) {
+                    const uint32_t d = sbase + OFF_Q + (uint32_t)x * QTILE;
+                    dec::tma_load_3d(d, &tmap_q, 0, g * G, cu0 + q0 + x * QT, bar(BAR_Q));
+                    dec::tma_load_3d(d + QHALF, &tmap_q, 64, g * G, cu0 + q0 + x * QT, bar(BAR_Q));
+                }
             }
             const int32_t* table = p.block_tables + (size_t)b * p.max_blocks;
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int slot = j % nst;
                 bool ok = true;
-                // tile j reuses the buffer of tile j - nst: freed when S (K) or
-                // PV (V) of that tile is done
+                // tile j reuses the buffer of tile j - nst: freed when every
+                // stream's S (K) or PV (V) of that tile is done
                 if (lane == 0 && j >= nst)
                     ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err);
                 if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
-                const int lb = j * nb_tile + lane;  // logical block of this lane
-                int id = -1;
+                const int t = j * BN + lane * R;   // first token of this lane's box
+                int row = -1;
                 bool load = false;
-                if (lane < nb_tile && lb * bs < L) {
-                    id = table[lb];
+                if (lane < nbox && t < L) {
+                    const int id = table[t / bs];
                     load = id >= 0 && id < p.num_blocks;
                     if (!load && is_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                    row = id * bs + t % bs;
                 }
                 const unsigned mask = __ballot_sync(FULL, load);
                 if (lane == 0)
-                    dec::mbar_arrive_tx(bar(full0 + slot), (uint32_t)__popc(mask) * 2u * blk_bytes);
+                    dec::mbar_arrive_tx(bar(full0 + slot), (uint32_t)__popc(mask) * 2u * box_bytes);
                 __syncwarp();
                 if (load) {
-                    const uint32_t d = buf0 + (uint32_t)slot * TILE_BYTES + (uint32_t)lane * blk_bytes;
-                    dec::tma_load_3d(d, map, 0, g, id * bs, bar(full0 + slot));
-                    dec::tma_load_3d(d + HALF_BYTES, map, 64, g, id * bs, bar(full0 + slot));
+                    const uint32_t d = buf0 + (uint32_t)slot * KVTILE + (uint32_t)lane * box_bytes;
+                    dec::tma_load_3d(d, map, 0, g, row, bar(full0 + slot));
+                    dec::tma_load_3d(d + KVHALF, map, 64, g, row, bar(full0 + slot));
                 }
                 issued = j + 1;
             }
@@ -371,19 +392,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!ok) atomicOr(p.err, KV_DEVERR_TIMEOUT);
             }
         }
-    } else if (warp == WARP_MMA) {
+    } else if (warp >= WARP_MMA) {
         // ----------------------------------------------------------- MMA ----
-        // The whole warp runs the loop (waits included) so every operand is
-        // warp-uniform; one elected lane issues each tcgen05 instruction.
-        if (ntiles > 0) {
+        // One warp per stream runs the loop (waits included) so every operand
+        // is warp-uniform; one elected lane issues each tcgen05 instruction.
+        const int x = warp - WARP_MMA;
+        if (ntiles > 0 && x < nstreams) {
             constexpr uint32_t fmt = H16<T>::kFmt;
             constexpr uint32_t id_s = idesc_f16(fmt, 0, BM, BN);   // S = Q K^T
             constexpr uint32_t id_pv = idesc_f16(fmt, 1, BM, D);   // O += P V (V MN-major)
-            const uint32_t tm = __shfl_sync(FULL, tmem, 0);
+            const uint32_t tm = __shfl_sync(FULL, tmem, 0) + (uint32_t)x * COL_STREAM;
             // base descriptors; a K step adds (byte offset >> 4) to the start field
-            const uint64_t dq = sdesc_sw128(sbase + OFF_Q, 16u, 1024u);
+            const uint64_t dq = sdesc_sw128(sbase + OFF_Q + (uint32_t)x * QTILE, 16u, 1024u);
             const uint64_t dk = sdesc_sw128(sbase + OFF_K, 16u, 1024u);
-            const uint64_t dv = sdesc_sw128(sbase + OFF_V, HALF_BYTES, 1024u);
+            const uint64_t dv = sdesc_sw128(sbase + OFF_V, KVHALF, 1024u);
             auto wait_all = [&](uint32_t bb, uint32_t parity) {
                 return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
             };
@@ -391,22 +413,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int done_pv = 0;                       // PV products issued
             auto pv = [&](int jj) -> bool {
                 const int s = jj % VST;
-                if (!wait_all(bar(BAR_PF), jj & 1)) return false;
+                if (!wait_all(sbar(x, SB_PF), jj & 1)) return false;
                 if (!wait_all(bar(BAR_VF + s), (jj / VST) & 1)) return false;
                 tc_fence_after();
-                const uint64_t vs = dv + (uint64_t)((uint32_t)s * (TILE_BYTES >> 4));
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         // 16 tokens = two 8-row swizzle atoms (2 KB); the two
-                        // 64-dim halves are HALF_BYTES apart (leading byte offset)
-                        const uint64_t vdesc = vs + (uint64_t)(kk * (2048 >> 4));
+                        // 64-dim halves are KVHALF apart (leading byte offset)
+                        const uint64_t vdesc = dv + (uint64_t)(((uint32_t)s * KVTILE + (uint32_t)kk * 2048u) >> 4);
                         mma_ts(tm + COL_O, tm + COL_PH + (uint32_t)kk * 8u, vdesc, id_pv,
                                (jj > 0 || kk > 0) ? 1u : 0u);
                         mma_ts(tm + COL_O, tm + COL_PL + (uint32_t)kk * 8u, vdesc, id_pv, 1u);
                     }
                     mma_commit(bar(BAR_VE + s));
-                    mma_commit(bar(BAR_OF));
+                    mma_commit(sbar(x, SB_OF));
                 }
                 __syncwarp();
                 done_pv = jj + 1;
@@ -416,71 +437,64 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int s = j % KST;
                 if (!wait_all(bar(BAR_KF + s), (j / KST) & 1)) break;
                 // S_j overwrites S_{j-1}: the softmax must have read it
-                if (j > 0 && !wait_all(bar(BAR_SR), (j - 1) & 1)) break;
+                if (j > 0 && !wait_all(sbar(x, SB_SR), (j - 1) & 1)) break;
                 tc_fence_after();
-                const uint64_t ks = dk + (uint64_t)((uint32_t)s * (TILE_BYTES >> 4));
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         // 16 dims = 32 bytes inside a 128-byte swizzled row
-                        const uint32_t off = ((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4;
-                        mma_ss(tm + COL_S, dq + off, ks + off, id_s, kk > 0 ? 1u : 0u);
+                        const uint32_t qo = ((uint32_t)(kk >> 2) * QHALF + (uint32_t)(kk & 3) * 32u) >> 4;
+                        const uint32_t ko = ((uint32_t)s * KVTILE + (uint32_t)(kk >> 2) * KVHALF +
+                                             (uint32_t)(kk & 3) * 32u) >> 4;
+                        mma_ss(tm + COL_S, dq + qo, dk + ko, id_s, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(BAR_KE + s));
-                    mma_commit(bar(BAR_SF));
+                    mma_commit(sbar(x, SB_SF));
                 }
                 __syncwarp();
                 if (j > 0 && !pv(j - 1)) break;
             }
             if (ok && *abort_flag == 0 && done_pv == ntiles - 1) pv(ntiles - 1);
             // Drain: every MMA issued has completed before TMEM is freed.
-            if (elect_one()) mma_commit(bar(BAR_DR));
+            if (elect_one()) mma_commit(sbar(x, SB_DR));
             __syncwarp();
-            if (!wait_all(bar(BAR_DR), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
+            if (!wait_all(sbar(x, SB_DR), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
         }
         __syncwarp();
-    } else {
+    } else if (warp / NSOFT < nstreams) {
         // ---------------------------------------------- softmax, epilogue ----
-        const int qd = warp & 3, half = warp >> 2;
+        const int x = warp / NSOFT, qd = warp % NSOFT;
         const int r = 32 * qd + lane;              // row = TMEM lane
         const int qi = r / G, hh = r % G;
+        const int nq = x == 0 ? nqa : nqb;
         const bool valid = qi < nq;
-        const int lim = valid ? P0 + qi : -1;      // last visible position
-        const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
-        const uint32_t cs = COL_S + 64u * half;    // this half's S columns
-        float* red = reinterpret_cast<float*>(smem + OFF_RED);     // [2][2][BM]
-        float* lred = reinterpret_cast<float*>(smem + OFF_LRED);   // [2][BM]
+        const int lim = valid ? P0 + x * QT + qi : -1;   // last visible position
+        const uint32_t trow = tmem + (uint32_t)x * COL_STREAM + ((uint32_t)(32 * qd) << 16);
+        const int stid = tid - x * NSOFT * 32;     // thread index within the stream
         const float qs = p.qscale;
         float m = -CUDART_INF_F;
         float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // partial row sums
         bool ok = true;
         // tcgen05.ld / st are warp-collective: every wait's outcome is made
-        // uniform across the warp.  After a failed wait the warp keeps meeting
-        // its partner at the named barriers but touches neither TMEM nor the
-        // pipeline barriers again.
+        // uniform across the warp; after a failed wait the warp touches
+        // neither TMEM nor the pipeline barriers again.
         auto wait_warp = [&](uint32_t bb, uint32_t parity) {
             return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
         };
-        for (int j = 0; j < ntiles; ++j) {
-            const int t0 = j * BN + 64 * half;     // first token of this half
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const int t0 = j * BN;
             uint32_t sv[2][32];
-            if (ok) ok = wait_warp(bar(BAR_SF), j & 1);
-            if (ok) {
-                tc_fence_after();
-                tmem_ld32(trow + cs, sv[0]);
-                tmem_ld32(trow + cs + 32u, sv[1]);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) dec::mbar_arrive(bar(BAR_SR));   // S may be overwritten
-            } else {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) sv[c][e] = __float_as_uint(-CUDART_INF_F);
-            }
+            ok = wait_warp(sbar(x, SB_SF), j & 1);
+            if (!ok) break;
+            tc_fence_after();
+            tmem_ld32(trow + COL_S, sv[0]);
+            tmem_ld32(trow + COL_S + 32u, sv[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dec::mbar_arrive(sbar(x, SB_SR));   // S may be overwritten
             // causal / length mask: tokens past `lim` do not exist for this row
-            if (t0 + 63 > lim) {
+            if (t0 + BN - 1 > lim) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -495,13 +509,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int e = 2; e < 32; e += 2)
                     mx2[c] = max3(mx2[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
             }
-            // the row maximum over both halves (buffer by tile parity: the
-            // partner has read this buffer before either reaches the next sync)
-            float* rb = red + (j & 1) * 2 * BM;
-            rb[half * BM + r] = fmaxf(mx2[0], mx2[1]);
-            pair_sync(qd);
-            const float mx = fmaxf(rb[r], rb[BM + r]);
-            const float m_new = fmaxf(m, mx * qs);
+            const float m_new = fmaxf(m, fmaxf(mx2[0], mx2[1]) * qs);
             float alpha = 1.f;
             const bool grow = m_new > m + kRescaleLog2;   // false while both are -inf
             if (grow) {
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float mu = m == -CUDART_INF_F ? 0.f : m;
             l2[0] = __fmul2_rn(l2[0], make_float2(alpha, alpha));
             l2[1] = __fmul2_rn(l2[1], make_float2(alpha, alpha));
-            // P = hi + lo of this half's 64 tokens, in registers until PV_{j-1}
+            // P = hi + lo of the tile's 64 tokens, in registers until PV_{j-1}
             // has finished with the P columns
             const float2 qs2 = make_float2(qs, qs), nmu2 = make_float2(-mu, -mu);
             uint32_t ph[32], pl[32];
@@ -519,74 +527,68 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int c = 0; c < 2; ++c)
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float2 x = __ffma2_rn(
+                    const float2 xx = __ffma2_rn(
                         make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), qs2,
                         nmu2);
-                    const float2 pp = make_float2(dec::fast_exp2(x.x), dec::fast_exp2(x.y));
+                    const float2 pp = make_float2(dec::fast_exp2(xx.x), dec::fast_exp2(xx.y));
                     l2[(e >> 1) & 1] = __fadd2_rn(l2[(e >> 1) & 1], pp);
                     H16<T>::split(pp.x, pp.y, ph[16 * c + e / 2], pl[16 * c + e / 2]);
                 }
             // the last tile: zero V rows past the sequence end (P is 0 there,
-            // but 0 x NaN from an unwritten row would poison the product)
-            if (ok && j * BN + BN > L) {
+            // but 0 x NaN from an unwritten row would poison the product);
+            // each stream zeroes before its own PV (both write the same zeros)
+            if (j * BN + BN > L) {
                 ok = wait_warp(bar(BAR_VF + j % VST), (j / VST) & 1);
-                if (ok) {
-                    const int r0 = max(L - j * BN, 0);
-                    unsigned char* vt = smem + OFF_V + (uint32_t)(j % VST) * TILE_BYTES;
-                    const int nchunks = (BN - r0) * 16;     // 16-byte chunks in both halves
-                    for (int i = tid; i < nchunks; i += NSOFT * 32) {
-                        const int row = r0 + (i >> 4), ch = i & 15;
-                        *reinterpret_cast<uint4*>(vt + (ch >> 3) * HALF_BYTES + row * 128 +
-                                                  (ch & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    dec::fence_proxy_async();
+                if (!ok) break;
+                const int r0 = max(L - j * BN, 0);
+                unsigned char* vt = smem + OFF_V + (uint32_t)(j % VST) * KVTILE;
+                const int nchunks = (BN - r0) * 16;     // 16-byte chunks in both halves
+                for (int i = stid; i < nchunks; i += NSOFT * 32) {
+                    const int row = r0 + (i >> 4), ch = i & 15;
+                    *reinterpret_cast<uint4*>(vt + (ch >> 3) * KVHALF + row * 128 + (ch & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
+                dec::fence_proxy_async();
             }
             // PV_{j-1} done: the P columns are free and O holds tile j-1's sum;
-            // rescale this half's O columns when any row's maximum grew
-            if (ok && j > 0) {
-                ok = wait_warp(bar(BAR_OF), (j - 1) & 1);
-                if (ok) {
-                    tc_fence_after();
-                    if (__any_sync(FULL, grow)) {
+            // rescale O when any row's maximum grew
+            if (j > 0) {
+                ok = wait_warp(sbar(x, SB_OF), (j - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(FULL, grow)) {
 #pragma unroll 1
-                        for (int c = 0; c < 2; ++c) {
-                            uint32_t ov[32];
-                            const uint32_t col = COL_O + 64u * half + 32u * c;
-                            tmem_ld32(trow + col, ov);
-                            tmem_wait_ld();
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(trow + COL_O + 32u * c, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            tmem_st32(trow + col, ov);
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(trow + COL_O + 32u * c, ov);
                     }
                 }
             }
-            if (ok) {
-                tmem_st32(trow + COL_PH + 32u * half, ph);
-                tmem_st32(trow + COL_PL + 32u * half, pl);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) dec::mbar_arrive(bar(BAR_PF));
-            }
+            tmem_st32(trow + COL_PH, ph);
+            tmem_st32(trow + COL_PL, pl);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dec::mbar_arrive(sbar(x, SB_PF));
         }
         // -- epilogue: out = O / l, rounded once to the output type ----------
-        const bool have_o = ok && ntiles > 0 && wait_warp(bar(BAR_OF), (ntiles - 1) & 1);
+        const bool have_o = ok && ntiles > 0 && wait_warp(sbar(x, SB_OF), (ntiles - 1) & 1);
         if (have_o) tc_fence_after();
-        lred[half * BM + r] = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
-        pair_sync(qd);
-        const float l = lred[r] + lred[BM + r];
-        const bool done = __all_sync(FULL, have_o || (ok && ntiles == 0));
+        const float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+        const bool done = have_o || (ok && ntiles == 0);
         const float inv = l > 0.f ? 1.f / l : 0.f;
         T* orow = static_cast<T*>(p.out) +
-                  ((size_t)(cu0 + q0 + qi) * p.num_q_heads + (size_t)g * G + hh) * D + 64 * half;
+                  ((size_t)(cu0 + q0 + x * QT + qi) * p.num_q_heads + (size_t)g * G + hh) * D;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
             uint32_t ov[32];
             if (have_o) {
-                tmem_ld32(trow + COL_O + 64u * half + 32u * c, ov);
+                tmem_ld32(trow + COL_O + 32u * c, ov);
                 tmem_wait_ld();
             }
             if (valid && done) {
