@@ -89,7 +89,11 @@ constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = BAR_KF + KST, BAR_VF = BAR_KE + KS
               BAR_VE = BAR_VF + VST, BAR_STREAM = BAR_VE + VST;
 constexpr int SB_SF = 0, SB_SR = 1, SB_PF = 2, SB_OF = 3, SB_DR = 4, SB_N = 5;
 constexpr int NBARS = BAR_STREAM + 2 * SB_N;
-constexpr uint32_t OFF_TMEM = OFF_BAR + 8u * NBARS;
+// launch order: the requests' costs (up to kMaxRanked of them) and the
+// request this CTA takes
+constexpr int kMaxRanked = 256;
+constexpr uint32_t OFF_ORDER = OFF_BAR + 8u * NBARS;
+constexpr uint32_t OFF_TMEM = OFF_ORDER + 4u * (kMaxRanked + 4);
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4u;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4u + 1024u;   // + slack to align the base to 1 KB
 
@@ -281,12 +285,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int pt = (int)gridDim.x - 1 - (int)blockIdx.x;   // later tile pairs (more work) first
     const int bs = p.bs;
 
     dec::pdl_launch_dependents();
     dec::pdl_wait();                              // inputs of earlier kernels are visible
+
+    // -- which (request, KV head, tile pair) this CTA takes -------------------
+    // CTAs start in launch order (x fastest).  Requests are taken longest
+    // first (the KV tiles their last queries walk), then their tile pairs from
+    // the last (which sees the most tokens), so the long work starts early and
+    // short work fills the tail.  Batches of more than kMaxRanked requests
+    // keep the grid's own order.
+    int b = blockIdx.z, g = blockIdx.y;
+    int pt = (int)gridDim.x - 1 - (int)blockIdx.x;
+    if (p.batch <= kMaxRanked) {
+        int* cost = reinterpret_cast<int*>(smem + OFF_ORDER);
+        int* pick = cost + kMaxRanked;
+        const int k = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+        const int per_req = (int)(gridDim.x * gridDim.y);
+        const int rank = k / per_req, rem = k % per_req;
+        for (int i = tid; i < p.batch; i += NTHREADS) {
+            const int c0 = p.cu_seqlens[i], c1 = p.cu_seqlens[i + 1];
+            const int Li = min(p.seq_lens[i], p.max_blocks * bs);
+            cost[i] = (c1 > c0 && Li > 0) ? (Li + BN - 1) / BN : 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < p.batch; i += NTHREADS) {
+            const int ci = cost[i];
+            int above = 0;                         // requests ordered before i
+            for (int o = 0; o < p.batch; ++o) above += cost[o] > ci || (cost[o] == ci && o < i);
+            if (above == rank) *pick = i;
+        }
+        __syncthreads();
+        b = *pick;
+        g = rem % (int)gridDim.y;
+        pt = (int)gridDim.x - 1 - rem / (int)gridDim.y;
+        __syncthreads();                           // every thread has read the pick
+    }
 
     // -- the two tiles' queries and the tokens they see ----------------------
     int cu0 = p.cu_seqlens[b], cu1 = p.cu_seqlens[b + 1];
