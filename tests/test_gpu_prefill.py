@@ -166,3 +166,16 @@ def test_host_argument_errors():
         assert ei.value.status == pagedkv.KV_EUNSUPPORTED
     finally:
         pool32.close()
+
+
+def test_many_requests_keep_grid_order_and_ties():
+    """More requests than the launch order ranks (257 > 256): the grid's own
+    order is used; a batch with many equal costs exercises the ranking's
+    tie-break.  Both match the oracle on sampled requests."""
+    rng = np.random.default_rng(11)
+    pre = rng.integers(0, 300, size=257)
+    chk = rng.integers(1, 40, size=257)
+    w = _step("257 requests", 11, pre, chk)
+    _check(w, "257 requests", requests=[0, 1, 128, 255, 256])
+    w2 = _step("ties", 12, [64] * 12 + [200, 7], [30] * 12 + [65, 1])
+    _check(w2, "equal costs")
