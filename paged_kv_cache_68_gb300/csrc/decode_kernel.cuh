@@ -453,6 +453,7 @@ struct CorePolicy {
     static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
     static constexpr int kKvBytes = sizeof(T);   // pool element
     static constexpr int kScaleBytes = 0;
+    static constexpr int kUnitBlocks = 1;        // pool blocks per work unit
 
     float2* pb;                   // this warp's (score | p, p) [bs][G]
     float2* ab;                   // this warp's (alpha, alpha) [G]
@@ -668,6 +669,7 @@ struct TcPolicy {
     static constexpr int kMinBlocks = 3;
     static constexpr int kKvBytes = sizeof(T);
     static constexpr int kScaleBytes = 0;
+    static constexpr int kUnitBlocks = 1;  // pool blocks per work unit
     static constexpr int KS = D / 16;      // QK k-steps (16 dims each)
     static constexpr int MT = D / 16;      // PV m-tiles (16 dims each)
     static constexpr int TT = BSC / 16;    // 16-token tiles per block
@@ -871,6 +873,16 @@ struct TcPolicy {
                 po.part_lse[h] = den > 0.f ? M + fast_log2(den) : -CUDART_INF_F;
         }
     }
+};
+
+// Block size 8 on the tensor cores: a work unit is two consecutive logical
+// blocks, loaded into one 16-row tile (block i of the unit fills rows
+// 8 i .. 8 i + 7 of both 64-dim halves, the same 128-byte swizzle pattern),
+// and attended exactly like a 16-token block.
+template <typename T, int D, int G>
+struct TcPolicy8x2 : TcPolicy<T, D, G, 16> {
+    static constexpr int kUnitBlocks = 2;
+    __device__ __forceinline__ TcPolicy8x2(float2* a, float2* b) : TcPolicy<T, D, G, 16>(a, b) {}
 };
 
 // ---------------------------------------------------- 8-bit pools on MMA --
@@ -1338,7 +1350,9 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int B = p.batch, S = p.stages, H = p.num_kv_heads, bs = p.bs;
-    const Layout lay(S, B, bs, G, D, ELT, p.num_groups, Pol::kScaleBytes);
+    constexpr int UB = Pol::kUnitBlocks;           // pool blocks per work unit
+    const int bsu = bs * UB;                       // tokens per work unit
+    const Layout lay(S, B, bsu, G, D, ELT, p.num_groups, Pol::kScaleBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
@@ -1350,7 +1364,8 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cap = p.max_blocks * bs;              // longest context a table can hold
-    const bool cascade = p.num_groups > 0;
+    // (cascade shapes have one block per unit; the host never pairs blocks there)
+    const bool cascade = UB == 1 && p.num_groups > 0;
 
     // -- 1. the blocks-per-sequence prefix of the clamped lengths -----------
     if (tid == 0) {
@@ -1376,7 +1391,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         for (int b = b0; b < b1; ++b) {
             const int L = p.seq_lens[b];
             over |= L > cap;
-            const int nb = (min(max(L, 0), cap) + bs - 1) / bs;
+            const int nb = (min(max(L, 0), cap) + bsu - 1) / bsu;
             const int skip = cascade ? min(group_skip(vg, p.num_groups, nvg, b), nb) : 0;
             if (cascade) skip_s[b] = skip;
             local += nb - skip;
@@ -1386,7 +1401,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         int run = block_excl_sum(local, warp_tot, &total);
         for (int b = b0; b < b1; ++b) {
             prefix[b] = run;
-            const int nb = (min(max(p.seq_lens[b], 0), cap) + bs - 1) / bs;
+            const int nb = (min(max(p.seq_lens[b], 0), cap) + bsu - 1) / bsu;
             run += nb - (cascade ? skip_s[b] : 0);
         }
         if (tid == 0) prefix[B] = total;
@@ -1415,27 +1430,37 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         // issues the TMA loads one unit at a time: one box per tile, or one
         // per 128-byte half of the row for the swizzled layout.
         constexpr int kBoxes = Pol::kSwizzled ? D * ELT / 128 : 1;
+        // a box is one block's rows of one 128-byte half (swizzled) or of the
+        // whole row; the halves of a unit's tile are bsu rows apart
         const uint32_t box_bytes = (uint32_t)bs * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
-        auto fetch = [&](int uu, int& id, int& gg) {
+        const uint32_t half_bytes = (uint32_t)bsu * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
+        // block ids of unit uu: the first, and (UB = 2) the second or -2 when
+        // the sequence ends inside the first
+        auto fetch = [&](int uu, int& id, int& id2, int& gg) {
             id = -1;
+            id2 = -2;
             gg = 0;
             if (uu < end) {
                 const int b = find_seq(prefix, B, uu, H);
                 const int nb = prefix[b + 1] - prefix[b];
                 const int r = uu - prefix[b] * H;
                 gg = r / nb;
-                id = __ldg(p.block_tables + (size_t)b * p.max_blocks +
-                           (cascade ? skip_s[b] : 0) + (r - gg * nb));
+                const int lb = ((cascade ? skip_s[b] : 0) + (r - gg * nb)) * UB;
+                const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
+                id = __ldg(row + lb);
+                if (UB == 2 && (lb + 1) * bs < min(max(p.seq_lens[b], 0), cap))
+                    id2 = __ldg(row + lb + 1);
             }
         };
-        int id_cur, g_cur, id_nxt, g_nxt;
-        fetch(start + lane, id_cur, g_cur);
+        int id_cur, id2_cur, g_cur, id_nxt, id2_nxt, g_nxt;
+        fetch(start + lane, id_cur, id2_cur, g_cur);
         int k = 0;
         for (int base = start; base < end; base += 32) {
-            fetch(base + 32 + lane, id_nxt, g_nxt);
+            fetch(base + 32 + lane, id_nxt, id2_nxt, g_nxt);
             const int n = min(32, end - base);
             for (int i = 0; i < n; ++i, ++k) {
                 const int id = __shfl_sync(FULL, id_cur, i);
+                const int id2 = __shfl_sync(FULL, id2_cur, i);
                 const int gg = __shfl_sync(FULL, g_cur, i);
                 if (lane == 0) {
                     const int s = k % S, ph = k / S;
@@ -1446,16 +1471,24 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                         ok = false;
                     }
                     const uint32_t fb = smem_u32(&full[s]);
-                    if (ok && id >= 0 && id < p.num_blocks) {
+                    const bool second = UB == 2 && id2 != -2;   // the unit's second block
+                    if (ok && id >= 0 && id < p.num_blocks &&
+                        (!second || (id2 >= 0 && id2 < p.num_blocks))) {
                         valid[s] = 1;
-                        mbar_arrive_tx(fb, lay.tx_bytes);
+                        mbar_arrive_tx(fb, second ? lay.tx_bytes : lay.tx_bytes / UB);
                         const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
-                        const uint32_t vdst = dst + (uint32_t)(bs * D * ELT);
+                        const uint32_t vdst = dst + (uint32_t)(bsu * D * ELT);
 #pragma unroll
                         for (int x = 0; x < kBoxes; ++x) {
                             const int col = x * (int)(128 / ELT);
-                            tma_load_3d(dst + x * box_bytes, &tmap_k, col, gg, id * bs, fb);
-                            tma_load_3d(vdst + x * box_bytes, &tmap_v, col, gg, id * bs, fb);
+                            tma_load_3d(dst + x * half_bytes, &tmap_k, col, gg, id * bs, fb);
+                            tma_load_3d(vdst + x * half_bytes, &tmap_v, col, gg, id * bs, fb);
+                            if (second) {
+                                tma_load_3d(dst + x * half_bytes + box_bytes, &tmap_k, col, gg,
+                                            id2 * bs, fb);
+                                tma_load_3d(vdst + x * half_bytes + box_bytes, &tmap_v, col, gg,
+                                            id2 * bs, fb);
+                            }
                         }
                         if constexpr (Pol::kScaleBytes > 0) {
                             const size_t srow = ((size_t)id * H + gg) * bs;
@@ -1473,6 +1506,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
             }
             __syncwarp();
             id_cur = id_nxt;
+            id2_cur = id2_nxt;
             g_cur = g_nxt;
         }
         // Drain: no copy may still be landing in shared memory at exit.
@@ -1536,7 +1570,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                 const float* sc = Pol::kScaleBytes > 0
                                       ? reinterpret_cast<const float*>(smem + lay.sring) + s * 2 * bs
                                       : nullptr;
-                pol.block(Ks, Ks + bs * D * ELT, sc, min(bs, Lb - j * bs), bs, p.qscale, lane);
+                pol.block(Ks, Ks + bsu * D * ELT, sc, min(bsu, Lb - j * bsu), bsu, p.qscale, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
@@ -1658,8 +1692,8 @@ cudaError_t attrs_typed(size_t smem, int* ctas_per_sm) {
 }
 
 // Which compute policy runs a shape.  Tensor cores: 16-bit pools, head_dim
-// 128, groups of 4 or 8, block size 16 or 32, a pool with swizzled
-// descriptors.  CUDA cores otherwise, with the token loops unrolled for block
+// 128, groups of 4 or 8, block size 8 (two blocks per unit), 16 or 32, a pool
+// with swizzled descriptors.  CUDA cores otherwise, with the token loops unrolled for block
 // size 16 (and 8 / 32 on bf16 head_dim 128); other block sizes take the
 // generic instance.
 template <typename T, int D>
@@ -1669,12 +1703,14 @@ constexpr bool kTensorCores = sizeof(T) == 2 && D == 128 && (G == 4 || G == 8);
 
 inline bool use_tensor_cores(const kv_pool& pool, int G) {
     return pool.elem_bytes == 2 && pool.head_dim == 128 && (G == 4 || G == 8) &&
-           (pool.block_size == 16 || pool.block_size == 32) && pool.has_swizzled_maps;
+           (pool.block_size == 8 || pool.block_size == 16 || pool.block_size == 32) &&
+           pool.has_swizzled_maps;
 }
 
 template <typename T, int D, int G, template <typename, int, int, class> class Fn, typename... A>
 cudaError_t with_policy(int bs, bool tc, A... args) {
     if constexpr (kTensorCores<T, D, G>) {
+        if (tc && bs == 8) return Fn<T, D, G, TcPolicy8x2<T, D, G>>::run(args...);
         if (tc && bs == 16) return Fn<T, D, G, TcPolicy<T, D, G, 16>>::run(args...);
         if (tc && bs == 32) return Fn<T, D, G, TcPolicy<T, D, G, 32>>::run(args...);
     }

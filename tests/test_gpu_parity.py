@@ -100,9 +100,10 @@ def test_long_context_full_sampled(bs):
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs", [
     ("f32", 8, 8, 64, 4), ("f32", 8, 2, 128, 16), ("f16", 4, 4, 64, 16), ("f16", 16, 2, 128, 8),
     ("bf16", 16, 8, 128, 16), ("bf16", 16, 2, 64, 32), ("bf16", 8, 1, 128, 1), ("f16", 8, 4, 64, 5),
-    # tensor-core path: 16-bit, head_dim 128, groups of 4 / 8, block sizes 16 / 32
+    # tensor-core path: 16-bit, head_dim 128, groups of 4 / 8, block sizes 8 (two blocks
+    # per tile), 16 and 32
     ("bf16", 16, 2, 128, 16), ("bf16", 32, 4, 128, 32), ("f16", 32, 8, 128, 16),
-    ("f16", 16, 2, 128, 32),
+    ("f16", 16, 2, 128, 32), ("bf16", 32, 8, 128, 8),
 ])
 def test_shapes_groups_and_block_sizes(dtype, hq, hkv, d, bs):
     ctx = [0, 1, bs - 1, bs, 2 * bs - 1, 3 * bs, 97, 300]
