@@ -137,6 +137,13 @@ struct Layout {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The dynamic shared-memory base rounded up to 1 KB (the swizzle atom) by
+// pointer arithmetic on the shared array itself: pointers derived from it stay
+// known to address shared memory, so their accesses compile to shared-memory
+// loads and stores rather than generic ones.
+__device__ __forceinline__ unsigned char* smem_align_1k(unsigned char* raw) {
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -156,6 +163,20 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try, but a thread whose phase is not complete may stay suspended for
+// up to `ns` nanoseconds; the hardware wakes it as soon as the phase
+// completes, so a waiting warp takes no issue slots from the warps working
+// beside it.
+__device__ __forceinline__ bool mbar_try_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -167,6 +188,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+// mbar_wait with suspended (not spinning) retries; same limit and result.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_for(bar, parity, 200000u)) {
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
@@ -673,6 +703,12 @@ struct TcPolicy {
     static constexpr int KS = D / 16;      // QK k-steps (16 dims each)
     static constexpr int MT = D / 16;      // PV m-tiles (16 dims each)
     static constexpr int TT = BSC / 16;    // 16-token tiles per block
+    // Groups of up to 4 heads leave half of the MMA's N = 8 columns free:
+    // columns 4..7 repeat the query heads of columns 0..3, so their scores,
+    // maxima and weights are bit-identical, and the PV product takes the hi
+    // halves of P in columns 0..3 and the lo halves in 4..7 -- one MMA per
+    // m-tile instead of two.  fold() adds the two halves.
+    static constexpr bool kPairHL = G <= 4;
 
     uint32_t qb[KS][2];                    // Q^T fragments (raw 16-bit query)
     float oacc[MT][4];                     // O^T accumulators
@@ -691,14 +727,20 @@ struct TcPolicy {
         return tile + (uint32_t)((c >> 3) * BSC * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
     }
 
+    // query head of MMA column n (-1: a padding column)
+    __device__ static __forceinline__ int col_head(int n) {
+        const int h = kPairHL ? (n & 3) : n;
+        return h < G ? h : -1;
+    }
+
     __device__ __forceinline__ void begin(const T* qp, float, int lane) {
-        const int gid = lane >> 2, tig = lane & 3;
+        const int gid = lane >> 2, tig = lane & 3, hq = col_head(gid);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-                qb[ks][j] = gid < G ? __ldg(reinterpret_cast<const uint32_t*>(
-                                          qp + gid * D + ks * 16 + j * 8 + tig * 2))
+                qb[ks][j] = hq >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(
+                                          qp + hq * D + ks * 16 + j * 8 + tig * 2))
                                     : 0u;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
@@ -741,67 +783,120 @@ struct TcPolicy {
             s[tt][3] = v1 ? acc[3] * qscale : -CUDART_INF_F;
         }
         // -- online softmax for heads 2 tig (j = 0) and 2 tig + 1 (j = 1) -----
-        float alpha[2];
-        float mnew[2];
+        float mloc[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            float mx = -CUDART_INF_F;
+            mloc[j] = -CUDART_INF_F;
 #pragma unroll
-            for (int tt = 0; tt < TT; ++tt) mx = fmaxf(mx, fmaxf(s[tt][j], s[tt][j + 2]));
+            for (int tt = 0; tt < TT; ++tt) mloc[j] = fmaxf(mloc[j], fmaxf(s[tt][j], s[tt][j + 2]));
+        }
+        online_max(mloc, lane);
+        softmax_weights<TT>(s);
+        pv<TT>(s, vbase, lane);
+    }
+
+    // Raise the running maxima to cover this tile's scores (mloc: this
+    // lane's maxima).  When no lane's score passes its head's running
+    // maximum, nothing moves and the shuffles are skipped; otherwise the
+    // maxima are reduced over the tile's token lanes and the accumulators and
+    // lane sums rescaled.
+    __device__ __forceinline__ void online_max(float (&mloc)[2], int) {
+        if (!__any_sync(FULL, mloc[0] > m_run[0] || mloc[1] > m_run[1])) return;
+        float alpha[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = mloc[j];
             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
-            mnew[j] = fmaxf(m_run[j], mx);
-            alpha[j] = mnew[j] == -CUDART_INF_F ? 1.f : fast_exp2(m_run[j] - mnew[j]);
+            const float mnew = fmaxf(m_run[j], mx);
+            alpha[j] = mnew == -CUDART_INF_F ? 1.f : fast_exp2(m_run[j] - mnew);
+            m_run[j] = mnew;
+            l_run[j] *= alpha[j];
         }
-        float lsum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = e & 1;
-                const float pe = mnew[j] == -CUDART_INF_F ? 0.f : fast_exp2(s[tt][e] - mnew[j]);
-                s[tt][e] = pe;
-                lsum[j] += pe;
-            }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            lsum[j] += __shfl_xor_sync(FULL, lsum[j], 4);
-            lsum[j] += __shfl_xor_sync(FULL, lsum[j], 8);
-            lsum[j] += __shfl_xor_sync(FULL, lsum[j], 16);
-            l_run[j] = l_run[j] * alpha[j] + lsum[j];
-            m_run[j] = mnew[j];
-        }
-        const float2 a2 = make_float2(alpha[0], alpha[1]);
-        // rescale the accumulators only when some running maximum moved
-        if (!__all_sync(FULL, alpha[0] == 1.f && alpha[1] == 1.f))
+        rescale(alpha[0], alpha[1]);
+    }
+
+    __device__ __forceinline__ void rescale(float a0, float a1) {
+        if (__all_sync(FULL, a0 == 1.f && a1 == 1.f)) return;
+        const float2 a2 = make_float2(a0, a1);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             float2 lo = __fmul2_rn(make_float2(oacc[mt][0], oacc[mt][1]), a2);
             float2 hi = __fmul2_rn(make_float2(oacc[mt][2], oacc[mt][3]), a2);
             oacc[mt][0] = lo.x; oacc[mt][1] = lo.y; oacc[mt][2] = hi.x; oacc[mt][3] = hi.y;
         }
-        // -- O^T += V_blk^T P^T, P as hi + lo 16-bit halves -------------------
+    }
+
+    // scores -> weights exp2(s - m) in place; the lane's own sums go into
+    // l_run (the token lanes' sums are added in fold())
+    template <int NT>
+    __device__ __forceinline__ void softmax_weights(float (&s)[NT][4]) {
 #pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-            const uint32_t h01 = Mma<T>::pack(s[tt][0], s[tt][1]);
-            const uint32_t h23 = Mma<T>::pack(s[tt][2], s[tt][3]);
-            const float2 f01 = Mma<T>::unpack(h01), f23 = Mma<T>::unpack(h23);
-            const uint32_t l01 = Mma<T>::pack(s[tt][0] - f01.x, s[tt][1] - f01.y);
-            const uint32_t l23 = Mma<T>::pack(s[tt][2] - f23.x, s[tt][3] - f23.y);
-            const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
-            const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+        for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = e & 1;
+                const float pe = m_run[j] == -CUDART_INF_F ? 0.f : fast_exp2(s[tt][e] - m_run[j]);
+                s[tt][e] = pe;
+                l_run[j] += pe;
+            }
+    }
+
+    // P^T operands of 16-token tile: hi + lo 16-bit halves of the weights
+    // (paired groups: one operand, hi in columns 0..3 and lo in 4..7)
+    template <typename M>
+    __device__ __forceinline__ void p_operands(const float (&p)[4], int lane, uint32_t (&bh)[2],
+                                               uint32_t (&bl)[2]) const {
+        const uint32_t h01 = M::pack(p[0], p[1]);
+        const uint32_t h23 = M::pack(p[2], p[3]);
+        const float2 f01 = M::unpack(h01), f23 = M::unpack(h23);
+        const uint32_t l01 = M::pack(p[0] - f01.x, p[1] - f01.y);
+        const uint32_t l23 = M::pack(p[2] - f23.x, p[3] - f23.y);
+        if constexpr (kPairHL) {
+            const bool lo = (lane & 3) >= 2;       // columns 4..7
+            bh[0] = movm_t(lo ? l01 : h01);
+            bh[1] = movm_t(lo ? l23 : h23);
+        } else {
+            bh[0] = movm_t(h01); bh[1] = movm_t(h23);
+            bl[0] = movm_t(l01); bl[1] = movm_t(l23);
+        }
+    }
+
+    // -- O^T += V_blk^T P^T ----------------------------------------------------
+    template <int NT>
+    __device__ __forceinline__ void pv(const float (&s)[NT][4], uint32_t vbase, int lane) {
+        const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+        for (int tt = 0; tt < NT; ++tt) {
+            uint32_t bh[2], bl[2];
+            p_operands<Mma<T>>(s[tt], lane, bh, bl);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a[4];
                 ldsm_x4_t(a, swz(vbase, tt * 16 + (mi >> 1) * 8 + r8, mt * 2 + (mi & 1)));
-                Mma<T>::run(oacc[mt], a, bh0, bh1);
-                Mma<T>::run(oacc[mt], a, bl0, bl1);
+                Mma<T>::run(oacc[mt], a, bh[0], bh[1]);
+                if constexpr (!kPairHL) Mma<T>::run(oacc[mt], a, bl[0], bl[1]);
             }
         }
     }
 
-    __device__ __forceinline__ void fold(int) {}
+    // End of a piece: the lo-column accumulators join the hi ones (paired
+    // groups) and the token lanes' sums are added up.
+    __device__ __forceinline__ void fold(int) {
+        if constexpr (kPairHL) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) oacc[mt][c] += __shfl_xor_sync(FULL, oacc[mt][c], 2);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            l_run[j] += __shfl_xor_sync(FULL, l_run[j], 4);
+            l_run[j] += __shfl_xor_sync(FULL, l_run[j], 8);
+            l_run[j] += __shfl_xor_sync(FULL, l_run[j], 16);
+        }
+    }
 
     __device__ __forceinline__ void put(float* mo, float* mm, int w, int lane) const {
         const int gid = lane >> 2, tig = lane & 3;
@@ -916,10 +1011,14 @@ constexpr int kFmtInt8 = 1;
 template <int FMT>
 __device__ __forceinline__ void cvt4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     if constexpr (FMT == kFmtE4M3) {
-        const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
-        const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-        lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
-        hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
+        // the two 16-bit halves of w, each a pair of codes, straight into the
+        // conversion (E4M3 -> f16 is exact)
+        asm("{ .reg .b16 l, h;\n"
+            "  mov.b32 {l, h}, %2;\n"
+            "  cvt.rn.f16x2.e4m3x2 %0, l;\n"
+            "  cvt.rn.f16x2.e4m3x2 %1, h; }"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
     } else {
         // two's complement byte b -> f16 (1024 + (b ^ 0x80)) - 1152 = b
         const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
@@ -948,6 +1047,7 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
     float vq;             // FP8: the V scale; INT8: 1
     float kq;             // FP8: the K scale; INT8: 1
     float R;              // the accumulators hold O / R
+    float Rinv;           // INT8: 1 / R (0 while R is 0)
 
     __device__ __forceinline__ Tc8Policy(float2* a, float2* b) : Base(a, b) {}
 
@@ -965,10 +1065,11 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
         const int gid = lane >> 2, tig = lane & 3;
         float2 qf[KS][2];
         float amax = 0.f;
+        const int hq = Base::col_head(gid);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint2 raw = make_uint2(0u, 0u);
-            if (gid < G) raw = __ldg(reinterpret_cast<const uint2*>(qp + gid * D + 32 * tig + 4 * ks));
+            if (hq >= 0) raw = __ldg(reinterpret_cast<const uint2*>(qp + hq * D + 32 * tig + 4 * ks));
             qf[ks][0] = Mma<T>::unpack(raw.x);
             qf[ks][1] = Mma<T>::unpack(raw.y);
 #pragma unroll
@@ -997,7 +1098,10 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
             this->oacc[mt][0] = this->oacc[mt][1] = this->oacc[mt][2] = this->oacc[mt][3] = 0.f;
         this->m_run[0] = this->m_run[1] = -CUDART_INF_F;
         this->l_run[0] = this->l_run[1] = 0.f;
-        R = vq;
+        // INT8: R is the largest V scale met so far in the piece (raised, with
+        // a rescale, when a tile brings a larger one); FP8: the pool's V scale
+        R = FMT == kFmtInt8 ? 0.f : vq;
+        Rinv = 0.f;
     }
 
     __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
@@ -1027,70 +1131,55 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
                 fa *= v0 ? sc[ta] : 0.f;
                 fb *= v1 ? sc[tb] : 0.f;
             }
-            float s[4];
-            s[0] = v0 ? (acc[0][0] + acc[1][0]) * fa : -CUDART_INF_F;
-            s[1] = v0 ? (acc[0][1] + acc[1][1]) * fa : -CUDART_INF_F;
-            s[2] = v1 ? (acc[0][2] + acc[1][2]) * fb : -CUDART_INF_F;
-            s[3] = v1 ? (acc[0][3] + acc[1][3]) * fb : -CUDART_INF_F;
-            // -- online softmax, heads 2 tig (j = 0) and 2 tig + 1 (j = 1) -----
-            float alpha[2], mnew[2], lsum[2] = {0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mx = fmaxf(s[j], s[j + 2]);
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
-                mnew[j] = fmaxf(this->m_run[j], mx);
-                alpha[j] = mnew[j] == -CUDART_INF_F ? 1.f : fast_exp2(this->m_run[j] - mnew[j]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = e & 1;
-                const float pe = mnew[j] == -CUDART_INF_F ? 0.f : fast_exp2(s[e] - mnew[j]);
-                s[e] = pe;
-                lsum[j] += pe;
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                lsum[j] += __shfl_xor_sync(FULL, lsum[j], 4);
-                lsum[j] += __shfl_xor_sync(FULL, lsum[j], 8);
-                lsum[j] += __shfl_xor_sync(FULL, lsum[j], 16);
-                this->l_run[j] = this->l_run[j] * alpha[j] + lsum[j];
-                this->m_run[j] = mnew[j];
-            }
-            // -- V scales: P' = P * vscale_t / vref, accumulators kept as O / vref --
-            float rf = 1.f, wa = 1.f, wb = 1.f;
+            float s[1][4];
+            s[0][0] = v0 ? (acc[0][0] + acc[1][0]) * fa : -CUDART_INF_F;
+            s[0][1] = v0 ? (acc[0][1] + acc[1][1]) * fa : -CUDART_INF_F;
+            s[0][2] = v1 ? (acc[0][2] + acc[1][2]) * fb : -CUDART_INF_F;
+            s[0][3] = v1 ? (acc[0][3] + acc[1][3]) * fb : -CUDART_INF_F;
+            // -- online softmax, heads 2 tig (j = 0) and 2 tig + 1 (j = 1); INT8:
+            // the running largest V scale R moves with the maxima ----------------
+            float sa = 0.f, sb = 0.f;
             if constexpr (FMT == kFmtInt8) {
-                const float sa = v0 ? sc[bs + ta] : 0.f, sb = v1 ? sc[bs + tb] : 0.f;
-                float mx = fmaxf(sa, sb);
+                sa = v0 ? sc[bs + ta] : 0.f;
+                sb = v1 ? sc[bs + tb] : 0.f;
+            }
+            const float smax = fmaxf(sa, sb);
+            float mloc[2] = {fmaxf(s[0][0], s[0][2]), fmaxf(s[0][1], s[0][3])};
+            if (__any_sync(FULL, mloc[0] > this->m_run[0] || mloc[1] > this->m_run[1] ||
+                                     (FMT == kFmtInt8 && smax > R))) {
+                float alpha[2];
 #pragma unroll
-                for (int off = 16; off >= 4; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
-                if (mx > 0.f) {
-                    const float inv = __frcp_rn(mx);
-                    wa = sa * inv;
-                    wb = sb * inv;
-                    rf = R * inv;
-                    R = mx;
-                } else {
-                    wa = wb = 0.f;                    // the tile's V rows are all zero
+                for (int j = 0; j < 2; ++j) {
+                    float mx = mloc[j];
+                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+                    const float mnew = fmaxf(this->m_run[j], mx);
+                    alpha[j] = mnew == -CUDART_INF_F ? 1.f : fast_exp2(this->m_run[j] - mnew);
+                    this->m_run[j] = mnew;
+                    this->l_run[j] *= alpha[j];
                 }
-            }
-            const float2 a2 = make_float2(alpha[0] * rf, alpha[1] * rf);
-            if (!__all_sync(FULL, a2.x == 1.f && a2.y == 1.f))
+                float rf = 1.f;
+                if constexpr (FMT == kFmtInt8) {
+                    float mx = smax;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const float2 lo = __fmul2_rn(make_float2(this->oacc[mt][0], this->oacc[mt][1]), a2);
-                const float2 hi = __fmul2_rn(make_float2(this->oacc[mt][2], this->oacc[mt][3]), a2);
-                this->oacc[mt][0] = lo.x; this->oacc[mt][1] = lo.y;
-                this->oacc[mt][2] = hi.x; this->oacc[mt][3] = hi.y;
+                    for (int off = 16; off >= 4; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+                    if (mx > R) {                     // (uniform: every lane sees all token rows)
+                        Rinv = __frcp_rn(mx);
+                        rf = R * Rinv;
+                        R = mx;
+                    }
+                }
+                this->rescale(alpha[0] * rf, alpha[1] * rf);
             }
-            s[0] *= wa; s[1] *= wa; s[2] *= wb; s[3] *= wb;
-            const uint32_t h01 = Mma<__half>::pack(s[0], s[1]), h23 = Mma<__half>::pack(s[2], s[3]);
-            const float2 f01 = Mma<__half>::unpack(h01), f23 = Mma<__half>::unpack(h23);
-            const uint32_t l01 = Mma<__half>::pack(s[0] - f01.x, s[1] - f01.y);
-            const uint32_t l23 = Mma<__half>::pack(s[2] - f23.x, s[3] - f23.y);
-            const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
-            const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+            this->template softmax_weights<1>(s);
+            // V scales: P' = P * vscale_t / R
+            if constexpr (FMT == kFmtInt8) {
+                const float wa = sa * Rinv, wb = sb * Rinv;
+                s[0][0] *= wa; s[0][1] *= wa; s[0][2] *= wb; s[0][3] *= wb;
+            }
+            uint32_t bh[2], bl[2];
+            this->template p_operands<Mma<__half>>(s[0], lane, bh, bl);
             // -- O^T += V_tile^T P'^T: token rows 2 tig, 2 tig + 1, + 8, + 9 ------
             // (rows past the sequence end read as zero codes: P' is 0 there, but
             // an E4M3 NaN code would still poison the MMA)
@@ -1111,19 +1200,20 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
                 uint32_t a[4];
                 cvt4<FMT>(x01, a[0], a[1]);
                 cvt4<FMT>(x23, a[2], a[3]);
-                Mma<__half>::run(this->oacc[mt], a, bh0, bh1);
-                Mma<__half>::run(this->oacc[mt], a, bl0, bl1);
+                Mma<__half>::run(this->oacc[mt], a, bh[0], bh[1]);
+                if constexpr (!Base::kPairHL) Mma<__half>::run(this->oacc[mt], a, bl[0], bl[1]);
             }
         }
     }
 
     // Before the warp merge: the accumulators become O itself.
-    __device__ __forceinline__ void fold(int) {
+    __device__ __forceinline__ void fold(int lane) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) this->oacc[mt][i] *= R;
         R = 1.f;
+        Base::fold(lane);
     }
 };
 
@@ -1347,8 +1437,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     const Params p) {
     constexpr int ELT = Pol::kKvBytes;             // bytes per pool element
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* smem = smem_align_1k(smem_raw);
     const int B = p.batch, S = p.stages, H = p.num_kv_heads, bs = p.bs;
     constexpr int UB = Pol::kUnitBlocks;           // pool blocks per work unit
     const int bsu = bs * UB;                       // tokens per work unit
@@ -1455,17 +1544,17 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         int id_cur, id2_cur, g_cur, id_nxt, id2_nxt, g_nxt;
         fetch(start + lane, id_cur, id2_cur, g_cur);
         int k = 0;
+        int s = 0, ph = 0;                         // stage and pass of unit k: k % S, k / S
         for (int base = start; base < end; base += 32) {
             fetch(base + 32 + lane, id_nxt, id2_nxt, g_nxt);
             const int n = min(32, end - base);
-            for (int i = 0; i < n; ++i, ++k) {
+            for (int i = 0; i < n; ++i, ++k, s = s + 1 == S ? 0 : s + 1, ph += s == 0) {
                 const int id = __shfl_sync(FULL, id_cur, i);
                 const int id2 = __shfl_sync(FULL, id2_cur, i);
                 const int gg = __shfl_sync(FULL, g_cur, i);
                 if (lane == 0) {
-                    const int s = k % S, ph = k / S;
                     bool ok = *abort_flag == 0;
-                    if (ok && ph > 0 && !mbar_wait(smem_u32(&empty[s]), (ph - 1) & 1)) {
+                    if (ok && ph > 0 && !mbar_wait_sleep(smem_u32(&empty[s]), (ph - 1) & 1)) {
                         *abort_flag = 1;
                         atomicOr(p.err, KV_DEVERR_TIMEOUT);
                         ok = false;
@@ -1512,7 +1601,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         // Drain: no copy may still be landing in shared memory at exit.
         if (lane == 0)
             for (int kk = max(0, k - S); kk < k; ++kk)
-                if (!mbar_wait(smem_u32(&full[kk % S]), (kk / S) & 1))
+                if (!mbar_wait_sleep(smem_u32(&full[kk % S]), (kk / S) & 1))
                     atomicOr(p.err, KV_DEVERR_TIMEOUT);
         return;
     }
@@ -1531,6 +1620,9 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     pol.setup(p);
 
     bool first_piece = true;
+    // stage and pass parity of this warp's next unit k (k = w, w + NCW, ...;
+    // S is a multiple of NCW): k % S and (k / S) & 1
+    int cs = w, cpar = 0;
     for (int u = start; u < end;) {
         const int b = find_seq(prefix, B, u, H);
         const int nb = prefix[b + 1] - prefix[b];
@@ -1556,9 +1648,15 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         // this warp's units of the piece: those with (uu - start) % NCW == w
         const int first = u + ((w - (u - start) % NCW) + NCW) % NCW;
         for (int uu = first; uu < piece_end; uu += NCW) {
-            const int k = uu - start, s = k % S;
+            const int s = cs;
+            cs += NCW;
+            const uint32_t par = cpar;
+            if (cs >= S) {
+                cs -= S;
+                cpar ^= 1;
+            }
             bool ok = *abort_flag == 0;
-            if (ok && !mbar_wait(smem_u32(&full[s]), (k / S) & 1)) {
+            if (ok && !mbar_wait_sleep(smem_u32(&full[s]), par)) {
                 *abort_flag = 1;
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
                 ok = false;

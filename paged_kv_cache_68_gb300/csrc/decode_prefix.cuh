@@ -361,8 +361,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
     constexpr int ELT = sizeof(T);
     constexpr int MS = kRows / G;                   // members per sub-group
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* smem = smem_align_1k(smem_raw);
     const int K = p.num_groups, S = p.stages, H = p.num_kv_heads, B = p.batch;
     const PLayout lay(S, K, BSC, D, ELT);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
@@ -440,7 +439,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                 if (lane == 0) {
                     const int s = k % S, ph = k / S;
                     bool ok = *abort_flag == 0;
-                    if (ok && ph > 0 && !mbar_wait(smem_u32(&empty[s]), (ph - 1) & 1)) {
+                    if (ok && ph > 0 && !mbar_wait_sleep(smem_u32(&empty[s]), (ph - 1) & 1)) {
                         *abort_flag = 1;
                         atomicOr(p.err, KV_DEVERR_TIMEOUT);
                         ok = false;
@@ -470,7 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
         }
         if (lane == 0)
             for (int kk = max(0, k - S); kk < k; ++kk)
-                if (!mbar_wait(smem_u32(&full[kk % S]), (kk / S) & 1))
+                if (!mbar_wait_sleep(smem_u32(&full[kk % S]), (kk / S) & 1))
                     atomicOr(p.err, KV_DEVERR_TIMEOUT);
         return;
     }
@@ -500,7 +499,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
         for (int uu = first; uu < piece_end; uu += NCW) {
             const int kk = uu - start, s = kk % S;
             bool ok = *abort_flag == 0;
-            if (ok && !mbar_wait(smem_u32(&full[s]), (kk / S) & 1)) {
+            if (ok && !mbar_wait_sleep(smem_u32(&full[s]), (kk / S) & 1)) {
                 *abort_flag = 1;
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
                 ok = false;

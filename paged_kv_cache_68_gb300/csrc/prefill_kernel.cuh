@@ -276,8 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
     constexpr int QT = BM / G;                    // queries per tile
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* smem = dec::smem_align_1k(smem_raw);
     const uint32_t sbase = dec::smem_u32(smem);
     auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
     auto sbar = [&](int x, int i) { return bar(BAR_STREAM + x * SB_N + i); };

@@ -105,6 +105,30 @@ def test_q8_append_special_rows(cache, sk, sv, dtype):
     assert_q8_pools_equal((gk, gv, gks, gvs), (rk, rv, rks, rvs), f"{cache} out of range")
 
 
+def test_q8_int8_v_scales_zero_then_jump():
+    """INT8 V scales that are zero over each sequence's first two blocks and
+    100x larger on one later block: the decode weighs P by each token's V
+    scale over the largest one met so far in the piece, which starts at zero
+    and then rises mid-sequence (with a rescale of the partial output)."""
+    w = wl.build_step("q8 vscale", 6, [20, 40, 300, 700, 1500], dtype="bf16", num_q_heads=32,
+                      num_kv_heads=8, head_dim=128, block_size=16)
+    p = wl.q8_pools(w, "int8", 11)
+    vs = np.array(p.v_scales, copy=True)                    # [N, Hkv, bs]
+    bt = np.asarray(w.block_tables)
+    for b, L in enumerate(np.asarray(w.seq_lens)):
+        nb = (int(L) + 15) // 16
+        for j in range(min(2, nb)):
+            vs[bt[b, j]] = 0.0
+        if nb > 4:
+            vs[bt[b, (3 * nb) // 5]] *= 100.0
+    p.v_scales = vs
+    gk, gv, gks, gvs, out, err = gpu_step_q8(w, p)
+    rk, rv, rks, rvs, ref = oracle_step_q8(w, p)
+    assert err == 0
+    assert_q8_pools_equal((gk, gv, gks, gvs), (rk, rv, rks, rvs), "int8 v scales")
+    print(check_attention(out, ref, w.dtype, "int8 v scales"))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("cache", ["fp8_e4m3", "int8"])
 def test_q8_llama_full_sampled(cache):
