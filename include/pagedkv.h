@@ -337,7 +337,7 @@ kv_status paged_attention_prefill(kv_pool_t pool, const void* q, void* out,
  * engine that reserves the whole device for its KV pool up front and forbids
  * allocation inside the decode loop, or a plug-in whose host framework owns
  * the allocator and passes it only input and output buffers.  The scratch
- * comes from an 8 MiB array compiled into the library, held on every device
+ * comes from a 32 MiB array compiled into the library, held on every device
  * that loads the library until the process exits.  Arguments, layouts and
  * results are those of paged_attention_decode.
  *
@@ -348,7 +348,7 @@ kv_status paged_attention_prefill(kv_pool_t pool, const void* q, void* out,
  * it and must be serialised by the caller.  Nothing persists in it between
  * calls.
  * Errors: those of paged_attention_decode, and KV_ENOWORKSPACE when the call
- *   would need more than the 8 MiB maximum (paged_attention_workspace_size
+ *   would need more than the 32 MiB maximum (paged_attention_workspace_size
  *   tells the need).
  */
 kv_status paged_attention_decode_noalloc(kv_pool_t pool, const void* q, void* out,

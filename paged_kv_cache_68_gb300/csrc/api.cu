@@ -61,6 +61,24 @@ bool encode_pool_map(CUtensorMap* map, void* base, const kv_pool& p, bool swizzl
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 16-bit head_dim-128 pool viewed as [heads][2 halves][N*bs rows][64 dims]
+// (dimension order 64 dims, rows, halves, heads): one box {64, bs, 2, 1} is a
+// block's rows for one KV head, 128-byte swizzled, the first half's bs rows
+// then the second half's -- the layout of two {64, 1, bs} boxes, in one copy.
+bool encode_pool_map_h2(CUtensorMap* map, void* base, const kv_pool& p) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t row = (cuuint64_t)p.num_kv_heads * 256u;       // bytes per token row
+    cuuint64_t dims[4] = {64u, (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_size, 2u,
+                          (cuuint64_t)p.num_kv_heads};
+    cuuint64_t strides[3] = {row, 128u, 256u};
+    cuuint32_t box[4] = {64u, (cuuint32_t)p.block_size, 2u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr size_t kMaxRingBytes = 128 * 1024;   // shared-memory ring per CTA, at most
@@ -146,10 +164,12 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     size_t off = 0;
     pl.ws_counter_off = off;
     off = align_up(off + 8ull * batch * pool.num_kv_heads, 256);
+    // two partial slots per worker (one worker per warp of the grid)
+    const size_t workers = (size_t)pl.num_ctas * dec::NCW;
     pl.ws_part_o_off = off;
-    off = align_up(off + 4ull * pl.num_ctas * 2 * G * D, 256);
+    off = align_up(off + 4ull * workers * 2 * G * D, 256);
     pl.ws_part_lse_off = off;
-    off = align_up(off + 4ull * pl.num_ctas * 2 * G, 256);
+    off = align_up(off + 4ull * workers * 2 * G, 256);
     pl.ws_bytes = off;
     {
         std::lock_guard<std::mutex> lock(pool.plan_mu);
@@ -280,6 +300,11 @@ static kv_status finish_pool(kv_pool* p, kv_pool_t* out) {
     if (maps_ok && p->has_swizzled_maps)
         maps_ok = encode_pool_map(&p->tmap_k_swz, k_pool, *p, true) &&
                   encode_pool_map(&p->tmap_v_swz, v_pool, *p, true);
+    // one-copy boxes for the tensor-core decode (without them it runs on the
+    // CUDA cores)
+    if (maps_ok && p->has_swizzled_maps && p->elem_bytes == 2)
+        p->has_h2_maps = encode_pool_map_h2(&p->tmap_k_h2, k_pool, *p) &&
+                         encode_pool_map_h2(&p->tmap_v_h2, v_pool, *p);
     if (!maps_ok) {
         cudaFree(p->d_err);
         delete p;

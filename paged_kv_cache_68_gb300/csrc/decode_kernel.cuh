@@ -1,5 +1,5 @@
 // PagedAttention decode for sm_103a: one persistent, token-balanced kernel fed
-// by TMA, with a log-sum-exp merge of the pieces cut across CTAs.
+// by TMA, with a log-sum-exp merge of the pieces cut across warps.
 //
 // What is computed ("Lecture 3", semidirectx.com CS349D notes, sec. 3.2; S06
 // "Implementation", llminference.xinbetween.com): for each sequence b and
@@ -8,32 +8,30 @@
 // softmaxes are merged with a running maximum and sum ("Lecture 24",
 // semidirectx.com CMU 11-868 notes, sec. 3.2 -- the FlashAttention /
 // Flash-Decoding trick); partial results of one sequence computed on
-// different CTAs are merged by log-sum-exp.
+// different warps are merged by log-sum-exp.
 //
 // Work decomposition.  A unit is one (sequence b, KV head g, logical block j).
 // Units are ordered b-major, then g, then j, and the U units are cut into
-// equal contiguous ranges, one per CTA of a persistent grid (#SMs x resident
-// CTAs), so every CTA streams the same number of KV blocks whatever the
-// length mix.  Every CTA derives the cut itself from seq_lens (a prefix sum in
-// shared memory): no host synchronisation, no atomics, no extra launch.  The
-// run of units of one (b, g) inside a CTA is a "piece".  A piece that is a
-// whole (b, g) is finished in the CTA and written to `out`; a piece cut by a
-// range boundary is written as a partial (normalised o, log2-sum-exp) to one
-// of two workspace slots of its CTA -- slot 0 for the CTA's first piece, slot
-// 1 for its last -- and counted in an epoch-tagged per-(b, g) counter; the CTA
-// that completes the count merges the partials by log-sum-exp (no second
-// kernel).
+// equal contiguous ranges, one per warp of a persistent grid (#SMs x resident
+// CTAs x NCW warps), so every warp streams the same number of KV blocks
+// whatever the length mix.  Every CTA derives the cut itself from seq_lens (a
+// prefix sum in shared memory): no host synchronisation, no atomics for
+// scheduling, no extra launch.  The run of units of one (b, g) inside a
+// warp's range is a "piece".  A piece that is a whole (b, g) is finished by
+// the warp and written to `out`; a piece cut by a range boundary is written
+// as a partial (normalised o, log2-sum-exp) to one of two workspace slots of
+// its warp -- slot 0 for the warp's first piece, slot 1 for its last -- and
+// counted in an epoch-tagged per-(b, g) counter; the warp that completes the
+// count merges the partials by log-sum-exp (no second kernel).
 //
-// One CTA = 1 producer warp + NCW consumer warps.  The producer walks the
-// CTA's units, looks each block id up in the block table, and issues the TMA
-// tile loads of the unit (the K and V rows of that block for KV head g: boxes
-// of the pool viewed as [N*bs, Hkv, D]) into a ring of S shared-memory stages
-// guarded by full/empty mbarriers.  Unit k of the CTA goes to stage k % S and
-// is consumed by warp k % NCW; S is a multiple of NCW, so every stage has one
-// fixed consumer that waits on it in order (the parity of an mbarrier wait is
-// only unambiguous when the waiter is at most one phase ahead).  The K/V of a
-// block is loaded once for the whole GQA group of G query heads.  Two compute
-// policies share this frame:
+// Each warp loads its own units: it owns S / NCW stages of the CTA's
+// shared-memory ring (one full mbarrier each), looks the block ids of its
+// next 32 units up in the block table (one lane each), and after attending a
+// unit issues the TMA tile loads of the unit S / NCW further on (the K and V
+// rows of that block for KV head g: boxes of the pool viewed as
+// [N*bs, Hkv, D]) into the stage it just read.  No warp waits on another.
+// The K/V of a block is loaded once for the whole GQA group of G query heads.
+// Two compute policies share this frame:
 //   CorePolicy (CUDA cores; fp32 pools, groups of 1-2, odd block sizes):
 //     QK with TPT lanes per token holding D/TPT dims of all G pre-scaled query
 //     rows, a transposing shuffle reduction, packed fp32x2 FMAs; PV with each
@@ -45,8 +43,7 @@
 //     transposed in registers with movmatrix and fed as bf16/f16 hi + lo
 //     halves, so its rounding stays below 2^-17 relative.
 // Softmax state is per block, per head, fp32, base 2.  Rows past the sequence
-// end never contribute.  At the end of a piece the NCW warps' (m, l, o) are
-// merged through shared memory by warp 0 (split arrive/sync named barriers).
+// end never contribute.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -62,7 +59,8 @@ namespace pagedkv {
 namespace dec {
 
 constexpr int NCW = 4;                       // consumer warps per CTA
-constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
+constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp (prefix pass)
+constexpr int SPLIT_THREADS = NCW * 32;      // split kernel: the consumer warps load too
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kMinChunk = 8;                 // fewest units a CTA is given
 
@@ -102,26 +100,23 @@ struct Params {
 
 // ---------------------------------------------------------------- layout ---
 struct Layout {
-    uint32_t full, empty, valid, misc, prefix, groups, skip, pst, pbuf, abuf, merge_o, merge_ml,
-        sring, ring;
-    uint32_t tx_bytes, stage_bytes, total;
+    uint32_t full, valid, misc, prefix, groups, skip, pst, pbuf, abuf, sring, ring;
+    uint32_t pst_bytes, tx_bytes, stage_bytes, total;
     // elt: bytes per pool element; K: cascade groups (0 for plain decode);
     // sb: scale bytes per token row of a tile (INT8 pools: 4)
     __host__ __device__ Layout(int S, int B, int bs, int G, int D, int elt, int K = 0, int sb = 0) {
         uint32_t off = 0;
         full = off;   off += 8u * S;
-        empty = off;  off += 8u * S;
         valid = off;  off += 4u * S;
         misc = off;   off += 4u * 40;            // abort flag + warp totals
         prefix = off; off += 4u * (B + 1);
         groups = off; off += K > 0 ? 4u * 3u * K : 0u;   // used groups: first, size, blocks
         skip = off;   off += K > 0 ? 4u * B : 0u;        // leading blocks each sequence skips
         off = (off + 15u) & ~15u;
-        pst = off;    off += K > 0 ? (4u * G * D + 4u * G + 15u) & ~15u : 0u;  // prefix state
+        pst_bytes = K > 0 ? (4u * G * D + 4u * G + 15u) & ~15u : 0u;
+        pst = off;    off += NCW * pst_bytes;    // prefix state, one per warp
         pbuf = off;   off += 8u * NCW * bs * G;
         abuf = off;   off += 8u * NCW * G;
-        merge_o = off;  off += 4u * (NCW - 1) * G * D;
-        merge_ml = off; off += 2u * 4u * (NCW - 1) * G;
         off = (off + 15u) & ~15u;
         sring = off;  off += (uint32_t)S * 2u * bs * sb;  // per stage: K then V scales
         off = (off + 1023u) & ~1023u;              // swizzle atoms are 1 KB
@@ -207,6 +202,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
         : "memory");
 }
 // Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
@@ -452,11 +455,10 @@ __host__ __device__ __forceinline__ int unit_chunk(int U, int num_ctas) {
 // ------------------------------------------------------- compute policies --
 // Both policies keep one warp's running softmax state for one (b, g) piece and
 // expose: begin (load the group's query rows), block (fold one KV block in),
-// fold (finish cross-lane sums), put (leave the state for warp 0) and
-// merge_store (warp 0: merge the other warps' states with its own, write the
-// output or the partial).
+// fold (finish cross-lane sums) and merge_store (normalise the state and
+// write the output or the partial).
 
-// Where warp 0 writes a finished piece.
+// Where a warp writes a finished piece.
 struct PieceOut {
     bool complete;        // whole (b, g): write `out`; else a partial slot
     void* out;            // &out[b, g*G, 0] (element type of the pool)
@@ -480,7 +482,8 @@ template <typename T, int D, int G, int BSC>
 struct CorePolicy {
     using C = Cfg<T, D, G>;
     static constexpr bool kSwizzled = false;
-    static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
+    static constexpr bool kH2 = false;        // tiles by the 3-D maps
+    static constexpr int kMinBlocks = G >= 8 ? 2 : (G >= 4 ? 3 : 4);
     static constexpr int kKvBytes = sizeof(T);   // pool element
     static constexpr int kScaleBytes = 0;
     static constexpr int kUnitBlocks = 1;        // pool blocks per work unit
@@ -609,21 +612,9 @@ struct CorePolicy {
                 }
     }
 
-    // merge area: o [NCW-1][G][D], then m [NCW-1][G], l [NCW-1][G]
-    __device__ __forceinline__ void put(float* mo, float* mm, int w, int lane) const {
-        const int dl = lane % C::LPV;
-        if (lane < C::LPV) {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-                *reinterpret_cast<float4*>(mo + ((w - 1) * G + h) * D + dl * 4) =
-                    make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-        }
-        if (lane < G) {
-            mm[(w - 1) * G + lane] = m_run;
-            mm[(NCW - 1) * G + (w - 1) * G + lane] = l_run;
-        }
-    }
-
+    // NW: warps whose states are merged (this one, and NW - 1 more left in
+    // mo / mm); the split kernel merges none (NW = 1).
+    template <int NW>
     __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
                                                 const PieceOut& po) const {
         const int dl = lane % C::LPV;
@@ -637,7 +628,7 @@ struct CorePolicy {
             const float l0 = __shfl_sync(FULL, l_run, h);
             float M = m0;
 #pragma unroll
-            for (int w2 = 1; w2 < NCW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
+            for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
             float den = 0.f;
             float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
             if (M != -CUDART_INF_F) {
@@ -645,9 +636,9 @@ struct CorePolicy {
                 den = c0 * l0;
                 num = make_float4(c0 * o[h][0].x, c0 * o[h][0].y, c0 * o[h][1].x, c0 * o[h][1].y);
 #pragma unroll
-                for (int w2 = 1; w2 < NCW; ++w2) {
+                for (int w2 = 1; w2 < NW; ++w2) {
                     const float c = fast_exp2(mm[(w2 - 1) * G + h] - M);
-                    den += c * mm[(NCW - 1) * G + (w2 - 1) * G + h];
+                    den += c * mm[(NW - 1) * G + (w2 - 1) * G + h];
                     const float4 ow =
                         *reinterpret_cast<const float4*>(mo + ((w2 - 1) * G + h) * D + dl * 4);
                     num.x += c * ow.x; num.y += c * ow.y; num.z += c * ow.z; num.w += c * ow.w;
@@ -690,13 +681,17 @@ struct CorePolicy {
 // kPermV: the MMA's output rows (m-slots) 16 mt + gid + 8 hf hold dims
 // 16 gid + 2 mt + hf instead of 16 mt + gid + 8 hf (the 8-bit policy loads V
 // that way); put / merge_store write every value to its own dim.
-template <typename T, int D, int G, int BSC, bool kPermV = false>
+// kPair: the tile holds two 8-row blocks, block i at byte 2048 i, each as
+// [half][8 rows][128 bytes] (block size 8, two blocks per work unit).
+template <typename T, int D, int G, int BSC, bool kPermV = false, bool kPair = false>
 struct TcPolicy {
     static_assert(sizeof(T) == 2, "tensor-core path takes 16-bit pools");
     static_assert(BSC % 16 == 0 && BSC > 0, "tensor-core path needs a block size of 16k");
     static_assert(G >= 1 && G <= 8, "the group's heads fill N = 8");
     static constexpr bool kSwizzled = true;
-    static constexpr int kMinBlocks = 3;
+    // 16-bit tiles come by the 4-D maps: one copy per block for both halves
+    static constexpr bool kH2 = sizeof(T) == 2 && D == 128;
+    static constexpr int kMinBlocks = 4;
     static constexpr int kKvBytes = sizeof(T);
     static constexpr int kScaleBytes = 0;
     static constexpr int kUnitBlocks = 1;  // pool blocks per work unit
@@ -721,10 +716,15 @@ struct TcPolicy {
         return kPermV ? 16 * gid + 2 * mt + hf : mt * 16 + gid + 8 * hf;
     }
 
+    // Byte offset of the 128-byte line holding half hf of row r: the halves
+    // are BSC rows apart (kPair: 8 rows apart within each 2 KB block).
+    __device__ static __forceinline__ int line(int r, int hf) {
+        return kPair ? (r >> 3) * 2048 + hf * 1024 + (r & 7) * 128 : hf * BSC * 128 + r * 128;
+    }
     // Shared address of 16-byte chunk c of row r in a 128-byte-swizzled tile
-    // of `rows` rows (chunks 0-7 in the first 128-byte half, 8-15 in the second).
+    // (chunks 0-7 in the first 128-byte half, 8-15 in the second).
     __device__ static __forceinline__ uint32_t swz(uint32_t tile, int r, int c) {
-        return tile + (uint32_t)((c >> 3) * BSC * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+        return tile + (uint32_t)(line(r, c >> 3) + (((c & 7) ^ (r & 7)) << 4));
     }
 
     // query head of MMA column n (-1: a padding column)
@@ -756,12 +756,13 @@ struct TcPolicy {
             // rows past the sequence end may hold anything; P is 0 there, and
             // 0 * NaN would still poison the MMA, so clear those V rows
             unsigned char* V = const_cast<unsigned char*>(Vs);
-            const int nbytes = (BSC - n_valid) * 128;
-            for (int i = lane * 16; i < nbytes; i += 32 * 16)
+            for (int i = lane; i < (BSC - n_valid) * 8; i += 32) {
+                const int r = n_valid + (i >> 3);
 #pragma unroll
                 for (int hf = 0; hf < D / 64; ++hf)
-                    *reinterpret_cast<uint4*>(V + hf * BSC * 128 + n_valid * 128 + i) =
+                    *reinterpret_cast<uint4*>(V + line(r, hf) + (i & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
+            }
             fence_proxy_async();
             __syncwarp();
         }
@@ -898,26 +899,9 @@ struct TcPolicy {
         }
     }
 
-    __device__ __forceinline__ void put(float* mo, float* mm, int w, int lane) const {
-        const int gid = lane >> 2, tig = lane & 3;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int h = 2 * tig + j;
-            if (h < G) {
-                float* row = mo + ((w - 1) * G + h) * D;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    row[dim(mt, gid, 0)] = oacc[mt][j];
-                    row[dim(mt, gid, 1)] = oacc[mt][j + 2];
-                }
-                if (gid == 0) {
-                    mm[(w - 1) * G + h] = m_run[j];
-                    mm[(NCW - 1) * G + (w - 1) * G + h] = l_run[j];
-                }
-            }
-        }
-    }
-
+    // NW: warps whose states are merged (this one, and NW - 1 more left in
+    // mo / mm); the split kernel merges none (NW = 1).
+    template <int NW>
     __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
                                                 const PieceOut& po) const {
         const int gid = lane >> 2, tig = lane & 3;
@@ -927,15 +911,15 @@ struct TcPolicy {
             if (h >= G) continue;
             float M = m_run[j];
 #pragma unroll
-            for (int w2 = 1; w2 < NCW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
-            float c[NCW];
+            for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
+            float c[NW];
             float den = 0.f;
             c[0] = M == -CUDART_INF_F ? 0.f : fast_exp2(m_run[j] - M);
             den = c[0] * l_run[j];
 #pragma unroll
-            for (int w2 = 1; w2 < NCW; ++w2) {
+            for (int w2 = 1; w2 < NW; ++w2) {
                 c[w2] = M == -CUDART_INF_F ? 0.f : fast_exp2(mm[(w2 - 1) * G + h] - M);
-                den += c[w2] * mm[(NCW - 1) * G + (w2 - 1) * G + h];
+                den += c[w2] * mm[(NW - 1) * G + (w2 - 1) * G + h];
             }
             float fs = 1.f, fp = 0.f;                 // cascade: fold the prefix state
             if (po.complete && po.pst_lse != nullptr) M = fold_state(M, den, po.pst_lse[h], fs, fp);
@@ -950,7 +934,7 @@ struct TcPolicy {
                     const int d = dim(mt, gid, hf);
                     float num = c[0] * oacc[mt][j + 2 * hf];
 #pragma unroll
-                    for (int w2 = 1; w2 < NCW; ++w2) num += c[w2] * mo[((w2 - 1) * G + h) * D + d];
+                    for (int w2 = 1; w2 < NW; ++w2) num += c[w2] * mo[((w2 - 1) * G + h) * D + d];
                     if (po.complete && po.pst_lse != nullptr) num = num * fs + po.pst_o[h * D + d] * fp;
                     v[mt][hf] = num * inv;
                 }
@@ -971,13 +955,15 @@ struct TcPolicy {
 };
 
 // Block size 8 on the tensor cores: a work unit is two consecutive logical
-// blocks, loaded into one 16-row tile (block i of the unit fills rows
-// 8 i .. 8 i + 7 of both 64-dim halves, the same 128-byte swizzle pattern),
-// and attended exactly like a 16-token block.
+// blocks, loaded into one 16-row tile (block i of the unit is rows
+// 8 i .. 8 i + 7, the 2 KB at byte 2048 i: its first 64-dim half, then its
+// second, the same 128-byte swizzle pattern), and attended exactly like a
+// 16-token block.
 template <typename T, int D, int G>
-struct TcPolicy8x2 : TcPolicy<T, D, G, 16> {
+struct TcPolicy8x2 : TcPolicy<T, D, G, 16, false, true> {
     static constexpr int kUnitBlocks = 2;
-    __device__ __forceinline__ TcPolicy8x2(float2* a, float2* b) : TcPolicy<T, D, G, 16>(a, b) {}
+    __device__ __forceinline__ TcPolicy8x2(float2* a, float2* b)
+        : TcPolicy<T, D, G, 16, false, true>(a, b) {}
 };
 
 // ---------------------------------------------------- 8-bit pools on MMA --
@@ -1039,7 +1025,8 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
     static constexpr int KS = Base::KS;
     static constexpr int MT = Base::MT;
     static constexpr bool kSwizzled = true;
-    static constexpr int kMinBlocks = 3;         // 12 consumer warps per SM beat 8 unspilled ones
+    static constexpr bool kH2 = false;           // one 128-byte code row: 3-D maps
+    static constexpr int kMinBlocks = 4;         // 16 consumer warps per SM at 128 registers
     static constexpr int kKvBytes = 1;
     static constexpr int kScaleBytes = FMT == kFmtInt8 ? 4 : 0;
 
@@ -1432,7 +1419,7 @@ __device__ __forceinline__ int group_skip(const int* vg, int K, int n, int b) {
 
 // ------------------------------------------------------------ split kernel --
 template <typename T, int D, int G, class Pol>
-__global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
+__global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_split(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
     constexpr int ELT = Pol::kKvBytes;             // bytes per pool element
@@ -1443,7 +1430,6 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
     const int bsu = bs * UB;                       // tokens per work unit
     const Layout lay(S, B, bsu, G, D, ELT, p.num_groups, Pol::kScaleBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc);
     int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
@@ -1458,10 +1444,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
 
     // -- 1. the blocks-per-sequence prefix of the clamped lengths -----------
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
-        }
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1473,7 +1456,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         const int nvg = cascade ? load_groups(p.g_first, p.g_size, p.g_blocks, p.num_groups,
                                               p.seq_lens, B, bs, cap, vg, warp_tot, p.err)
                                 : 0;
-        const int per = (B + NTHREADS - 1) / NTHREADS;
+        const int per = (B + SPLIT_THREADS - 1) / SPLIT_THREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int local = 0;
         bool over = false;
@@ -1501,127 +1484,137 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         if (prefix[b + 1] == prefix[b]) {
             T* ob = static_cast<T*>(p.out) + (size_t)b * p.num_q_heads * D;
             const bool has = cascade && skip_s[b] > 0;
-            for (int i = tid; i < p.num_q_heads * D; i += NTHREADS) {
+            for (int i = tid; i < p.num_q_heads * D; i += SPLIT_THREADS) {
                 const size_t row = (size_t)b * p.num_q_heads + i / D;
                 ob[i] = Elt<T>::store(has ? p.pst_o[row * D + i % D] : 0.f);
             }
         }
 
+    // -- 2. this warp's range of units -------------------------------------
+    // Every warp is a worker of its own: the units (b, g, j) are cut into
+    // equal contiguous ranges, one per warp of the grid, so no warp waits on
+    // another of its CTA from here on.
     const int U = prefix[B] * H;
-    const int chunk = unit_chunk(U, p.num_ctas);
-    const int start = blockIdx.x * chunk;
+    const int worker = blockIdx.x * NCW + warp;
+    const int chunk = unit_chunk(U, p.num_ctas * NCW);
+    const int start = worker * chunk;
     const int end = min(U, start + chunk);
     if (start >= end) return;
-
-    if (warp == NCW) {
-        // ---------------------------------------------------- producer warp --
-        // Lanes look up the block ids of the next 32 units in parallel; lane 0
-        // issues the TMA loads one unit at a time: one box per tile, or one
-        // per 128-byte half of the row for the swizzled layout.
-        constexpr int kBoxes = Pol::kSwizzled ? D * ELT / 128 : 1;
-        // a box is one block's rows of one 128-byte half (swizzled) or of the
-        // whole row; the halves of a unit's tile are bsu rows apart
-        const uint32_t box_bytes = (uint32_t)bs * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
-        const uint32_t half_bytes = (uint32_t)bsu * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
-        // block ids of unit uu: the first, and (UB = 2) the second or -2 when
-        // the sequence ends inside the first
-        auto fetch = [&](int uu, int& id, int& id2, int& gg) {
-            id = -1;
-            id2 = -2;
-            gg = 0;
-            if (uu < end) {
-                const int b = find_seq(prefix, B, uu, H);
-                const int nb = prefix[b + 1] - prefix[b];
-                const int r = uu - prefix[b] * H;
-                gg = r / nb;
-                const int lb = ((cascade ? skip_s[b] : 0) + (r - gg * nb)) * UB;
-                const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
-                id = __ldg(row + lb);
-                if (UB == 2 && (lb + 1) * bs < min(max(p.seq_lens[b], 0), cap))
-                    id2 = __ldg(row + lb + 1);
-            }
-        };
-        int id_cur, id2_cur, g_cur, id_nxt, id2_nxt, g_nxt;
-        fetch(start + lane, id_cur, id2_cur, g_cur);
-        int k = 0;
-        int s = 0, ph = 0;                         // stage and pass of unit k: k % S, k / S
-        for (int base = start; base < end; base += 32) {
-            fetch(base + 32 + lane, id_nxt, id2_nxt, g_nxt);
-            const int n = min(32, end - base);
-            for (int i = 0; i < n; ++i, ++k, s = s + 1 == S ? 0 : s + 1, ph += s == 0) {
-                const int id = __shfl_sync(FULL, id_cur, i);
-                const int id2 = __shfl_sync(FULL, id2_cur, i);
-                const int gg = __shfl_sync(FULL, g_cur, i);
-                if (lane == 0) {
-                    bool ok = *abort_flag == 0;
-                    if (ok && ph > 0 && !mbar_wait_sleep(smem_u32(&empty[s]), (ph - 1) & 1)) {
-                        *abort_flag = 1;
-                        atomicOr(p.err, KV_DEVERR_TIMEOUT);
-                        ok = false;
-                    }
-                    const uint32_t fb = smem_u32(&full[s]);
-                    const bool second = UB == 2 && id2 != -2;   // the unit's second block
-                    if (ok && id >= 0 && id < p.num_blocks &&
-                        (!second || (id2 >= 0 && id2 < p.num_blocks))) {
-                        valid[s] = 1;
-                        mbar_arrive_tx(fb, second ? lay.tx_bytes : lay.tx_bytes / UB);
-                        const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
-                        const uint32_t vdst = dst + (uint32_t)(bsu * D * ELT);
-#pragma unroll
-                        for (int x = 0; x < kBoxes; ++x) {
-                            const int col = x * (int)(128 / ELT);
-                            tma_load_3d(dst + x * half_bytes, &tmap_k, col, gg, id * bs, fb);
-                            tma_load_3d(vdst + x * half_bytes, &tmap_v, col, gg, id * bs, fb);
-                            if (second) {
-                                tma_load_3d(dst + x * half_bytes + box_bytes, &tmap_k, col, gg,
-                                            id2 * bs, fb);
-                                tma_load_3d(vdst + x * half_bytes + box_bytes, &tmap_v, col, gg,
-                                            id2 * bs, fb);
-                            }
-                        }
-                        if constexpr (Pol::kScaleBytes > 0) {
-                            const size_t srow = ((size_t)id * H + gg) * bs;
-                            const uint32_t sdst = smem_u32(smem + lay.sring) + (uint32_t)(s * 2 * bs * 4);
-                            bulk_load(sdst, p.k_scales + srow, (uint32_t)bs * 4u, fb);
-                            bulk_load(sdst + (uint32_t)bs * 4u, p.v_scales + srow, (uint32_t)bs * 4u,
-                                      fb);
-                        }
-                    } else {
-                        valid[s] = 0;
-                        if (ok) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-                        mbar_arrive(fb);
-                    }
-                }
-            }
-            __syncwarp();
-            id_cur = id_nxt;
-            id2_cur = id2_nxt;
-            g_cur = g_nxt;
-        }
-        // Drain: no copy may still be landing in shared memory at exit.
-        if (lane == 0)
-            for (int kk = max(0, k - S); kk < k; ++kk)
-                if (!mbar_wait_sleep(smem_u32(&full[kk % S]), (kk / S) & 1))
-                    atomicOr(p.err, KV_DEVERR_TIMEOUT);
-        return;
-    }
 
     // ---------------------------------------------------- consumer warps ----
     const int w = warp;
     float2* pb = reinterpret_cast<float2*>(smem + lay.pbuf) + w * bs * G;
     float2* ab = reinterpret_cast<float2*>(smem + lay.abuf) + w * G;
-    // merge area: warps 1..NCW-1 leave (o [G][D], m [G], l [G]) for warp 0
-    float* mo = reinterpret_cast<float*>(smem + lay.merge_o);
-    float* mm = reinterpret_cast<float*>(smem + lay.merge_ml);
-    float* pst_s = reinterpret_cast<float*>(smem + lay.pst);   // cascade: [G][D] then [G]
+    // cascade: this warp's copy of the prefix state, [G][D] then [G]
+    float* pst_s = reinterpret_cast<float*>(smem + lay.pst + w * lay.pst_bytes);
     const T* qbase = static_cast<const T*>(p.q);
     T* obase = static_cast<T*>(p.out);
     Pol pol(pb, ab);
     pol.setup(p);
 
-    bool first_piece = true;
-    // stage and pass parity of this warp's next unit k (k = w, w + NCW, ...;
-    // S is a multiple of NCW): k % S and (k / S) & 1
+    // -- 3. loads: each warp issues the TMA copies of its own units ---------
+    // Warp w owns stages w + NCW j (j < S / NCW); unit k = uu - start goes to
+    // j = k % (S / NCW).  After attending unit k the warp loads unit
+    // k + S / NCW into the same stage.  A box is one
+    // block's rows of one 128-byte half (swizzled) or of the whole row; the
+    // halves of a unit's tile are bsu rows apart.
+    constexpr int kBoxes = Pol::kSwizzled ? D * ELT / 128 : 1;
+    const uint32_t box_bytes = (uint32_t)bs * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
+    const uint32_t half_bytes = (uint32_t)bsu * (Pol::kSwizzled ? 128u : (uint32_t)(D * ELT));
+    const int per_warp = S / NCW;                  // stages this warp owns
+    // block ids of this warp's issue i (unit start + i): the first and
+    // (UB = 2) the second, -2 when the sequence ends inside the first; -1: none
+    auto fetch = [&](int i, int& id, int& id2, int& gg) {
+        id = -1;
+        id2 = -2;
+        gg = 0;
+        const int uu = start + i;
+        if (uu < end) {
+            const int b = find_seq(prefix, B, uu, H);
+            const int nb = prefix[b + 1] - prefix[b];
+            const int r = uu - prefix[b] * H;
+            gg = r / nb;
+            const int lb = ((cascade ? skip_s[b] : 0) + (r - gg * nb)) * UB;
+            const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
+            id = __ldg(row + lb);
+            if (UB == 2 && (lb + 1) * bs < min(max(p.seq_lens[b], 0), cap))
+                id2 = __ldg(row + lb + 1);
+        }
+    };
+    int nx = 0;                                    // issues made (= unit nx)
+    int ib = 0;                                    // first issue of the fetched batch
+    int is = w;                                    // stage of issue nx
+    // lane l holds issue ib + l and, one batch ahead (its table loads in
+    // flight meanwhile), issue ib + 32 + l
+    int id_b, id2_b, g_b, id_n, id2_n, g_n;
+    fetch(lane, id_b, id2_b, g_b);
+    fetch(32 + lane, id_n, id2_n, g_n);
+    const int n_issue = end - start;
+    auto issue_next = [&]() {
+        if (nx >= n_issue) return;
+        if (nx - ib == 32) {                       // (warp-uniform)
+            ib += 32;
+            id_b = id_n; id2_b = id2_n; g_b = g_n;
+            fetch(ib + 32 + lane, id_n, id2_n, g_n);
+        }
+        const int i = nx - ib;
+        const int id = __shfl_sync(FULL, id_b, i);
+        const int id2 = __shfl_sync(FULL, id2_b, i);
+        const int gg = __shfl_sync(FULL, g_b, i);
+        const int st = is;
+        ++nx;
+        is += NCW;
+        if (is >= S) is -= S;
+        if (lane == 0) {
+            const uint32_t fb = smem_u32(&full[st]);
+            const bool second = UB == 2 && id2 != -2;   // the unit's second block
+            if (*abort_flag == 0 && id >= 0 && id < p.num_blocks &&
+                (!second || (id2 >= 0 && id2 < p.num_blocks))) {
+                valid[st] = 1;
+                // the stage's last reads (generic proxy) before the copy's writes
+                fence_proxy_async();
+                mbar_arrive_tx(fb, second ? lay.tx_bytes : lay.tx_bytes / UB);
+                const uint32_t dst = smem_u32(ring + (size_t)st * lay.stage_bytes);
+                const uint32_t vdst = dst + (uint32_t)(bsu * D * ELT);
+                if constexpr (Pol::kH2) {
+                    // one copy per block: both halves, [half][bs rows][128 B]
+                    const uint32_t blk = 2u * (uint32_t)bs * 128u;
+                    tma_load_4d(dst, &tmap_k, 0, id * bs, 0, gg, fb);
+                    tma_load_4d(vdst, &tmap_v, 0, id * bs, 0, gg, fb);
+                    if (second) {
+                        tma_load_4d(dst + blk, &tmap_k, 0, id2 * bs, 0, gg, fb);
+                        tma_load_4d(vdst + blk, &tmap_v, 0, id2 * bs, 0, gg, fb);
+                    }
+                } else {
+#pragma unroll
+                    for (int x = 0; x < kBoxes; ++x) {
+                        const int col = x * (int)(128 / ELT);
+                        tma_load_3d(dst + x * half_bytes, &tmap_k, col, gg, id * bs, fb);
+                        tma_load_3d(vdst + x * half_bytes, &tmap_v, col, gg, id * bs, fb);
+                        if (second) {
+                            tma_load_3d(dst + x * half_bytes + box_bytes, &tmap_k, col, gg,
+                                        id2 * bs, fb);
+                            tma_load_3d(vdst + x * half_bytes + box_bytes, &tmap_v, col, gg,
+                                        id2 * bs, fb);
+                        }
+                    }
+                }
+                if constexpr (Pol::kScaleBytes > 0) {
+                    const size_t srow = ((size_t)id * H + gg) * bs;
+                    const uint32_t sdst = smem_u32(smem + lay.sring) + (uint32_t)(st * 2 * bs * 4);
+                    bulk_load(sdst, p.k_scales + srow, (uint32_t)bs * 4u, fb);
+                    bulk_load(sdst + (uint32_t)bs * 4u, p.v_scales + srow, (uint32_t)bs * 4u, fb);
+                }
+            } else {
+                valid[st] = 0;
+                if (*abort_flag == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                mbar_arrive(fb);
+            }
+        }
+    };
+    for (int i = 0; i < per_warp; ++i) issue_next();
+
+    // stage and pass parity of this warp's next unit
     int cs = w, cpar = 0;
     for (int u = start; u < end;) {
         const int b = find_seq(prefix, B, u, H);
@@ -1634,9 +1627,9 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
         const int Lb = min(max(p.seq_lens[b], 0), cap);
         const int skip = cascade ? skip_s[b] : 0;
         const size_t head0 = (size_t)b * p.num_q_heads + (size_t)g * G;
-        // cascade: warp 0, which merges, stages this (b, g)'s prefix state in
-        // shared memory while the piece's blocks are attended
-        if (w == 0 && skip > 0) {
+        // cascade: stage this (b, g)'s prefix state in shared memory while
+        // the piece's blocks are attended
+        if (skip > 0) {
             __syncwarp();                          // the last piece's reads are done
             for (int i = lane; i < G * D / 4; i += 32)
                 cp_async16(pst_s + 4 * i, p.pst_o + head0 * D + 4 * i);
@@ -1645,9 +1638,7 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
 
         pol.begin(qbase + head0 * D, p.qscale, lane);
 
-        // this warp's units of the piece: those with (uu - start) % NCW == w
-        const int first = u + ((w - (u - start) % NCW) + NCW) % NCW;
-        for (int uu = first; uu < piece_end; uu += NCW) {
+        for (int uu = u; uu < piece_end; ++uu) {
             const int s = cs;
             cs += NCW;
             const uint32_t par = cpar;
@@ -1670,23 +1661,14 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                                       : nullptr;
                 pol.block(Ks, Ks + bsu * D * ELT, sc, min(bsu, Lb - j * bsu), bsu, p.qscale, lane);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            __syncwarp();                          // every lane is done with stage s
+            issue_next();                          // unit k + S into stage s
         }
 
-        // -- merge the NCW warps' partial softmaxes of this piece -------------
-        // Warps 1..NCW-1 leave their state in shared memory and move on
-        // (bar.arrive); warp 0 waits for it (bar.sync), merges it with its own
-        // registers and writes the result; before a warp overwrites the area
-        // for its next piece it waits (bar.sync) for warp 0 to have read it.
+        // -- the piece's result: out, or a partial for the cross-warp merge ---
         pol.fold(lane);
-        if (w != 0) {
-            if (!first_piece) named_sync(2);
-            pol.put(mo, mm, w, lane);
-            named_arrive(1);
-        } else {
-            named_sync(1);
-            const size_t ps = (size_t)blockIdx.x * 2 + ((u == start) ? 0 : 1);
+        {
+            const size_t ps = (size_t)worker * 2 + ((u == start) ? 0 : 1);
             PieceOut po;
             po.complete = seg_start >= start && seg_start + nb <= end;
             po.out = obase + head0 * D;
@@ -1698,9 +1680,9 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                 cp_async_wait_all();
                 __syncwarp();
             }
-            pol.merge_store(mo, mm, lane, po);
+            pol.template merge_store<1>(nullptr, nullptr, lane, po);
             if (!po.complete) {
-                // Count the finished pieces of (b, g); the CTA that finishes
+                // Count the finished pieces of (b, g); the warp that finishes
                 // the last one merges all their partials into `out`.
                 __threadfence();
                 __syncwarp();
@@ -1720,12 +1702,17 @@ __global__ void __launch_bounds__(NTHREADS, Pol::kMinBlocks) paged_decode_split(
                                     });
                 }
             }
-            named_arrive(2);
         }
-        first_piece = false;
         u = piece_end;
     }
-    if (w != 0 && !first_piece) named_sync(2);   // match warp 0's last arrive
+    // Drain: no copy may still be landing in shared memory at exit (after a
+    // timeout the waits above were skipped).  The last per_warp issues hold
+    // distinct stages; a phase already waited on passes at once.
+    if (lane == 0)
+        for (int i = max(0, nx - per_warp); i < nx; ++i) {
+            if (!mbar_wait_sleep(smem_u32(&full[w + NCW * (i % per_warp)]), (i / per_warp) & 1))
+                atomicOr(p.err, KV_DEVERR_TIMEOUT);
+        }
 }
 
 // ------------------------------------------------------------- host side --
@@ -1768,7 +1755,7 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.fp8_v_scale = pool.fp8_v_scale;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.num_ctas);
-    cfg.blockDim = dim3(NTHREADS);
+    cfg.blockDim = dim3(SPLIT_THREADS);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1776,6 +1763,7 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (Pol::kH2) return cudaLaunchKernelEx(&cfg, split, pool.tmap_k_h2, pool.tmap_v_h2, p);
     if (Pol::kSwizzled)
         return cudaLaunchKernelEx(&cfg, split, pool.tmap_k_swz, pool.tmap_v_swz, p);
     return cudaLaunchKernelEx(&cfg, split, pool.tmap_k, pool.tmap_v, p);
@@ -1786,7 +1774,7 @@ cudaError_t attrs_typed(size_t smem, int* ctas_per_sm) {
     auto split = paged_decode_split<T, D, G, Pol>;
     cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split, NTHREADS, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split, SPLIT_THREADS, smem);
 }
 
 // Which compute policy runs a shape.  Tensor cores: 16-bit pools, head_dim
@@ -1802,7 +1790,7 @@ constexpr bool kTensorCores = sizeof(T) == 2 && D == 128 && (G == 4 || G == 8);
 inline bool use_tensor_cores(const kv_pool& pool, int G) {
     return pool.elem_bytes == 2 && pool.head_dim == 128 && (G == 4 || G == 8) &&
            (pool.block_size == 8 || pool.block_size == 16 || pool.block_size == 32) &&
-           pool.has_swizzled_maps;
+           pool.has_h2_maps;
 }
 
 template <typename T, int D, int G, template <typename, int, int, class> class Fn, typename... A>

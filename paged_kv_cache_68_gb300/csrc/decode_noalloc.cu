@@ -28,7 +28,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(8) << 20;   // 8 MiB
+constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];

@@ -41,6 +41,10 @@ struct kv_pool {
     CUtensorMap tmap_k_swz; // same view, box {128 bytes of dims, 1, block_size},
     CUtensorMap tmap_v_swz; //   128-byte swizzle (16-bit pools, head_dim 128)
     bool has_swizzled_maps;
+    CUtensorMap tmap_k_h2;  // 16-bit pools, head_dim 128: 4-D {64 dims, rows, 2 halves,
+    CUtensorMap tmap_v_h2;  //   heads}, box {64, block_size, 2, 1}, 128-byte swizzle: one
+    bool has_h2_maps = false;   // copy puts both 128-byte halves of a block's rows,
+                                // one after the other, in shared memory
     int device;
     int num_sms;
     // last decode plan, keyed by (batch, num_q_heads)

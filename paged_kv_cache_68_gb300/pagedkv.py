@@ -386,7 +386,7 @@ def paged_attention_decode_noalloc(handle, q, out, block_tables, seq_lens, scale
     """Decode without a workspace argument, for callers that cannot allocate
     device memory (an engine that reserved the device for its KV pool, a
     plug-in whose host framework owns the allocator): the library's built-in
-    8 MiB scratch array is used.  Calls that overlap on the GPU race on that
+    32 MiB scratch array is used.  Calls that overlap on the GPU race on that
     array; the first call on a device should precede any stream capture."""
     fn = load().paged_attention_decode_noalloc
     if fn.restype is not ctypes.c_int:
