@@ -494,8 +494,10 @@ def run_ours(args):
             pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     n_pairs = int(w.pairs.shape[0])
-    # copy (if pairs), append, decode (two kernels for a cascade decode)
-    launches_per_step = (1 if n_pairs else 0) + 1 + (2 if cascade else 1)
+    # copy (if pairs), append, decode (split, + merge for long contexts; a cascade decode adds
+    # the prefix pass)
+    dec_launches = pagedkv.paged_attention_decode_launches(pool.handle, w.batch, w.num_q_heads)
+    launches_per_step = (1 if n_pairs else 0) + 1 + dec_launches + (1 if cascade else 0)
 
     def step():
         pool.copy_blocks(pairs)
@@ -614,9 +616,9 @@ def run_ours(args):
         **unique_bytes_fields(w, world, max_dec_ms),
         "attention_gbs": round(att_bytes * world / (max_dec_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm",
-                     "kernel": ("paged_decode_prefix + paged_decode_split (the whole cascade decode call)"
+                     "kernel": ("paged_decode_prefix + paged_decode_split (+ paged_decode_merge) (the whole cascade decode call)"
                                 if cascade else
-                                "paged_decode_split (the whole decode call: one kernel, merges included)"),
+                                "paged_decode_split (+ paged_decode_merge) (the whole decode call)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
                      "traffic": (profiled_traffic()

@@ -210,6 +210,18 @@ kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_he
                                          size_t* bytes);
 
 /*
+ * paged_attention_decode_launches -- how many kernels one
+ * paged_attention_decode call with these arguments enqueues: 1 (the split
+ * kernel, which also merges the pieces it cut), or 2 (split, then a merge
+ * kernel: long contexts, where few (sequence, KV head) pairs are each cut
+ * across many warps' ranges).  Like the workspace size, it depends only on
+ * the arguments and the device.  A cascade call adds its prefix pass.
+ * Errors: KV_EINVAL (null launches, bad shape), KV_EUNSUPPORTED, KV_ECUDA.
+ */
+kv_status paged_attention_decode_launches(kv_pool_t pool, int batch, int num_q_heads,
+                                          int* launches);
+
+/*
  * paged_attention_decode -- one query token per sequence attends over its
  * whole cached context ("Lecture 3", sec. 3.2; S06 "Implementation").
  *

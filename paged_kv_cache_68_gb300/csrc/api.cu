@@ -405,6 +405,20 @@ kv_status paged_attention_workspace_size(kv_pool_t pool, int batch, int num_q_he
     return KV_OK;
 }
 
+kv_status paged_attention_decode_launches(kv_pool_t pool, int batch, int num_q_heads,
+                                          int* launches) {
+    if (!launches) return KV_EINVAL;
+    kv_status st = check_decode_shape(pool, batch, num_q_heads);
+    if (st != KV_OK) return st;
+    pagedkv::DecodePlan plan;
+    cudaError_t e = pagedkv::plan_decode(*pool, batch, num_q_heads, 0, &plan);
+    if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_launches");
+    *launches = 1 + (pagedkv::merge_warps_per_pair(plan.num_ctas * pagedkv::dec::NCW,
+                                                    batch * pool->num_kv_heads) > 0);
+    return KV_OK;
+}
+
 static kv_status decode_impl(kv_pool_t pool, const void* q, void* out,
                              const int32_t* block_tables, int max_blocks_per_seq,
                              const int32_t* seq_lens, int batch, int num_q_heads, float scale,

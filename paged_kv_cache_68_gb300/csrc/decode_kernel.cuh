@@ -51,6 +51,7 @@
 #include <cuda_fp8.h>
 #include <math_constants.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "pagedkv_internal.cuh"
@@ -96,6 +97,10 @@ struct Params {
     const float* k_scales; // [num_blocks][num_kv_heads][bs]
     const float* v_scales;
     float fp8_k_scale, fp8_v_scale;
+    // Partials of a (b, g) cut across warps: 0 = counted and merged in the
+    // split kernel by the warp that finishes last; > 0 = merged by
+    // paged_decode_merge, that many warps per (b, g) (they split its passes)
+    int merge_wpp;
 };
 
 // ---------------------------------------------------------------- layout ---
@@ -1269,24 +1274,27 @@ __host__ __device__ constexpr int merge_epl() {
          : ((R * D) % 64 == 0 && D % 2 == 0) ? 2 : 1;
 }
 
-template <int R, int D, class Store>
-__device__ __forceinline__ void merge_cut(const float* part_o, const float* part_lse, int c0,
-                                          int c1, int slot0, const float* x_o, const float* x_lse,
-                                          int lane, Store&& store) {
+// merge_cut over the element passes pass0, pass0 + pstep, ... (one warp each
+// when several warps share a segment), BATCH slots in flight at a time.
+template <int R, int D, int BATCH, class Store>
+__device__ __forceinline__ void merge_slots(const float* part_o, const float* part_lse, int c0,
+                                            int c1, int slot0, const float* x_o,
+                                            const float* x_lse, int lane, int pass0, int pstep,
+                                            Store&& store) {
     constexpr int E = R * D;
     constexpr int EPL = merge_epl<R, D>();
     static_assert(E % (32 * EPL) == 0, "rows x dims must be whole warps of lanes");
 #pragma unroll 1
-    for (int pass = 0; pass < E / (32 * EPL); ++pass) {
+    for (int pass = pass0; pass < E / (32 * EPL); pass += pstep) {
         const int e0 = (pass * 32 + lane) * EPL;
         const int r = e0 / D, d0 = e0 % D;
         float M = -CUDART_INF_F, den = 0.f, acc[EPL];
 #pragma unroll
         for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
-        for (int c = c0; c <= c1; c += kMergeBatch) {
-            float ls[kMergeBatch], ov[kMergeBatch][EPL];
+        for (int c = c0; c <= c1; c += BATCH) {
+            float ls[BATCH], ov[BATCH][EPL];
 #pragma unroll
-            for (int t = 0; t < kMergeBatch; ++t) {
+            for (int t = 0; t < BATCH; ++t) {
                 const int cc = c + t;
                 const size_t slot = (size_t)cc * 2 + (cc == c0 ? slot0 : 0);
                 ls[t] = -CUDART_INF_F;
@@ -1296,7 +1304,7 @@ __device__ __forceinline__ void merge_cut(const float* part_o, const float* part
                 }
             }
 #pragma unroll
-            for (int t = 0; t < kMergeBatch; ++t)
+            for (int t = 0; t < BATCH; ++t)
                 if (c + t <= c1) lse_add<EPL>(M, den, acc, ls[t], ov[t]);
         }
         if (x_lse != nullptr) {
@@ -1309,6 +1317,14 @@ __device__ __forceinline__ void merge_cut(const float* part_o, const float* part
         for (int k = 0; k < EPL; ++k) acc[k] *= inv;
         store(r, d0, acc, den > 0.f ? M + fast_log2(den) : -CUDART_INF_F);
     }
+}
+
+template <int R, int D, class Store>
+__device__ __forceinline__ void merge_cut(const float* part_o, const float* part_lse, int c0,
+                                          int c1, int slot0, const float* x_o, const float* x_lse,
+                                          int lane, Store&& store) {
+    merge_slots<R, D, kMergeBatch>(part_o, part_lse, c0, c1, slot0, x_o, x_lse, lane, 0, 1,
+                                   static_cast<Store&&>(store));
 }
 
 // ------------------------------------------------- block-wide scans --
@@ -1417,6 +1433,47 @@ __device__ __forceinline__ int group_skip(const int* vg, int K, int n, int b) {
     return b < vg[lo] + vg[K + lo] ? vg[2 * K + lo] : 0;
 }
 
+// -- the units of a call ------------------------------------------------------
+// prefix[b] (shared memory) = the units of KV head 0 in sequences before b:
+// each sequence contributes its blocks (clamped to the table's capacity, in
+// units of bsu tokens) less, for cascade decode, the leading blocks the
+// shared-prefix pass attended (skip_s[b]).  prefix[B] is the total.  Every
+// thread of the CTA calls; `report` flags contexts longer than the table.
+__device__ __forceinline__ void unit_prefix(const Params& p, unsigned char* smem, const Layout& lay,
+                                            int bsu, bool cascade, bool report) {
+    const int B = p.batch, tid = threadIdx.x, nthreads = blockDim.x;
+    const int cap = p.max_blocks * p.bs;
+    int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
+    int* prefix = reinterpret_cast<int*>(smem + lay.prefix);
+    int* skip_s = reinterpret_cast<int*>(smem + lay.skip);
+    // cascade: the leading blocks the shared-prefix pass attended
+    int* vg = reinterpret_cast<int*>(smem + lay.groups);
+    const int nvg = cascade ? load_groups(p.g_first, p.g_size, p.g_blocks, p.num_groups,
+                                          p.seq_lens, B, p.bs, cap, vg, warp_tot, p.err)
+                            : 0;
+    const int per = (B + nthreads - 1) / nthreads;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int local = 0;
+    bool over = false;
+    for (int b = b0; b < b1; ++b) {
+        const int L = p.seq_lens[b];
+        over |= L > cap;
+        const int nb = (min(max(L, 0), cap) + bsu - 1) / bsu;
+        const int skip = cascade ? min(group_skip(vg, p.num_groups, nvg, b), nb) : 0;
+        if (cascade) skip_s[b] = skip;
+        local += nb - skip;
+    }
+    if (over && report) atomicOr(p.err, KV_DEVERR_SEQ_RANGE);
+    int total = 0;
+    int run = block_excl_sum(local, warp_tot, &total);
+    for (int b = b0; b < b1; ++b) {
+        prefix[b] = run;
+        const int nb = (min(max(p.seq_lens[b], 0), cap) + bsu - 1) / bsu;
+        run += nb - (cascade ? skip_s[b] : 0);
+    }
+    if (tid == 0) prefix[B] = total;
+}
+
 // ------------------------------------------------------------ split kernel --
 template <typename T, int D, int G, class Pol>
 __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_split(
@@ -1450,34 +1507,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
     }
     pdl_launch_dependents();
     pdl_wait();                                    // inputs of earlier kernels are visible
-    {
-        // cascade: the leading blocks the shared-prefix pass attended
-        int* vg = reinterpret_cast<int*>(smem + lay.groups);
-        const int nvg = cascade ? load_groups(p.g_first, p.g_size, p.g_blocks, p.num_groups,
-                                              p.seq_lens, B, bs, cap, vg, warp_tot, p.err)
-                                : 0;
-        const int per = (B + SPLIT_THREADS - 1) / SPLIT_THREADS;
-        const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-        int local = 0;
-        bool over = false;
-        for (int b = b0; b < b1; ++b) {
-            const int L = p.seq_lens[b];
-            over |= L > cap;
-            const int nb = (min(max(L, 0), cap) + bsu - 1) / bsu;
-            const int skip = cascade ? min(group_skip(vg, p.num_groups, nvg, b), nb) : 0;
-            if (cascade) skip_s[b] = skip;
-            local += nb - skip;
-        }
-        if (over && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_SEQ_RANGE);
-        int total = 0;
-        int run = block_excl_sum(local, warp_tot, &total);
-        for (int b = b0; b < b1; ++b) {
-            prefix[b] = run;
-            const int nb = (min(max(p.seq_lens[b], 0), cap) + bsu - 1) / bsu;
-            run += nb - (cascade ? skip_s[b] : 0);
-        }
-        if (tid == 0) prefix[B] = total;
-    }
+    unit_prefix(p, smem, lay, bsu, cascade, blockIdx.x == 0);
     __syncthreads();
     // sequences no unit covers: zeros, or (cascade) the prefix state alone
     for (int b = blockIdx.x; b < B; b += gridDim.x)
@@ -1681,9 +1711,10 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                 __syncwarp();
             }
             pol.template merge_store<1>(nullptr, nullptr, lane, po);
-            if (!po.complete) {
+            if (!po.complete && p.merge_wpp == 0) {
                 // Count the finished pieces of (b, g); the warp that finishes
-                // the last one merges all their partials into `out`.
+                // the last one merges all their partials into `out`.  (With
+                // merge_wpp > 0 the partials wait for paged_decode_merge.)
                 __threadfence();
                 __syncwarp();
                 const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
@@ -1713,6 +1744,53 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
             if (!mbar_wait_sleep(smem_u32(&full[w + NCW * (i % per_warp)]), (i / per_warp) & 1))
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
         }
+}
+
+// ------------------------------------------------------------ merge kernel --
+// After the split kernel (programmatic dependent launch): merge_wpp warps per
+// (sequence b, KV head g), in a grid-stride loop.  A (b, g) whose units fall
+// in more than one warp's range was left as partials in those warps' slots
+// (the first warp's slot 0 or 1, every later warp's slot 0); its warps merge
+// them by log-sum-exp (with the cascade prefix state, if any) into `out`.
+// The split kernel's cut is recomputed here from the same seq_lens and grid.
+template <typename T, int D, int G, int UB>
+__global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_align_1k(smem_raw);
+    const int B = p.batch, H = p.num_kv_heads;
+    const int bsu = p.bs * UB;
+    const Layout lay(0, B, bsu, G, D, 2, p.num_groups, 0);
+    const int* prefix = reinterpret_cast<const int*>(smem + lay.prefix);
+    const int* skip_s = reinterpret_cast<const int*>(smem + lay.skip);
+    const bool cascade = UB == 1 && p.num_groups > 0;
+    pdl_wait();                                    // the split kernel's partials are visible
+    unit_prefix(p, smem, lay, bsu, cascade, false);
+    __syncthreads();
+    const int U = prefix[B] * H;
+    const int chunk = unit_chunk(U, p.num_ctas * NCW);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    T* obase = static_cast<T*>(p.out);
+    const int wpp = p.merge_wpp;
+    const int nwarps = gridDim.x * NCW;
+    for (int task = blockIdx.x * NCW + warp; task < B * H * wpp; task += nwarps) {
+        const int pair = task / wpp, sub = task - pair * wpp;
+        const int b = pair / H, g = pair - b * H;
+        const int nb = prefix[b + 1] - prefix[b];
+        if (nb == 0) continue;
+        const int seg_start = prefix[b] * H + g * nb;
+        const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
+        if (c0 == c1) continue;                    // one warp's: written by the split kernel
+        const size_t head0 = (size_t)b * p.num_q_heads + (size_t)g * G;
+        const bool pst = cascade && skip_s[b] > 0;
+        T* ob = obase + head0 * D;
+        merge_slots<G, D, 4>(p.part_o, p.part_lse, c0, c1, seg_start == c0 * chunk ? 0 : 1,
+                             pst ? p.pst_o + head0 * D : nullptr, pst ? p.pst_lse + head0 : nullptr,
+                             lane, sub, wpp, [&](int r, int d0, const float* v, float) {
+#pragma unroll
+                                 for (int k = 0; k < merge_epl<G, D>(); ++k)
+                                     ob[r * D + d0 + k] = Elt<T>::store(v[k]);
+                             });
+    }
 }
 
 // ------------------------------------------------------------- host side --
@@ -1763,10 +1841,23 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (Pol::kH2) return cudaLaunchKernelEx(&cfg, split, pool.tmap_k_h2, pool.tmap_v_h2, p);
-    if (Pol::kSwizzled)
-        return cudaLaunchKernelEx(&cfg, split, pool.tmap_k_swz, pool.tmap_v_swz, p);
-    return cudaLaunchKernelEx(&cfg, split, pool.tmap_k, pool.tmap_v, p);
+    // where the partials of cut (b, g) merge: in this kernel or a second one
+    const int pairs = call.batch * pool.num_kv_heads;
+    p.merge_wpp = merge_warps_per_pair(plan.num_ctas * NCW, pairs);
+    if (Pol::kH2)
+        e = cudaLaunchKernelEx(&cfg, split, pool.tmap_k_h2, pool.tmap_v_h2, p);
+    else if (Pol::kSwizzled)
+        e = cudaLaunchKernelEx(&cfg, split, pool.tmap_k_swz, pool.tmap_v_swz, p);
+    else
+        e = cudaLaunchKernelEx(&cfg, split, pool.tmap_k, pool.tmap_v, p);
+    if (e != cudaSuccess || p.merge_wpp == 0) return e;
+    // the partials of (b, g) cut across warps, merged behind the split kernel
+    auto merge = paged_decode_merge<T, D, G, Pol::kUnitBlocks>;
+    const Layout ml(0, call.batch, pool.block_size * Pol::kUnitBlocks, G, D, 2, call.num_groups, 0);
+    cfg.gridDim = dim3((unsigned)std::max(1, std::min((pairs * p.merge_wpp + NCW - 1) / NCW,
+                                                      pool.num_sms * 4)));
+    cfg.dynamicSmemBytes = ml.pst + 1024;
+    return cudaLaunchKernelEx(&cfg, merge, p);
 }
 
 template <typename T, int D, int G, class Pol>

@@ -57,6 +57,15 @@ struct kv_pool {
 
 namespace pagedkv {
 
+// Where the decode merges the partials of a (b, g) cut across warp ranges
+// (warps = the split grid's warps, pairs = batch x KV heads): 0 = in the
+// split kernel, by the warp that finishes last (a cut (b, g) has two or three
+// partials); > 0 = in the merge kernel, that many warps per (b, g) (long
+// contexts: dozens of partials each).
+inline int merge_warps_per_pair(int warps, int pairs) {
+    return warps < 2 * pairs ? 0 : (pairs <= 512 ? 4 : 1);
+}
+
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxGroups = 1024;   // cascade decode: groups per call
 

@@ -75,6 +75,7 @@ def load(build: bool = True) -> ctypes.CDLL:
             "kv_append": ([P, P, P, P, I, P], I),
             "copy_blocks": ([P, P, I, P], I),
             "paged_attention_workspace_size": ([P, I, I, ctypes.POINTER(S)], I),
+            "paged_attention_decode_launches": ([P, I, I, ctypes.POINTER(I)], I),
             "paged_attention_decode": ([P, P, P, P, I, P, I, I, F, I, P, S, P], I),
             "paged_attention_cascade_workspace_size": ([P, I, I, I, ctypes.POINTER(S)], I),
             "paged_attention_decode_cascade": ([P, P, P, P, I, P, I, I, F, I, P, P, P, I, P, S, P], I),
@@ -195,6 +196,13 @@ def kv_swap_blocks(handle, host_k, host_v, pairs, direction: int, host_k_scales=
                                  hs(host_k_scales, "host_k_scales"),
                                  hs(host_v_scales, "host_v_scales"), int(host_k.shape[0]), ptr, n,
                                  int(direction), _stream(stream)), "kv_swap_blocks")
+
+
+def paged_attention_decode_launches(handle, batch: int, num_q_heads: int) -> int:
+    out = ctypes.c_int()
+    _check(load().paged_attention_decode_launches(handle, batch, num_q_heads, ctypes.byref(out)),
+           "paged_attention_decode_launches")
+    return int(out.value)
 
 
 def paged_attention_workspace_size(handle, batch: int, num_q_heads: int) -> int:

@@ -65,6 +65,23 @@ def test_shared_prefix_fresh_fork_copies():
     _full_check(w, "fresh fork")
 
 
+@pytest.mark.parametrize("batch,median,hi,launches", [(256, 48, 400, 1), (4, 1500, 6000, 2)])
+def test_both_merge_paths(batch, median, hi, launches):
+    """A (sequence, KV head) cut across warp ranges is merged in the split
+    kernel when the pairs are many (one launch) and by a second kernel when a
+    few pairs are each cut across many ranges (two launches): both against
+    the oracle, at sizes that reach each path."""
+    w = wl.llama3_8b_gqa(11, batch=batch, median=median, hi=hi)
+    k = torch.empty(tuple(w.k_pool.shape), dtype=TORCH_DTYPE[w.dtype], device="cuda")
+    pool = pagedkv.KVPool(k, k.clone())
+    try:
+        n = pagedkv.paged_attention_decode_launches(pool.handle, w.batch, w.num_q_heads)
+    finally:
+        pool.close()
+    assert n == launches
+    _full_check(w, f"merge path ({launches} launches)")
+
+
 # -- full sizes, in the launch configuration the benchmark times --------------------
 
 @pytest.mark.slow
