@@ -119,9 +119,12 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     const int G = num_q_heads / pool.num_kv_heads;
     const int D = pool.head_dim, elt = pool.elem_bytes;
     const bool q8 = is_q8(pool);
-    // tokens per work unit: block size 8 on the tensor cores pairs two blocks
-    // (TcPolicy8x2); the kernel lays out its ring for the same unit size
-    const int bs = pool.block_size * (!q8 && pool.block_size == 8 && dec::use_tensor_cores(pool, G) ? 2 : 1);
+    // tokens per work unit: block size 8 on the tensor cores, and 8-bit pools
+    // of block size 16 with groups of 4 or 8, pair two blocks (TcPolicy8x2,
+    // Tc8Policy2); the kernel lays out its ring for the same unit size
+    const bool pairs = q8 ? dec::q8_pairs_blocks(pool, G)
+                          : pool.block_size == 8 && dec::use_tensor_cores(pool, G);
+    const int bs = pool.block_size * (pairs ? 2 : 1);
     const int sb = pool.cache_dtype == KV_INT8 ? 4 : 0;     // scale bytes per tile row
     const size_t stage = 2ull * bs * D * elt + 2ull * bs * sb;
     // Ring depth S is a multiple of the consumer-warp count (each stage has a

@@ -1209,6 +1209,14 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
     }
 };
 
+// Two consecutive 16-row blocks per work unit (the kernel puts the second
+// block's code rows, and its INT8 scales, right after the first's).
+template <typename T, int D, int G, int FMT>
+struct Tc8Policy2 : Tc8Policy<T, D, G, FMT> {
+    static constexpr int kUnitBlocks = 2;
+    __device__ __forceinline__ Tc8Policy2(float2* a, float2* b) : Tc8Policy<T, D, G, FMT>(a, b) {}
+};
+
 // ------------------------------------------------- cross-CTA partial merge --
 // Pieces of one (b, g) cut across CTAs: CTA c holds its piece in slot
 // (c, 0) when the piece is its first, else (c, 1).  The piece counter is
@@ -1630,10 +1638,17 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                     }
                 }
                 if constexpr (Pol::kScaleBytes > 0) {
+                    // per stage: the unit's K scales [bsu], then its V scales [bsu]
                     const size_t srow = ((size_t)id * H + gg) * bs;
-                    const uint32_t sdst = smem_u32(smem + lay.sring) + (uint32_t)(st * 2 * bs * 4);
+                    const uint32_t sdst = smem_u32(smem + lay.sring) + (uint32_t)(st * 2 * bsu * 4);
                     bulk_load(sdst, p.k_scales + srow, (uint32_t)bs * 4u, fb);
-                    bulk_load(sdst + (uint32_t)bs * 4u, p.v_scales + srow, (uint32_t)bs * 4u, fb);
+                    bulk_load(sdst + (uint32_t)bsu * 4u, p.v_scales + srow, (uint32_t)bs * 4u, fb);
+                    if (second) {
+                        const size_t srow2 = ((size_t)id2 * H + gg) * bs;
+                        bulk_load(sdst + (uint32_t)bs * 4u, p.k_scales + srow2, (uint32_t)bs * 4u, fb);
+                        bulk_load(sdst + (uint32_t)(bsu + bs) * 4u, p.v_scales + srow2,
+                                  (uint32_t)bs * 4u, fb);
+                    }
                 }
             } else {
                 valid[st] = 0;
@@ -1687,7 +1702,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                 const int j = skip + j0 + (uu - u);
                 const unsigned char* Ks = ring + (size_t)s * lay.stage_bytes;
                 const float* sc = Pol::kScaleBytes > 0
-                                      ? reinterpret_cast<const float*>(smem + lay.sring) + s * 2 * bs
+                                      ? reinterpret_cast<const float*>(smem + lay.sring) + s * 2 * bsu
                                       : nullptr;
                 pol.block(Ks, Ks + bsu * D * ELT, sc, min(bsu, Lb - j * bsu), bsu, p.qscale, lane);
             }
@@ -1943,8 +1958,17 @@ inline bool q8_shape_ok(const kv_pool& pool) {
     return pool.head_dim == 128 && pool.block_size % 16 == 0 && pool.block_size <= 256;
 }
 
+// Block size 16 with groups of 4 or 8: a work unit is two consecutive blocks
+// (a 32-row tile, the second block's rows after the first's), which halves
+// the per-unit costs (loads issued, barrier waits) per token.
+inline bool q8_pairs_blocks(const kv_pool& pool, int G) {
+    return pool.block_size == 16 && (G == 4 || G == 8);
+}
+
 template <typename T, int FMT, template <typename, int, int, class> class Fn, typename... A>
-cudaError_t with_q8_policy(int G, A... args) {
+cudaError_t with_q8_policy(int G, bool pairs, A... args) {
+    if (pairs && G == 4) return Fn<T, 128, 4, Tc8Policy2<T, 128, 4, FMT>>::run(args...);
+    if (pairs && G == 8) return Fn<T, 128, 8, Tc8Policy2<T, 128, 8, FMT>>::run(args...);
     if (G == 1) return Fn<T, 128, 1, Tc8Policy<T, 128, 1, FMT>>::run(args...);
     if (G == 2) return Fn<T, 128, 2, Tc8Policy<T, 128, 2, FMT>>::run(args...);
     if (G == 4) return Fn<T, 128, 4, Tc8Policy<T, 128, 4, FMT>>::run(args...);
@@ -1956,20 +1980,22 @@ template <typename T>
 cudaError_t dispatch_q8(const kv_pool& pool, const DecodeCall& call, const DecodePlan& plan,
                         cudaStream_t stream) {
     if (!q8_shape_ok(pool)) return cudaErrorNotSupported;
+    const bool pairs = q8_pairs_blocks(pool, plan.group);
     if (pool.cache_dtype == KV_FP8_E4M3)
-        return with_q8_policy<T, kFmtE4M3, LaunchFn>(plan.group, &pool, &call, &plan, stream);
+        return with_q8_policy<T, kFmtE4M3, LaunchFn>(plan.group, pairs, &pool, &call, &plan, stream);
     if (pool.cache_dtype == KV_INT8)
-        return with_q8_policy<T, kFmtInt8, LaunchFn>(plan.group, &pool, &call, &plan, stream);
+        return with_q8_policy<T, kFmtInt8, LaunchFn>(plan.group, pairs, &pool, &call, &plan, stream);
     return cudaErrorNotSupported;
 }
 
 template <typename T>
 cudaError_t attrs_q8(const kv_pool& pool, int group, size_t smem, int* ctas_per_sm) {
     if (!q8_shape_ok(pool)) return cudaErrorNotSupported;
+    const bool pairs = q8_pairs_blocks(pool, group);
     if (pool.cache_dtype == KV_FP8_E4M3)
-        return with_q8_policy<T, kFmtE4M3, AttrsFn>(group, smem, ctas_per_sm);
+        return with_q8_policy<T, kFmtE4M3, AttrsFn>(group, pairs, smem, ctas_per_sm);
     if (pool.cache_dtype == KV_INT8)
-        return with_q8_policy<T, kFmtInt8, AttrsFn>(group, smem, ctas_per_sm);
+        return with_q8_policy<T, kFmtInt8, AttrsFn>(group, pairs, smem, ctas_per_sm);
     return cudaErrorNotSupported;
 }
 
