@@ -39,6 +39,7 @@ METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), seq-steps/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_decode_split_llama3_8b_gqa.md")
+PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "paged_decode_split_fp8_llama3_8b_gqa.md")
 DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "decode_kernel.cuh")
 PREFILL_SUMMARY = os.path.join(ROOT, "profiles", "paged_prefill_chunked_llama3_8b.md")
 PREFILL_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "prefill_kernel.cuh")
@@ -621,8 +622,9 @@ def run_ours(args):
                                 "paged_decode_split (+ paged_decode_merge) (the whole decode call)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": (profiled_traffic()
-                                 if (not cascade and q8 is None and args.workload == "llama3_8b_gqa"
+                     "traffic": (profiled_traffic(PROFILE_SUMMARY_FP8 if q8 is not None else None)
+                                 if (not cascade and (q8 is None or q8.cache == "fp8_e4m3")
+                                     and args.workload == "llama3_8b_gqa"
                                      and args.batch is None and args.seed == 0
                                      and args.placement == "random") else None),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)",

@@ -527,8 +527,9 @@ def value_to_torch(a, dtype: str, device):
 
 
 def value_to_numpy(t, dtype: str) -> np.ndarray:
-    """Torch tensor (any device) or host array -> raw host array."""
-    if isinstance(t, np.ndarray):
+    """Torch tensor (any device) or host array -> raw host array (None stays None:
+    an 8-bit step drops its 16-bit pools)."""
+    if t is None or isinstance(t, np.ndarray):
         return t
     import torch
     t = t.detach().contiguous()
