@@ -32,7 +32,7 @@ struct PrefixPlan {
 
 bool cascade_shape(const kv_pool& pool, int group) {
     return pool.elem_bytes == 2 && pool.head_dim == 128 && (group == 4 || group == 8) &&
-           (pool.block_size == 16 || pool.block_size == 32) && pool.has_swizzled_maps;
+           (pool.block_size == 16 || pool.block_size == 32) && pool.has_h2_maps;
 }
 
 template <typename T, int G, int BSC>
@@ -59,7 +59,7 @@ cudaError_t prefix_launch(const kv_pool& pool, const dec::PParams& p, size_t sme
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, pool.tmap_k_swz, pool.tmap_v_swz, p);
+    return cudaLaunchKernelEx(&cfg, k, pool.tmap_k_h2, pool.tmap_v_h2, p);
 }
 
 // Dispatch on (dtype, group, block size) for one of the two functions above.

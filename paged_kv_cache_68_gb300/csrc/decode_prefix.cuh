@@ -426,7 +426,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                 id = __ldg(p.block_tables + (size_t)gfirst[k] * p.max_blocks + r % P);
             }
         };
-        const uint32_t box_bytes = BSC * 128u;
         int id_cur, g_cur, id_nxt, g_nxt;
         fetch(start + lane, id_cur, g_cur);
         int k = 0;
@@ -449,13 +448,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                         valid[s] = 1;
                         mbar_arrive_tx(fb, lay.stage_bytes);
                         const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
-#pragma unroll
-                        for (int x = 0; x < D * ELT / 128; ++x) {
-                            const int col = x * (128 / ELT);
-                            tma_load_3d(dst + x * box_bytes, &tmap_k, col, gg, id * BSC, fb);
-                            tma_load_3d(dst + lay.stage_bytes / 2 + x * box_bytes, &tmap_v, col, gg,
-                                        id * BSC, fb);
-                        }
+                        // one 4-D copy per block: both 128-byte halves, [half][rows]
+                        tma_load_4d(dst, &tmap_k, 0, id * BSC, 0, gg, fb);
+                        tma_load_4d(dst + lay.stage_bytes / 2, &tmap_v, 0, id * BSC, 0, gg, fb);
                     } else {
                         valid[s] = 0;
                         if (ok) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
