@@ -59,7 +59,7 @@
 namespace pagedkv {
 namespace dec {
 
-constexpr int NCW = 4;                       // consumer warps per CTA
+constexpr int NCW = 4;                       // attending warps per CTA
 constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp (prefix pass)
 constexpr int SPLIT_THREADS = NCW * 32;      // split kernel: the consumer warps load too
 constexpr unsigned FULL = 0xffffffffu;
@@ -226,7 +226,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
-// Named barriers among the NCW consumer warps (id 0 is __syncthreads).
+// Named barriers among the NCW attending warps (id 0 is __syncthreads; the
+// prefix pass's warps merge through them).
 __device__ __forceinline__ void named_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NCW * 32) : "memory");
 }
@@ -977,7 +978,7 @@ struct TcPolicy8x2 : TcPolicy<T, D, G, 16, false, true> {
 // turned back into wider numbers when read): FP8 E4M3 with one scale per pool,
 // or INT8 with one fp32 scale per (block, KV head, token row).  The tiles
 // arrive by TMA with the 128-byte swizzle (one 128-byte row per token); INT8
-// scales come by bulk copy into a small ring beside them.  The consumer builds
+// scales come by bulk copy into a small ring beside them.  The warp builds
 // the f16 MMA fragments straight from the codes in registers -- every E4M3
 // value and every integer in [-128, 127] is an f16, so the conversion is
 // exact -- with no shared-memory round trip:
@@ -1031,7 +1032,7 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
     static constexpr int MT = Base::MT;
     static constexpr bool kSwizzled = true;
     static constexpr bool kH2 = false;           // one 128-byte code row: 3-D maps
-    static constexpr int kMinBlocks = 4;         // 16 consumer warps per SM at 128 registers
+    static constexpr int kMinBlocks = 4;         // 16 warps per SM at 128 registers
     static constexpr int kKvBytes = 1;
     static constexpr int kScaleBytes = FMT == kFmtInt8 ? 4 : 0;
 
@@ -1217,11 +1218,12 @@ struct Tc8Policy2 : Tc8Policy<T, D, G, FMT> {
     __device__ __forceinline__ Tc8Policy2(float2* a, float2* b) : Tc8Policy<T, D, G, FMT>(a, b) {}
 };
 
-// ------------------------------------------------- cross-CTA partial merge --
-// Pieces of one (b, g) cut across CTAs: CTA c holds its piece in slot
-// (c, 0) when the piece is its first, else (c, 1).  The piece counter is
-// tagged with the call's epoch, so a value left by an earlier call (or never
-// written) counts as zero; the CTA that completes the count resets it.
+// ---------------------------------------------- cross-range partial merge --
+// Pieces of one (b, g) cut across work ranges (a warp's in the split kernel,
+// a CTA's in the prefix pass): range c holds its piece in slot (c, 0) when
+// the piece is its first, else (c, 1).  The piece counter is tagged with the
+// call's epoch, so a value left by an earlier call (or never written) counts
+// as zero; the worker that completes the count resets it.
 __device__ __forceinline__ int count_piece(unsigned long long* ctr, unsigned epoch, int pieces) {
     const unsigned long long tag = (unsigned long long)epoch << 32;
     unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
@@ -1265,9 +1267,9 @@ __device__ __forceinline__ void load_row(float* v, const float* src, bool cached
     }
 }
 
-// One warp merges the partial states that a segment cut across CTAs c0..c1
-// left in their slots (CTA c0's piece in slot slot0 of c0, every later CTA's
-// in slot 0), plus an optional extra state (x_o, x_lse; null for none).  Each
+// One warp merges the partial states that a segment cut across ranges c0..c1
+// left in their slots (range c0's piece in slot slot0 of c0, every later
+// range's in slot 0), plus an optional extra state (x_o, x_lse; null for none).  Each
 // is a normalised output [R][D] with its log2-sum-exp [R]:
 //   out[r, d] = sum_i 2^(lse_i[r] - M) o_i[r, d] / sum_i 2^(lse_i[r] - M).
 // A lane owns EPL consecutive dims of one row; the slots are read
@@ -1539,7 +1541,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
     const int end = min(U, start + chunk);
     if (start >= end) return;
 
-    // ---------------------------------------------------- consumer warps ----
+    // ------------------------------------------------------ the warp's work --
     const int w = warp;
     float2* pb = reinterpret_cast<float2*>(smem + lay.pbuf) + w * bs * G;
     float2* ab = reinterpret_cast<float2*>(smem + lay.abuf) + w * G;
