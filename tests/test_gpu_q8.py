@@ -46,8 +46,8 @@ def test_q8_llama_small(cache, sk, sv, dtype):
 
 
 @pytest.mark.parametrize("cache", ["fp8_e4m3", "int8"])
-@pytest.mark.parametrize("hq,hkv,bs", [(4, 4, 16), (8, 4, 32), (16, 4, 16), (16, 2, 64),
-                                       (40, 40, 16), (8, 1, 48)])
+@pytest.mark.parametrize("hq,hkv,bs", [(4, 4, 16), (8, 4, 32), (16, 4, 16), (16, 2, 16),
+                                       (16, 2, 64), (40, 40, 16), (8, 1, 48)])
 def test_q8_groups_and_block_sizes(cache, hq, hkv, bs):
     ctx = [0, 1, bs - 1, bs, 2 * bs + 3, 5 * bs, 301]
     w = wl.build_step("q8 shapes", 4, ctx, dtype="bf16", num_q_heads=hq, num_kv_heads=hkv,
