@@ -618,11 +618,8 @@ struct CorePolicy {
                 }
     }
 
-    // NW: warps whose states are merged (this one, and NW - 1 more left in
-    // mo / mm); the split kernel merges none (NW = 1).
-    template <int NW>
-    __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
-                                                const PieceOut& po) const {
+    // Normalise the warp's state and write `out` or the partial slot.
+    __device__ __forceinline__ void merge_store(int lane, const PieceOut& po) const {
         const int dl = lane % C::LPV;
         // every load of the merge before the first store: the compiler
         // cannot move a load above a store it might alias
@@ -630,25 +627,13 @@ struct CorePolicy {
         float lse[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float m0 = __shfl_sync(FULL, m_run, h);
+            float M = __shfl_sync(FULL, m_run, h);
             const float l0 = __shfl_sync(FULL, l_run, h);
-            float M = m0;
-#pragma unroll
-            for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
             float den = 0.f;
             float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
             if (M != -CUDART_INF_F) {
-                const float c0 = fast_exp2(m0 - M);
-                den = c0 * l0;
-                num = make_float4(c0 * o[h][0].x, c0 * o[h][0].y, c0 * o[h][1].x, c0 * o[h][1].y);
-#pragma unroll
-                for (int w2 = 1; w2 < NW; ++w2) {
-                    const float c = fast_exp2(mm[(w2 - 1) * G + h] - M);
-                    den += c * mm[(NW - 1) * G + (w2 - 1) * G + h];
-                    const float4 ow =
-                        *reinterpret_cast<const float4*>(mo + ((w2 - 1) * G + h) * D + dl * 4);
-                    num.x += c * ow.x; num.y += c * ow.y; num.z += c * ow.z; num.w += c * ow.w;
-                }
+                den = l0;
+                num = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
             }
             if (po.complete && po.pst_lse != nullptr) {
                 float cs, cp;
@@ -686,7 +671,7 @@ struct CorePolicy {
 // are padding (zero query rows) and are never written out.
 // kPermV: the MMA's output rows (m-slots) 16 mt + gid + 8 hf hold dims
 // 16 gid + 2 mt + hf instead of 16 mt + gid + 8 hf (the 8-bit policy loads V
-// that way); put / merge_store write every value to its own dim.
+// that way); merge_store writes every value to its own dim.
 // kPair: the tile holds two 8-row blocks, block i at byte 2048 i, each as
 // [half][8 rows][128 bytes] (block size 8, two blocks per work unit).
 template <typename T, int D, int G, int BSC, bool kPermV = false, bool kPair = false>
@@ -905,28 +890,16 @@ struct TcPolicy {
         }
     }
 
-    // NW: warps whose states are merged (this one, and NW - 1 more left in
-    // mo / mm); the split kernel merges none (NW = 1).
-    template <int NW>
-    __device__ __forceinline__ void merge_store(const float* mo, const float* mm, int lane,
-                                                const PieceOut& po) const {
+    // Normalise the warp's state and write `out` or the partial slot.
+    __device__ __forceinline__ void merge_store(int lane, const PieceOut& po) const {
         const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int h = 2 * tig + j;
             if (h >= G) continue;
             float M = m_run[j];
-#pragma unroll
-            for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mm[(w2 - 1) * G + h]);
-            float c[NW];
-            float den = 0.f;
-            c[0] = M == -CUDART_INF_F ? 0.f : fast_exp2(m_run[j] - M);
-            den = c[0] * l_run[j];
-#pragma unroll
-            for (int w2 = 1; w2 < NW; ++w2) {
-                c[w2] = M == -CUDART_INF_F ? 0.f : fast_exp2(mm[(w2 - 1) * G + h] - M);
-                den += c[w2] * mm[(NW - 1) * G + (w2 - 1) * G + h];
-            }
+            const float c0 = M == -CUDART_INF_F ? 0.f : 1.f;   // an empty state counts zero
+            float den = c0 * l_run[j];
             float fs = 1.f, fp = 0.f;                 // cascade: fold the prefix state
             if (po.complete && po.pst_lse != nullptr) M = fold_state(M, den, po.pst_lse[h], fs, fp);
             const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -938,9 +911,7 @@ struct TcPolicy {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int d = dim(mt, gid, hf);
-                    float num = c[0] * oacc[mt][j + 2 * hf];
-#pragma unroll
-                    for (int w2 = 1; w2 < NW; ++w2) num += c[w2] * mo[((w2 - 1) * G + h) * D + d];
+                    float num = c0 * oacc[mt][j + 2 * hf];
                     if (po.complete && po.pst_lse != nullptr) num = num * fs + po.pst_o[h * D + d] * fp;
                     v[mt][hf] = num * inv;
                 }
@@ -1727,7 +1698,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                 cp_async_wait_all();
                 __syncwarp();
             }
-            pol.template merge_store<1>(nullptr, nullptr, lane, po);
+            pol.merge_store(lane, po);
             if (!po.complete && p.merge_wpp == 0) {
                 // Count the finished pieces of (b, g); the warp that finishes
                 // the last one merges all their partials into `out`.  (With
