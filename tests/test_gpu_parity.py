@@ -82,6 +82,29 @@ def test_both_merge_paths(batch, median, hi, launches):
     _full_check(w, f"merge path ({launches} launches)")
 
 
+def test_max_batch_of_short_and_empty_sequences():
+    """4,096 sequences (the largest batch) of 0-41 tokens, one in twenty empty:
+    thousands of short pieces per warp range, and (b, g) pairs with no units."""
+    rng = np.random.default_rng(21)
+    ctx = rng.integers(0, 41, size=4096)
+    w = wl.build_step("max batch", 21, ctx, dtype="bf16", num_q_heads=32, num_kv_heads=8,
+                      head_dim=128, block_size=16)
+    lens = np.asarray(w.seq_lens).copy()
+    lens[rng.random(4096) < 0.05] = 0
+    w.seq_lens = lens.astype(np.int32)
+    print(_full_check(w, "max batch, short and empty"))
+
+
+def test_long_contexts_with_an_empty_sequence():
+    """The merge kernel's path (few (b, g) pairs, each cut across many warp
+    ranges) with a zero-length sequence among the long ones."""
+    w = wl.long_context(5, batch=3, lo=3000, hi=9000, block_size=16)
+    lens = np.asarray(w.seq_lens).copy()
+    lens[1] = 0
+    w.seq_lens = lens.astype(np.int32)
+    print(_full_check(w, "long contexts, one empty"))
+
+
 # -- full sizes, in the launch configuration the benchmark times --------------------
 
 @pytest.mark.slow
