@@ -1857,17 +1857,19 @@ cudaError_t attrs_typed(size_t smem, int* ctas_per_sm) {
 }
 
 // Which compute policy runs a shape.  Tensor cores: 16-bit pools, head_dim
-// 128, groups of 4 or 8, block size 8 (two blocks per unit), 16 or 32, a pool
-// with swizzled descriptors.  CUDA cores otherwise, with the token loops unrolled for block
+// 128, groups of 1, 2, 4 or 8 (groups of up to 4 fill the free MMA columns
+// with the lo halves of P), block size 8 (two blocks per unit), 16 or 32, a
+// pool with one-copy (4-D) tensor maps.  CUDA cores otherwise (fp32 pools,
+// head_dim 64, other block sizes), with the token loops unrolled for block
 // size 16 (and 8 / 32 on bf16 head_dim 128); other block sizes take the
 // generic instance.
 template <typename T, int D>
 constexpr bool kExtraBlockSizes = std::is_same<T, __nv_bfloat16>::value && D == 128;
 template <typename T, int D, int G>
-constexpr bool kTensorCores = sizeof(T) == 2 && D == 128 && (G == 4 || G == 8);
+constexpr bool kTensorCores = sizeof(T) == 2 && D == 128 && (G == 1 || G == 2 || G == 4 || G == 8);
 
 inline bool use_tensor_cores(const kv_pool& pool, int G) {
-    return pool.elem_bytes == 2 && pool.head_dim == 128 && (G == 4 || G == 8) &&
+    return pool.elem_bytes == 2 && pool.head_dim == 128 && (G == 1 || G == 2 || G == 4 || G == 8) &&
            (pool.block_size == 8 || pool.block_size == 16 || pool.block_size == 32) &&
            pool.has_h2_maps;
 }
