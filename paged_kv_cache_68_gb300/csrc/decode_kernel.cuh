@@ -1933,15 +1933,17 @@ inline bool q8_shape_ok(const kv_pool& pool) {
     return pool.head_dim == 128 && pool.block_size % 16 == 0 && pool.block_size <= 256;
 }
 
-// Block size 16 with groups of 4 or 8: a work unit is two consecutive blocks
-// (a 32-row tile, the second block's rows after the first's), which halves
-// the per-unit costs (loads issued, barrier waits) per token.
+// Block size 16: a work unit is two consecutive blocks (a 32-row tile, the
+// second block's rows after the first's), which halves the per-unit costs
+// (loads issued, barrier waits) per token.
 inline bool q8_pairs_blocks(const kv_pool& pool, int G) {
-    return pool.block_size == 16 && (G == 4 || G == 8);
+    return pool.block_size == 16 && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
 template <typename T, int FMT, template <typename, int, int, class> class Fn, typename... A>
 cudaError_t with_q8_policy(int G, bool pairs, A... args) {
+    if (pairs && G == 1) return Fn<T, 128, 1, Tc8Policy2<T, 128, 1, FMT>>::run(args...);
+    if (pairs && G == 2) return Fn<T, 128, 2, Tc8Policy2<T, 128, 2, FMT>>::run(args...);
     if (pairs && G == 4) return Fn<T, 128, 4, Tc8Policy2<T, 128, 4, FMT>>::run(args...);
     if (pairs && G == 8) return Fn<T, 128, 8, Tc8Policy2<T, 128, 8, FMT>>::run(args...);
     if (G == 1) return Fn<T, 128, 1, Tc8Policy<T, 128, 1, FMT>>::run(args...);
