@@ -1734,15 +1734,60 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         }
 }
 
+// Shared memory the merge kernel's warps exchange their states through: per
+// warp, element pass and lane, the running (M, den) and EPL numerators.
+template <int G, int D>
+__host__ __device__ constexpr int merge_red_bytes() {
+    return NCW * (G * D / (32 * merge_epl<G, D>())) * 32 * (merge_epl<G, D>() + 2) * 4;
+}
+
+// One warp's share of a cut segment: the unnormalised log-sum-exp state
+// (base M, denominator den, numerators acc) of the partials in slots of
+// ranges lo..hi (range c0's piece in slot slot0 of c0, every later range's in
+// slot 0) for element pass `pass`, BATCH slots' loads in flight together.
+template <int R, int D, int BATCH>
+__device__ __forceinline__ void lse_range(const float* part_o, const float* part_lse, int lo,
+                                          int hi, int c0, int slot0, int pass, int lane,
+                                          float& M, float& den, float* acc) {
+    constexpr int EPL = merge_epl<R, D>();
+    const int e0 = (pass * 32 + lane) * EPL;
+    const int r = e0 / D, d0 = e0 % D;
+    M = -CUDART_INF_F;
+    den = 0.f;
+#pragma unroll
+    for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
+    for (int c = lo; c <= hi; c += BATCH) {
+        float ls[BATCH], ov[BATCH][EPL];
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t) {
+            const int cc = c + t;
+            const size_t slot = (size_t)cc * 2 + (cc == c0 ? slot0 : 0);
+            ls[t] = -CUDART_INF_F;
+            if (cc <= hi) {
+                ls[t] = __ldcg(part_lse + slot * R + r);
+                load_row<EPL>(ov[t], part_o + (slot * R + r) * D + d0, true);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t)
+            if (c + t <= hi) lse_add<EPL>(M, den, acc, ls[t], ov[t]);
+    }
+}
+
 // ------------------------------------------------------------ merge kernel --
-// After the split kernel (programmatic dependent launch): merge_wpp warps per
-// (sequence b, KV head g), in a grid-stride loop.  A (b, g) whose units fall
-// in more than one warp's range was left as partials in those warps' slots
-// (the first warp's slot 0 or 1, every later warp's slot 0); its warps merge
-// them by log-sum-exp (with the cascade prefix state, if any) into `out`.
-// The split kernel's cut is recomputed here from the same seq_lens and grid.
+// After the split kernel (programmatic dependent launch): the (sequence b,
+// KV head g) pairs whose units fall in more than one warp's range were left
+// as partials in those warps' slots (the first warp's slot 0 or 1, every later
+// warp's slot 0); they are merged by log-sum-exp (with the cascade prefix
+// state, if any) into `out`.  merge_wpp = NCW: a CTA takes one pair at a time
+// and its warps split the pair's partials, then combine their states through
+// shared memory (long contexts: dozens of partials per pair); merge_wpp = 1:
+// a warp per pair.  The split kernel's cut is recomputed here from the same
+// seq_lens and grid.
 template <typename T, int D, int G, int UB>
 __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params p) {
+    constexpr int EPL = merge_epl<G, D>();
+    constexpr int NP = G * D / (32 * EPL);         // element passes of a warp
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_align_1k(smem_raw);
     const int B = p.batch, H = p.num_kv_heads;
@@ -1750,6 +1795,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
     const Layout lay(0, B, bsu, G, D, 2, p.num_groups, 0);
     const int* prefix = reinterpret_cast<const int*>(smem + lay.prefix);
     const int* skip_s = reinterpret_cast<const int*>(smem + lay.skip);
+    float* red = reinterpret_cast<float*>(smem + lay.pst);   // [NCW][NP][32][EPL + 2]
     const bool cascade = UB == 1 && p.num_groups > 0;
     pdl_wait();                                    // the split kernel's partials are visible
     unit_prefix(p, smem, lay, bsu, cascade, false);
@@ -1758,10 +1804,68 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
     const int chunk = unit_chunk(U, p.num_ctas * NCW);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     T* obase = static_cast<T*>(p.out);
-    const int wpp = p.merge_wpp;
-    const int nwarps = gridDim.x * NCW;
-    for (int task = blockIdx.x * NCW + warp; task < B * H * wpp; task += nwarps) {
-        const int pair = task / wpp, sub = task - pair * wpp;
+    auto store = [&](T* ob, int r, int d0, const float* v) {
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) ob[r * D + d0 + k] = Elt<T>::store(v[k]);
+    };
+    if (p.merge_wpp == NCW) {
+        for (int pair = blockIdx.x; pair < B * H; pair += gridDim.x) {   // CTA-uniform
+            const int b = pair / H, g = pair - b * H;
+            const int nb = prefix[b + 1] - prefix[b];
+            if (nb == 0) continue;
+            const int seg_start = prefix[b] * H + g * nb;
+            const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
+            if (c0 == c1) continue;                // one warp's: written by the split kernel
+            const int slot0 = seg_start == c0 * chunk ? 0 : 1;
+            const int per = (c1 - c0 + NCW) / NCW;
+            const int lo = c0 + warp * per, hi = min(c1, lo + per - 1);
+#pragma unroll
+            for (int pass = 0; pass < NP; ++pass) {
+                float M, den, acc[EPL];
+                lse_range<G, D, 8>(p.part_o, p.part_lse, lo, hi, c0, slot0, pass, lane, M, den, acc);
+                float* st = red + ((warp * NP + pass) * 32 + lane) * (EPL + 2);
+                st[0] = M;
+                st[1] = den;
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) st[2 + k] = acc[k];
+            }
+            __syncthreads();
+            const size_t head0 = (size_t)b * p.num_q_heads + (size_t)g * G;
+            const bool pst = cascade && skip_s[b] > 0;
+            for (int pass = warp; pass < NP; pass += NCW) {
+                float M = -CUDART_INF_F;
+#pragma unroll
+                for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, red[((w2 * NP + pass) * 32 + lane) * (EPL + 2)]);
+                float den = 0.f, acc[EPL];
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
+                if (M != -CUDART_INF_F) {
+#pragma unroll
+                    for (int w2 = 0; w2 < NCW; ++w2) {
+                        const float* st = red + ((w2 * NP + pass) * 32 + lane) * (EPL + 2);
+                        const float c = st[0] == -CUDART_INF_F ? 0.f : fast_exp2(st[0] - M);
+                        den += c * st[1];
+#pragma unroll
+                        for (int k = 0; k < EPL; ++k) acc[k] += c * st[2 + k];
+                    }
+                }
+                const int e0 = (pass * 32 + lane) * EPL;
+                const int r = e0 / D, d0 = e0 % D;
+                if (pst) {                          // the cascade prefix state, normalised
+                    float xv[EPL];
+                    load_row<EPL>(xv, p.pst_o + head0 * D + r * D + d0, false);
+                    lse_add<EPL>(M, den, acc, p.pst_lse[head0 + r], xv);
+                }
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) acc[k] *= inv;
+                store(obase + head0 * D, r, d0, acc);
+            }
+            __syncthreads();                       // red is read before the next pair's writes
+        }
+        return;
+    }
+    for (int pair = blockIdx.x * NCW + warp; pair < B * H; pair += gridDim.x * NCW) {
         const int b = pair / H, g = pair - b * H;
         const int nb = prefix[b + 1] - prefix[b];
         if (nb == 0) continue;
@@ -1773,10 +1877,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
         T* ob = obase + head0 * D;
         merge_slots<G, D, 4>(p.part_o, p.part_lse, c0, c1, seg_start == c0 * chunk ? 0 : 1,
                              pst ? p.pst_o + head0 * D : nullptr, pst ? p.pst_lse + head0 : nullptr,
-                             lane, sub, wpp, [&](int r, int d0, const float* v, float) {
-#pragma unroll
-                                 for (int k = 0; k < merge_epl<G, D>(); ++k)
-                                     ob[r * D + d0 + k] = Elt<T>::store(v[k]);
+                             lane, 0, 1, [&](int r, int d0, const float* v, float) {
+                                 store(ob, r, d0, v);
                              });
     }
 }
@@ -1842,9 +1944,14 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     // the partials of (b, g) cut across warps, merged behind the split kernel
     auto merge = paged_decode_merge<T, D, G, Pol::kUnitBlocks>;
     const Layout ml(0, call.batch, pool.block_size * Pol::kUnitBlocks, G, D, 2, call.num_groups, 0);
+    const size_t merge_smem = ml.pst + merge_red_bytes<G, D>() + 1024;
     cfg.gridDim = dim3((unsigned)std::max(1, std::min((pairs * p.merge_wpp + NCW - 1) / NCW,
                                                       pool.num_sms * 4)));
-    cfg.dynamicSmemBytes = ml.pst + 1024;
+    cfg.dynamicSmemBytes = merge_smem;
+    if (merge_smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
+        if (e != cudaSuccess) return e;
+    }
     return cudaLaunchKernelEx(&cfg, merge, p);
 }
 

@@ -65,12 +65,14 @@ def test_shared_prefix_fresh_fork_copies():
     _full_check(w, "fresh fork")
 
 
-@pytest.mark.parametrize("batch,median,hi,launches", [(256, 48, 400, 1), (4, 1500, 6000, 2)])
+@pytest.mark.parametrize("batch,median,hi,launches", [(256, 48, 400, 1), (96, 48, 400, 2),
+                                                      (4, 1500, 6000, 2)])
 def test_both_merge_paths(batch, median, hi, launches):
     """A (sequence, KV head) cut across warp ranges is merged in the split
-    kernel when the pairs are many (one launch) and by a second kernel when a
-    few pairs are each cut across many ranges (two launches): both against
-    the oracle, at sizes that reach each path."""
+    kernel when the pairs are many (one launch) and by a second kernel when
+    there are fewer (two launches: one warp per pair for some hundreds of
+    pairs, four warps sharing a pair's partials for a few pairs): each
+    against the oracle, at sizes that reach each path."""
     w = wl.llama3_8b_gqa(11, batch=batch, median=median, hi=hi)
     k = torch.empty(tuple(w.k_pool.shape), dtype=TORCH_DTYPE[w.dtype], device="cuda")
     pool = pagedkv.KVPool(k, k.clone())
