@@ -99,7 +99,7 @@ struct Params {
     float fp8_k_scale, fp8_v_scale;
     // Partials of a (b, g) cut across warps: 0 = counted and merged in the
     // split kernel by the warp that finishes last; > 0 = merged by
-    // paged_decode_merge, that many warps per (b, g) (they split its passes)
+    // paged_decode_merge, that many warps per (b, g) (they split its partials)
     int merge_wpp;
 };
 
