@@ -1470,9 +1470,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc);
-    int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
-    int* prefix = reinterpret_cast<int*>(smem + lay.prefix);
-    int* skip_s = reinterpret_cast<int*>(smem + lay.skip);
+    const int* prefix = reinterpret_cast<const int*>(smem + lay.prefix);
+    const int* skip_s = reinterpret_cast<const int*>(smem + lay.skip);
     unsigned char* ring = smem + lay.ring;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
