@@ -1003,7 +1003,10 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
     static constexpr int MT = Base::MT;
     static constexpr bool kSwizzled = true;
     static constexpr bool kH2 = false;           // one 128-byte code row: 3-D maps
-    static constexpr int kMinBlocks = 4;         // 16 warps per SM at 128 registers
+    // A ring of two 8 KB stages per warp (32 code rows of K and V) leaves room
+    // for 3 CTAs per SM, and so do larger blocks: up to 168 registers a
+    // thread cost no occupancy (the two-tile step needs about 160).
+    static constexpr int kMinBlocks = 3;
     static constexpr int kKvBytes = 1;
     static constexpr int kScaleBytes = FMT == kFmtInt8 ? 4 : 0;
 
@@ -1068,47 +1071,67 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
         Rinv = 0.f;
     }
 
+    // Two 16-token tiles per step (rows t0 .. t0 + 31): both tiles' QK
+    // products are issued together, one max vote covers the 32 tokens, then
+    // both tiles' PV products.  When the rows end inside the first tile the
+    // second tile's scores are masked and its V rows read as zeros; its K
+    // reads stay inside the stage (a K tile is followed by its V tile).
     __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
                                           const float* sc, int n_valid, int bs, float, int lane) {
         const int gid = lane >> 2, tig = lane & 3;
-        for (int t0 = 0; t0 < n_valid; t0 += 16) {
-            const unsigned char* Kt = Ks + t0 * 128;
-            const unsigned char* Vt = Vs + t0 * 128;
-            // -- S^T of the tile: 16 tokens x the group's heads -----------------
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int t0 = 0; t0 < n_valid; t0 += 32) {
+            // -- S^T of the two tiles: 16 tokens x the group's heads each ------
+            float acc[2][2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) acc[x][c][0] = acc[x][c][1] = acc[x][c][2] = acc[x][c][3] = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const uint4 ra = chunk(Kt, gid, 2 * tig + h), rb = chunk(Kt, gid + 8, 2 * tig + h);
-                const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+                uint32_t wa[2][4], wb[2][4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t a[4];
-                    cvt4<FMT>(wa[q], a[0], a[2]);
-                    cvt4<FMT>(wb[q], a[1], a[3]);
-                    Mma<__half>::run(acc[q & 1], a, this->qb[4 * h + q][0], this->qb[4 * h + q][1]);
+                for (int x = 0; x < 2; ++x) {
+                    const unsigned char* Kt = Ks + (t0 + 16 * x) * 128;
+                    const uint4 ra = chunk(Kt, gid, 2 * tig + h), rb = chunk(Kt, gid + 8, 2 * tig + h);
+                    wa[x][0] = ra.x; wa[x][1] = ra.y; wa[x][2] = ra.z; wa[x][3] = ra.w;
+                    wb[x][0] = rb.x; wb[x][1] = rb.y; wb[x][2] = rb.z; wb[x][3] = rb.w;
                 }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        uint32_t a[4];
+                        cvt4<FMT>(wa[x][q], a[0], a[2]);
+                        cvt4<FMT>(wb[x][q], a[1], a[3]);
+                        Mma<__half>::run(acc[x][q & 1], a, this->qb[4 * h + q][0],
+                                         this->qb[4 * h + q][1]);
+                    }
             }
-            const int ta = t0 + gid, tb = ta + 8;
-            const bool v0 = ta < n_valid, v1 = tb < n_valid;
-            float fa = qs, fb = qs;
-            if constexpr (FMT == kFmtInt8) {
-                fa *= v0 ? sc[ta] : 0.f;
-                fb *= v1 ? sc[tb] : 0.f;
+            float s[2][4];
+            float sv[2][2];                         // INT8: the V scales of the lane's rows
+            float smax = 0.f;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const int ta = t0 + 16 * x + gid, tb = ta + 8;
+                const bool v0 = ta < n_valid, v1 = tb < n_valid;
+                float fa = qs, fb = qs;
+                sv[x][0] = sv[x][1] = 0.f;
+                if constexpr (FMT == kFmtInt8) {
+                    fa *= v0 ? sc[ta] : 0.f;
+                    fb *= v1 ? sc[tb] : 0.f;
+                    sv[x][0] = v0 ? sc[bs + ta] : 0.f;
+                    sv[x][1] = v1 ? sc[bs + tb] : 0.f;
+                    smax = fmaxf(smax, fmaxf(sv[x][0], sv[x][1]));
+                }
+                s[x][0] = v0 ? (acc[x][0][0] + acc[x][1][0]) * fa : -CUDART_INF_F;
+                s[x][1] = v0 ? (acc[x][0][1] + acc[x][1][1]) * fa : -CUDART_INF_F;
+                s[x][2] = v1 ? (acc[x][0][2] + acc[x][1][2]) * fb : -CUDART_INF_F;
+                s[x][3] = v1 ? (acc[x][0][3] + acc[x][1][3]) * fb : -CUDART_INF_F;
             }
-            float s[1][4];
-            s[0][0] = v0 ? (acc[0][0] + acc[1][0]) * fa : -CUDART_INF_F;
-            s[0][1] = v0 ? (acc[0][1] + acc[1][1]) * fa : -CUDART_INF_F;
-            s[0][2] = v1 ? (acc[0][2] + acc[1][2]) * fb : -CUDART_INF_F;
-            s[0][3] = v1 ? (acc[0][3] + acc[1][3]) * fb : -CUDART_INF_F;
             // -- online softmax, heads 2 tig (j = 0) and 2 tig + 1 (j = 1); INT8:
             // the running largest V scale R moves with the maxima ----------------
-            float sa = 0.f, sb = 0.f;
-            if constexpr (FMT == kFmtInt8) {
-                sa = v0 ? sc[bs + ta] : 0.f;
-                sb = v1 ? sc[bs + tb] : 0.f;
-            }
-            const float smax = fmaxf(sa, sb);
-            float mloc[2] = {fmaxf(s[0][0], s[0][2]), fmaxf(s[0][1], s[0][3])};
+            const float mloc[2] = {fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2])),
+                                   fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]))};
             if (__any_sync(FULL, mloc[0] > this->m_run[0] || mloc[1] > this->m_run[1] ||
                                      (FMT == kFmtInt8 && smax > R))) {
                 float alpha[2];
@@ -1136,36 +1159,41 @@ struct Tc8Policy : TcPolicy<T, D, G, 16, true> {
                 }
                 this->rescale(alpha[0] * rf, alpha[1] * rf);
             }
-            this->template softmax_weights<1>(s);
-            // V scales: P' = P * vscale_t / R
-            if constexpr (FMT == kFmtInt8) {
-                const float wa = sa * Rinv, wb = sb * Rinv;
-                s[0][0] *= wa; s[0][1] *= wa; s[0][2] *= wb; s[0][3] *= wb;
-            }
-            uint32_t bh[2], bl[2];
-            this->template p_operands<Mma<__half>>(s[0], lane, bh, bl);
-            // -- O^T += V_tile^T P'^T: token rows 2 tig, 2 tig + 1, + 8, + 9 ------
-            // (rows past the sequence end read as zero codes: P' is 0 there, but
-            // an E4M3 NaN code would still poison the MMA)
-            uint32_t vw[4][4];
+            this->template softmax_weights<2>(s);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = 2 * tig + (i & 1) + 8 * (i >> 1);
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (t0 + r < n_valid) v = chunk(Vt, r, gid);
-                vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;
-            }
+            for (int x = 0; x < 2; ++x) {
+                // V scales: P' = P * vscale_t / R
+                if constexpr (FMT == kFmtInt8) {
+                    const float wa = sv[x][0] * Rinv, wb = sv[x][1] * Rinv;
+                    s[x][0] *= wa; s[x][1] *= wa; s[x][2] *= wb; s[x][3] *= wb;
+                }
+                uint32_t bh[2], bl[2];
+                this->template p_operands<Mma<__half>>(s[x], lane, bh, bl);
+                // -- O^T += V_tile^T P'^T: token rows 2 tig, 2 tig + 1, + 8, + 9 --
+                // (rows past the sequence end read as zero codes: P' is 0 there,
+                // but an E4M3 NaN code would still poison the MMA)
+                const int tv = t0 + 16 * x;
+                const unsigned char* Vt = Vs + tv * 128;
+                uint32_t vw[4][4];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                // dims 16 gid + 2 mt (+1): bytes 2 mt, 2 mt + 1 of each row's chunk
-                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                const uint32_t x01 = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
-                const uint32_t x23 = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
-                uint32_t a[4];
-                cvt4<FMT>(x01, a[0], a[1]);
-                cvt4<FMT>(x23, a[2], a[3]);
-                Mma<__half>::run(this->oacc[mt], a, bh[0], bh[1]);
-                if constexpr (!Base::kPairHL) Mma<__half>::run(this->oacc[mt], a, bl[0], bl[1]);
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 2 * tig + (i & 1) + 8 * (i >> 1);
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (tv + r < n_valid) v = chunk(Vt, r, gid);
+                    vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;
+                }
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    // dims 16 gid + 2 mt (+1): bytes 2 mt, 2 mt + 1 of each row's chunk
+                    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                    const uint32_t x01 = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
+                    const uint32_t x23 = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
+                    uint32_t a[4];
+                    cvt4<FMT>(x01, a[0], a[1]);
+                    cvt4<FMT>(x23, a[2], a[3]);
+                    Mma<__half>::run(this->oacc[mt], a, bh[0], bh[1]);
+                    if constexpr (!Base::kPairHL) Mma<__half>::run(this->oacc[mt], a, bl[0], bl[1]);
+                }
             }
         }
     }
