@@ -1609,8 +1609,9 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
             if (*abort_flag == 0 && id >= 0 && id < p.num_blocks &&
                 (!second || (id2 >= 0 && id2 < p.num_blocks))) {
                 valid[st] = 1;
-                // the stage's last reads (generic proxy) before the copy's writes
-                fence_proxy_async();
+                // No proxy fence: every read of the stage fed an MMA or FMA that
+                // the warp issued before this point, so the reads are complete;
+                // a policy that writes into a stage fences those writes itself.
                 mbar_arrive_tx(fb, second ? lay.tx_bytes : lay.tx_bytes / UB);
                 const uint32_t dst = smem_u32(ring + (size_t)st * lay.stage_bytes);
                 const uint32_t vdst = dst + (uint32_t)(bsu * D * ELT);
