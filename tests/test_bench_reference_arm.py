@@ -5,7 +5,6 @@ and nothing from ranks other than 0."""
 import json
 
 
-
 def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
     import bench
     monkeypatch.delenv("RANK", raising=False)
