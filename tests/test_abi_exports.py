@@ -4,6 +4,7 @@ declares; host-side argument checks answer without touching a GPU (no GPU)."""
 import ctypes
 import os
 import re
+import shutil
 import subprocess
 
 import pytest
@@ -76,3 +77,30 @@ def test_calls_on_null_pool_are_rejected(lib):
 def test_build_is_sm103a_only():
     from paged_kv_cache_68_gb300 import _build
     assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_header_is_plain_c_and_links_from_c(lib, tmp_path):
+    """A C99 program (pedantic, warnings as errors) that includes the header,
+    takes the address of every declared entry point, links against the
+    library and calls kv_strerror: the boundary is a C ABI, not a C++ one."""
+    from paged_kv_cache_68_gb300 import pagedkv
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include "pagedkv.h"\n#include <stdio.h>\n'
+        "typedef void (*entry)(void);\n"
+        "int main(void) {\n  entry fns[] = {\n"
+        + "".join(f"    (entry)&{n},\n" for n in names)
+        + "  };\n"
+        '  printf("%d %s\\n", (int)(sizeof fns / sizeof fns[0]), kv_strerror(KV_OK));\n'
+        "  return 0;\n}\n")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(pagedkv.library_path())
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.dirname(HEADER), str(src), "-o", str(exe), "-L", libdir,
+                    "-lpagedkv", f"-Wl,-rpath,{libdir}"], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    assert out.split() == [str(len(names)), "ok"]
