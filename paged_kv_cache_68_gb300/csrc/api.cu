@@ -328,6 +328,7 @@ kv_status kv_pool_destroy(kv_pool_t pool) {
 
 kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
                     const int64_t* slot_mapping, int num_tokens, void* stream) {
+    const pagedkv::NvtxRange range("kv_append");
     if (!pool || num_tokens < 0) return KV_EINVAL;
     if (num_tokens == 0) return KV_OK;
     if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new) ||
@@ -339,6 +340,7 @@ kv_status kv_append(kv_pool_t pool, const void* k_new, const void* v_new,
 }
 
 kv_status copy_blocks(kv_pool_t pool, const int32_t* pairs, int num_pairs, void* stream) {
+    const pagedkv::NvtxRange range("copy_blocks");
     if (!pool || num_pairs < 0 || num_pairs > (1 << 30)) return KV_EINVAL;
     if (num_pairs == 0) return KV_OK;
     if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 7u)) return KV_EINVAL;
@@ -362,6 +364,7 @@ static bool device_accessible(const void* p) {
 kv_status kv_swap_blocks(kv_pool_t pool, void* host_k, void* host_v, float* host_k_scales,
                          float* host_v_scales, int num_host_blocks, const int32_t* pairs,
                          int num_pairs, int direction, void* stream) {
+    const pagedkv::NvtxRange range("kv_swap_blocks");
     if (!pool || num_pairs < 0 || num_pairs > (1 << 28) || num_host_blocks < 1) return KV_EINVAL;
     if (direction != KV_SWAP_OUT && direction != KV_SWAP_IN) return KV_EINVAL;
     if (num_pairs == 0) return KV_OK;
@@ -467,6 +470,7 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
                                  const int32_t* seq_lens, int batch, int num_q_heads, float scale,
                                  int num_kv_heads, void* workspace, size_t workspace_bytes,
                                  void* stream) {
+    const pagedkv::NvtxRange range("paged_attention_decode");
     return decode_impl(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
                        num_q_heads, scale, num_kv_heads, workspace, workspace_bytes, nullptr,
                        nullptr, nullptr, 0, nullptr, nullptr, stream);

@@ -147,6 +147,7 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
                                          const int32_t* group_size,
                                          const int32_t* group_shared_blocks, int num_groups,
                                          void* workspace, size_t workspace_bytes, void* stream) {
+    const pagedkv::NvtxRange range("paged_attention_decode_cascade");
     if (num_groups < 0 || num_groups > pagedkv::kMaxGroups) return KV_EINVAL;
     if (num_groups > 0 && (!group_first || !group_size || !group_shared_blocks ||
                            (reinterpret_cast<uintptr_t>(group_first) & 3u) ||

@@ -60,6 +60,7 @@ extern "C" kv_status paged_attention_decode_noalloc(kv_pool_t pool, const void* 
                                                     int max_blocks_per_seq, const int32_t* seq_lens,
                                                     int batch, int num_q_heads, float scale,
                                                     int num_kv_heads, void* stream) {
+    const pagedkv::NvtxRange range("paged_attention_decode_noalloc");
     size_t need = 0;
     kv_status st = paged_attention_workspace_size(pool, batch, num_q_heads, &need);
     if (st != KV_OK) return st;

@@ -7,6 +7,8 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pagedkv.h"
 
 namespace pagedkv {
@@ -65,6 +67,29 @@ namespace pagedkv {
 inline int merge_warps_per_pair(int warps, int pairs) {
     return warps < 2 * pairs ? 0 : (pairs <= 512 ? 4 : 1);
 }
+
+// A named range in the "pagedkv" NVTX domain around one C-ABI call, so a
+// profiler's timeline (Nsight Systems, `ncu --nvtx`) shows each call with the
+// kernels it launched.  Without an attached tool a push or pop tests one
+// function pointer and returns.
+inline nvtxDomainHandle_t nvtx_domain() {
+    static const nvtxDomainHandle_t d = nvtxDomainCreateA("pagedkv");
+    return d;
+}
+class NvtxRange {
+public:
+    explicit NvtxRange(const char* name) {
+        nvtxEventAttributes_t a = {};
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(nvtx_domain(), &a);
+    }
+    ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxGroups = 1024;   // cascade decode: groups per call

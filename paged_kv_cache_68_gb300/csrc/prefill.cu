@@ -99,6 +99,7 @@ kv_status paged_attention_prefill(kv_pool_t pool, const void* q, void* out,
                                   const int32_t* block_tables, int max_blocks_per_seq,
                                   const int32_t* seq_lens, int batch, int num_q_heads,
                                   float scale, int num_kv_heads, void* stream) {
+    const pagedkv::NvtxRange range("paged_attention_prefill");
     if (!pool || batch < 1 || num_q_heads < 1 || num_tokens < 0) return KV_EINVAL;
     if (num_kv_heads != pool->num_kv_heads || num_q_heads % num_kv_heads) return KV_EINVAL;
     const int g = num_q_heads / num_kv_heads;
