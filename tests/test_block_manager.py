@@ -168,3 +168,26 @@ def test_shared_prefix_workload_copy_counts():
     assert w2.info["history_copies"] == 0 and w2.pairs.shape == (12, 2)
     dsts = w2.pairs[:, 1]
     assert len(set(dsts.tolist())) == len(dsts) and not set(dsts) & set(w2.pairs[:, 0])
+
+
+def test_expected_waste_is_under_one_block_and_independent_of_length():
+    """Only a sequence's last block holds unused slots: [S06] "how to choose the
+    block size" puts the expected waste at half a block per request, whatever
+    its length.  Over every length residue the mean is exactly (bs - 1) / 2
+    slots, the same for short and long sequences; growing a sequence token by
+    token keeps it below one block."""
+    for bs in (1, 4, 8, 16, 32):
+        for base in (0, 10 * bs, 1000 * bs):
+            m = BlockManager(num_blocks=4096, block_size=bs)
+            waste = []
+            for i, n in enumerate(range(base + 1, base + bs + 1)):
+                m.allocate_prompt(i, n)
+                waste.append(len(m.table(i)) * bs - n)
+                m.free_seq(i)
+            assert sum(waste) * 2 == (bs - 1) * bs, (bs, base)
+        m = BlockManager(num_blocks=64, block_size=bs)
+        m.allocate_prompt(0, 1)
+        for _ in range(3 * bs):
+            m.append_slot(0)
+            assert 0 <= len(m.table(0)) * bs - m.lens[0] < bs
+        m.check_invariant()

@@ -49,3 +49,19 @@ def test_long_context_block_sizes():
         assert w.block_size == bs and w.k_pool.shape[1] == bs
         assert all(len([x for x in row if x >= 0]) == -(-int(L) // bs)
                    for row, L in zip(w.block_tables, w.seq_lens))
+
+
+def test_kv_bytes_per_token_match_the_pages_model_sizes():
+    """Per token and layer, K + V take 4 KiB for the Llama-3-8B shape (8 KV heads
+    x 128 dims x 2 bytes x 2) and 20 KiB for the OPT-13B shape (40 heads).  Over
+    32 and 40 layers that is 128 KiB per token and 2 MiB per 16-token block
+    ([11868-L24] reference answer 1) and 800 KiB per token and 12.5 MiB per
+    block ([CS349D-L3] exercise 1)."""
+    llama = wl.llama3_8b_gqa(0, batch=2, median=40, hi=100)
+    opt = wl.opt13b_mha(0, batch=2, lo=10, hi=40)
+    for w, layers, per_token, per_block in ((llama, 32, 128 << 10, 2 << 20),
+                                            (opt, 40, 800 << 10, 25 << 19)):
+        row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2
+        assert row * layers == per_token
+        assert row * layers * w.block_size == per_block
+        assert w.block_size == 16
