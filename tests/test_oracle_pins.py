@@ -226,6 +226,50 @@ def test_placement_permutation_invariance(c_oracle, dtype):
         assert np.array_equal(o0, o1), name
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_lse_merge_of_block_pieces_equals_whole(c_oracle, dtype):
+    """Attention over a sequence cut at block boundaries into pieces, each piece
+    attended on its own (a table of just its blocks) and the pieces combined by
+    log-sum-exp weights (the combine of the split decode, [11868-L24] sec. 3.2:
+    partial softmaxes merge exactly through their maxima and sums), equals the
+    attention over the whole sequence.  The per-piece log-sum-exp of the
+    scores is taken here from the gathered K in numpy; the outputs come from
+    the oracles."""
+    w = wl.build_step("lse", 11, [1, 37, 64, 150], dtype=dtype, num_q_heads=8, num_kv_heads=2,
+                      head_dim=32, block_size=8)
+    k, v = w.k_pool.copy(), w.v_pool.copy()
+    np_oracle.append(k, v, w.k_new, w.v_new, w.slot_mapping)
+    group = w.num_q_heads // w.num_kv_heads
+    q = np_oracle.to_f64(w.q, dtype)
+    bs = w.block_size
+    for name, f in _both(c_oracle):
+        whole = f(w.q, k, v, dtype, w.block_tables, w.seq_lens, w.scale, w.num_kv_heads)
+        for b in range(w.batch):
+            L = int(w.seq_lens[b])
+            nb = -(-L // bs)
+            cuts = sorted({0, nb // 3, (2 * nb) // 3, nb})
+            outs, lses = [], []
+            for j0, j1 in zip(cuts[:-1], cuts[1:]):
+                if j1 == j0:
+                    continue
+                row = np.full((1, w.block_tables.shape[1]), -1, np.int32)
+                row[0, :j1 - j0] = w.block_tables[b, j0:j1]
+                n = min(L, j1 * bs) - j0 * bs
+                outs.append(f(w.q[b:b + 1], k, v, dtype, row, np.array([n], np.int32), w.scale,
+                              w.num_kv_heads)[0])
+                K = np_oracle.to_f64(np_oracle.gather_kv(k, row[0], n), dtype)   # [n, Hkv, D]
+                lse = np.empty(w.num_q_heads)
+                for h in range(w.num_q_heads):
+                    sc = w.scale * (K[:, h // group, :] @ q[b, h])
+                    lse[h] = sc.max() + np.log(np.exp(sc - sc.max()).sum())
+                lses.append(lse)
+            lses = np.array(lses)                                    # [pieces, Hq]
+            wts = np.exp(lses - lses.max(axis=0))
+            merged = (wts[:, :, None] * np.array(outs)).sum(axis=0) / wts.sum(axis=0)[:, None]
+            np.testing.assert_allclose(merged, whole[b], rtol=0, atol=1e-12,
+                                       err_msg=f"{name} b={b}")
+
+
 def test_shared_blocks_equal_private_copies(c_oracle):
     """Samples whose tables share refcounted prefix blocks give the same output
     as samples holding private copies of those blocks ([CS349D-L3] sec. 4.1:
