@@ -7,8 +7,8 @@ paged_attention_decode (split + log-sum-exp combine).  Default workload: the
 Llama-3-8B-shaped GQA step (32 query / 8 KV heads, head_dim 128, bf16, block
 size 16, batch 256, lognormal context lengths with median 1024 clipped to
 [16, 8192], blocks scattered over a pool 1.5x the need), inputs resident in
-HBM.  The L2 is flushed (512 MB write) between timed steps, outside the timed
-events.
+HBM.  The L2 is flushed (a 512 MB write, then a 256 MB read, so no dirty
+lines are left) between timed steps, outside the timed events.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 this machine's host cores instead (the reference arm).  Under torchrun every
@@ -38,10 +38,10 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), seq-steps/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_decode_split_llama3_8b_gqa.md")
-PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "paged_decode_split_fp8_llama3_8b_gqa.md")
+# DRAM bytes per launch from ncu captures, keyed by kernel and workload, each
+# with the sha256 of the kernel source the counters were taken on
+TRAFFIC_DATA = os.path.join(ROOT, "profiles", "dram_traffic.json")
 DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "decode_kernel.cuh")
-PREFILL_SUMMARY = os.path.join(ROOT, "profiles", "paged_prefill_chunked_llama3_8b.md")
 PREFILL_SOURCE = os.path.join(ROOT, "paged_kv_cache_68_gb300", "csrc", "prefill_kernel.cuh")
 
 WORKLOAD_TEXT = {
@@ -125,6 +125,23 @@ def make_workload(name: str, seed: int, device, placement: str = "random", batch
     raise ValueError(name)
 
 
+class L2Flush:
+    """Between timed steps: write 512 MB (every line of the 129 MB L2 is
+    replaced), then read 256 MB, so that the lines left in L2 are clean.
+    Without the read, the step would start with ~129 MB of the flush's dirty
+    lines in L2, written back to HBM while the decode streams its K/V -- a
+    cost of the flush, not of the step."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -135,21 +152,18 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(summary=None, source=None):
-    """DRAM bytes per launch of a kernel from its committed ncu summary, if the
-    counters were taken on the current kernel source (else None)."""
-    summary = summary or PROFILE_SUMMARY
-    source = source or DECODE_SOURCE
+def profiled_traffic(key, source):
+    """DRAM bytes (read + write) per launch of the kernel under `key` in the
+    traffic data file, if its counters were taken on the current source of
+    that kernel (else None: the kernel changed since)."""
     try:
-        text = open(summary).read()
+        entry = json.load(open(TRAFFIC_DATA))[key]
         sha = hashlib.sha256(open(source, "rb").read()).hexdigest()
-    except OSError:
+    except (OSError, KeyError, ValueError):
         return None
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9]+)", text)
-    if not m_sha or not m_b or m_sha.group(1) != sha:
+    if entry.get("source_sha256") != sha:
         return None
-    return int(m_b.group(1))
+    return int(entry["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -323,6 +337,59 @@ def unique_bytes_fields(w, world, dec_ms):
             "cow_pairs_per_step": int(w.pairs.shape[0])}
 
 
+def decode_config(args, w, q8, world):
+    """The workload description both arms print (the same keys and values)."""
+    step_bytes = w.step_bytes() if q8 is None else q8.step_bytes(w)
+    kv_bytes = w.kv_bytes() if q8 is None else q8.kv_bytes(w)
+    return {"workload": WORKLOAD_TEXT[args.workload]
+            + ("" if args.batch is None else f" (batch overridden to {args.batch})")
+            + ("" if args.block_size is None else f" (block_size {args.block_size})")
+            + ("" if args.prompt_len is None else f" (prompt_len {args.prompt_len})")
+            + ("" if q8 is None else f", K/V stored as {q8.cache} codes"),
+            "seed": args.seed, "placement": args.placement, "global_batch": w.batch * world,
+            "kv_cache": q8.cache if q8 is not None else w.dtype,
+            "tokens_per_replica": int(w.seq_lens.sum()),
+            "kv_bytes_per_replica": kv_bytes, "step_bytes_per_replica": step_bytes,
+            "l2": "flushed between timed steps (512 MB write, then 256 MB read: no dirty lines "
+                  f"left); K/V read per step {kv_bytes / 1e9:.3f} GB"
+                  + (" > 129 MB L2" if kv_bytes > 129e6 else " (smaller than L2: the flush keeps it cold)"),
+            "parallelism": f"replicas x{world}"}
+
+
+def prefill_config(args, w, world, flops):
+    return {"workload": WORKLOAD_TEXT[args.workload]
+            + ("" if args.batch is None else f" (requests overridden to {args.batch})")
+            + ("" if args.chunk is None else f" (chunk {args.chunk})")
+            + ("" if not args.decodes else f", + {args.decodes} decode requests"),
+            "seed": args.seed, "global_batch": w.batch * world,
+            "query_tokens_per_replica": int(w.info["query_tokens"]),
+            "context_tokens_per_replica": int(w.seq_lens.sum()),
+            "attention_flops_per_replica": flops,
+            "l2": "flushed between timed steps (512 MB write, then 256 MB read: no dirty lines left)",
+            "parallelism": f"replicas x{world}"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(line.split(":", 1) for line in out.splitlines() if ":" in line)
+        name = fields.get("Model name", "").strip()
+        vendor = fields.get("Vendor ID", "").strip()
+        if name:
+            return f"{vendor} {name}".strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 # ----------------------------------------------------------- CPU baseline --
 
 def oracle_sample_step(host_w, seqs, threads, q8=None):
@@ -403,11 +470,11 @@ def time_swap(pool, w, frac, flush, K, dev):
 
     def timed(fn):
         for _ in range(3):
-            flush.zero_()
+            flush()
             fn()
         ms = 0.0
         for _ in range(K):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -493,7 +560,7 @@ def run_ours(args):
                                                    ws, pool.dtype)
         else:
             pool.decode(q, tables, lens, w.scale, out=out, workspace=ws)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     n_pairs = int(w.pairs.shape[0])
     # copy (if pairs), append, decode (split, + merge for long contexts; a cascade decode adds
     # the prefix pass)
@@ -506,7 +573,7 @@ def run_ours(args):
         decode()
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert pool.get_error() == 0, "device error word set during warm-up"
@@ -518,7 +585,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     sampler.begin()
     for i in range(K):
-        flush.zero_()                                   # L2 flush, outside the events
+        flush()                                   # L2 flush, outside the events
         e = ev[i]
         e[0].record()
         pool.copy_blocks(pairs)
@@ -546,7 +613,7 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     for i in range(KE):
-        flush.zero_()
+        flush()
         eve[i][0].record()
         dev_in.copy_(host_in, non_blocking=True)
         step()
@@ -587,9 +654,20 @@ def run_ours(args):
         while passes < 3 or dt < 5.0:                   # a few seconds of CPU work at least
             t, b = oracle_sample_step(host_w, seqs, threads, hq8)
             dt, nb, passes = dt + t, nb + b, passes + 1
+        # the same on one core (a smaller sample of the same step)
+        seqs1 = pick_sample(host_w, 2.0, 1, hq8)
+        dt1, nb1, passes1 = 0.0, 0, 0
+        while passes1 < 2 or dt1 < 3.0:
+            t, b = oracle_sample_step(host_w, seqs1, 1, hq8)
+            dt1, nb1, passes1 = dt1 + t, nb1 + b, passes1 + 1
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "cpu_model": cpu_model(),
                "sample": f"{len(seqs)} of {w.batch} sequences of the same step (copy + append + "
-                         f"attention, fp64 C oracle), {passes} passes, {dt:.1f} s"}
+                         f"attention, fp64 C oracle, threaded over sequences), {passes} passes, "
+                         f"{dt:.1f} s",
+               "single_thread": {"value": round(nb1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                                 "sample": f"{len(seqs1)} of {w.batch} sequences, {passes1} "
+                                           f"passes, {dt1:.1f} s"}}
 
     pool.close()
     if rank != 0:
@@ -600,19 +678,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype if q8 is None else f"{q8.cache} storage, f16 MMA, fp32 softmax",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload]
-                   + ("" if args.batch is None else f" (batch overridden to {args.batch})")
-                   + ("" if args.block_size is None else f" (block_size {args.block_size})")
-                   + ("" if args.prompt_len is None else f" (prompt_len {args.prompt_len})")
-                   + ("" if q8 is None else f", K/V stored as {q8.cache} codes"),
-                   "seed": args.seed, "placement": args.placement, "global_batch": w.batch * world,
-                   "kv_cache": q8.cache if q8 is not None else w.dtype,
-                   "tokens_per_replica": int(w.seq_lens.sum()),
-                   "kv_bytes_per_replica": kv_bytes, "step_bytes_per_replica": step_bytes,
-                   "l2": f"flushed (512 MB write) between timed steps; K/V read per step "
-                         f"{kv_bytes / 1e9:.3f} GB"
-                         + (" > 129 MB L2" if kv_bytes > 129e6 else " (smaller than L2: the flush keeps it cold)"),
-                   "parallelism": f"replicas x{world}"},
+        "config": decode_config(args, w, q8, world),
         "seq_steps_per_s": round(total_seqs / (max_step_ms * 1e-3), 1),
         **unique_bytes_fields(w, world, max_dec_ms),
         "attention_gbs": round(att_bytes * world / (max_dec_ms * 1e-3) / 1e9, 2),
@@ -622,7 +688,9 @@ def run_ours(args):
                                 "paged_decode_split (+ paged_decode_merge) (the whole decode call)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": (profiled_traffic(PROFILE_SUMMARY_FP8 if q8 is not None else None)
+                     "traffic": (profiled_traffic("paged_decode_split/llama3_8b_gqa/"
+                                                  + ("fp8_e4m3" if q8 is not None else "bf16"),
+                                                  DECODE_SOURCE)
                                  if (not cascade and (q8 is None or q8.cache == "fp8_e4m3")
                                      and args.workload == "llama3_8b_gqa"
                                      and args.batch is None and args.seed == 0
@@ -725,9 +793,9 @@ def run_prefill(args):
     def prefill():
         pool.prefill(view["q"], view["cu"], maxq, view["tables"], view["lens"], w.scale, out=out)
 
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         append()
         prefill()
     torch.cuda.synchronize()
@@ -739,7 +807,7 @@ def run_prefill(args):
     torch.cuda.synchronize()
     sampler.begin()
     for i in range(K):
-        flush.zero_()                                   # L2 flush, outside the events
+        flush()                                   # L2 flush, outside the events
         e = ev[i]
         e[0].record()
         append()
@@ -760,7 +828,7 @@ def run_prefill(args):
     barrier()
     torch.cuda.synchronize()
     for i in range(KE):
-        flush.zero_()
+        flush()
         eve[i][0].record()
         dev_in.copy_(host_in, non_blocking=True)
         append()
@@ -800,23 +868,14 @@ def run_prefill(args):
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(max_step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload]
-                   + ("" if args.batch is None else f" (requests overridden to {args.batch})")
-                   + ("" if args.chunk is None else f" (chunk {args.chunk})")
-                   + ("" if not args.decodes else f", + {args.decodes} decode requests"),
-                   "seed": args.seed, "global_batch": w.batch * world,
-                   "query_tokens_per_replica": int(w.info["query_tokens"]),
-                   "context_tokens_per_replica": int(w.seq_lens.sum()),
-                   "attention_flops_per_replica": flops,
-                   "l2": "flushed (512 MB write) between timed steps",
-                   "parallelism": f"replicas x{world}"},
+        "config": prefill_config(args, w, world, flops),
         "query_tokens_per_s": round(qtok / (max_step_ms * 1e-3), 1),
         "attention_tflops": round(total_flops / (max_pf_ms * 1e-3) / 1e12, 2),
         "roofline": {"bound": "tensor",
                      "kernel": "paged_prefill (tcgen05; the whole prefill call, one kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind} (bf16 burst)",
-                     "traffic": (profiled_traffic(PREFILL_SUMMARY, PREFILL_SOURCE)
+                     "traffic": (profiled_traffic("paged_prefill/chunked_prefill/bf16", PREFILL_SOURCE)
                                  if args.batch is None and args.chunk is None and not args.decodes
                                  and args.seed == 0 else None),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
@@ -859,8 +918,11 @@ def run_prefill_reference(args):
         "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload], "seed": args.seed},
+        "data": "synthetic",
+        "config": prefill_config(args, w, int(os.environ.get("WORLD_SIZE", "1")),
+                                 w.attention_flops()),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "cpu_model": cpu_model(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -903,12 +965,9 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload]
-                   + ("" if q8 is None else f", K/V stored as {q8.cache} codes"),
-                   "seed": args.seed, "placement": args.placement,
-                   "kv_cache": q8.cache if q8 is not None else w.dtype},
+        "config": decode_config(args, w, q8, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

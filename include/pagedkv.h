@@ -249,9 +249,13 @@ kv_status paged_attention_decode_launches(kv_pool_t pool, int batch, int num_q_h
  *   1 <= batch <= 4096.
  * workspace: device scratch of at least paged_attention_workspace_size bytes,
  *   16-byte aligned, owned by the caller.  Its contents need no initialisation
- *   and carry nothing the caller must manage between calls (it holds per-call
- *   partial results and self-resetting piece counters tagged with a call
- *   number).  Calls that use the same workspace must not overlap in time.
+ *   and carry nothing the caller must manage between calls: it holds per-call
+ *   partial results and piece counters; every call tags its counters with a
+ *   fresh random 64-bit value and counts a counter of another tag as zero,
+ *   so whatever the memory held before (an earlier call's counters, other
+ *   data) is taken for a live count only if it matches that tag, with
+ *   probability 2^-64.  Calls that use the same workspace must not overlap
+ *   in time.
  * Errors: KV_EINVAL, KV_EUNSUPPORTED, KV_ENOWORKSPACE, KV_ECUDA.
  */
 kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
@@ -358,20 +362,39 @@ kv_status paged_attention_prefill(kv_pool_t pool, const void* q, void* out,
  * that loads the library until the process exits.  Arguments, layouts and
  * results are those of paged_attention_decode.
  *
- * The first call on a device looks up that device's address of the array
- * (once, with the device current); make that first call before any stream
- * capture.  The call allocates nothing.  All calls share the one array: calls
- * whose work overlaps on the GPU (other streams, other host threads) race on
- * it and must be serialised by the caller.  Nothing persists in it between
- * calls.
+ * The calling thread's current device must be the pool's device (KV_EINVAL
+ * otherwise).  The first call on a device looks up that device's address of
+ * the array (once, with the device current); make that first call before any
+ * stream capture.  The call allocates nothing.  All calls share the one
+ * array: calls whose work overlaps on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller.  Nothing
+ * persists in it between calls (each call's counters carry its own random
+ * tag, so an earlier call's contents count as empty).
  * Errors: those of paged_attention_decode, and KV_ENOWORKSPACE when the call
- *   would need more than the 32 MiB maximum (paged_attention_workspace_size
- *   tells the need).
+ *   would need more than the 32 MiB array holds (paged_attention_workspace_size
+ *   tells the need; the piece counters take 16 bytes per sequence x KV head,
+ *   so e.g. 4,096 sequences x 1,024 KV heads need 64 MiB of them).
  */
 kv_status paged_attention_decode_noalloc(kv_pool_t pool, const void* q, void* out,
                                          const int32_t* block_tables, int max_blocks_per_seq,
                                          const int32_t* seq_lens, int batch, int num_q_heads,
                                          float scale, int num_kv_heads, void* stream);
+
+/*
+ * kv_pool_set_wait_limit -- how long one pipeline wait of the decode kernels
+ * (paged_attention_decode, _cascade, _noalloc) may last before the kernel
+ * gives up: it sets KV_DEVERR_TIMEOUT, stops loading and attending, lets the
+ * copies already in flight land (those waits always take the default limit)
+ * and returns; the outputs of that call are then unspecified.  The default
+ * and largest value is 2 s (2e9 ns); larger values are clamped to it.  A
+ * limit of 0 makes every wait that does not find its tile already there give
+ * up, which exercises the failure path with valid inputs.  Host-side only,
+ * takes effect for the calls enqueued after it.  (The source pages have no
+ * counterpart: the kernels' waits are bounded so that a fault cannot hang
+ * the GPU, and this is the knob that tests that bound.)
+ * Errors: KV_EINVAL (null pool).
+ */
+kv_status kv_pool_set_wait_limit(kv_pool_t pool, unsigned long long limit_ns);
 
 /*
  * kv_pool_get_error -- read the pool's device error word (KV_DEVERR_* bits,

@@ -4,7 +4,9 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <chrono>
 #include <cstdio>
+#include <random>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -100,6 +102,24 @@ bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+unsigned long long new_counter_tag() {
+    static std::atomic<unsigned long long> next{0};
+    static const unsigned long long key = [] {
+        std::random_device rd;
+        const unsigned long long t = (unsigned long long)
+            std::chrono::high_resolution_clock::now().time_since_epoch().count();
+        return ((unsigned long long)rd() << 32) ^ rd() ^ (t * 0x9e3779b97f4a7c15ull);
+    }();
+    while (true) {
+        // splitmix64's finaliser: a bijection, so distinct counters give distinct tags
+        unsigned long long z = key + next.fetch_add(1) * 0x9e3779b97f4a7c15ull;
+        z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+        z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+        z ^= z >> 31;
+        if (z != 0 && z != ~0ull) return z;
+    }
+}
+
 kv_status cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where,
                   cudaGetErrorString(e));
@@ -165,8 +185,8 @@ cudaError_t plan_decode(kv_pool& pool, int batch, int num_q_heads, int num_group
     pl.smem_bytes = best_smem;
     pl.num_ctas = pool.num_sms * best_occ;
     size_t off = 0;
-    pl.ws_counter_off = off;
-    off = align_up(off + 8ull * batch * pool.num_kv_heads, 256);
+    pl.ws_counter_off = off;                 // piece counters {tag, count}, one per (b, g)
+    off = align_up(off + 16ull * batch * pool.num_kv_heads, 256);
     // two partial slots per worker (one worker per warp of the grid)
     const size_t workers = (size_t)pl.num_ctas * dec::NCW;
     pl.ws_part_o_off = off;
@@ -431,7 +451,7 @@ static kv_status decode_impl(kv_pool_t pool, const void* q, void* out,
                              int num_kv_heads, void* workspace, size_t workspace_bytes,
                              const int32_t* g_first, const int32_t* g_size,
                              const int32_t* g_blocks, int num_groups, const float* pst_o,
-                             const float* pst_lse, void* stream) {
+                             const float* pst_lse, unsigned long long tag, void* stream) {
     kv_status st = check_decode_shape(pool, batch, num_q_heads);
     if (st != KV_OK) return st;
     if (num_kv_heads != pool->num_kv_heads) return KV_EINVAL;
@@ -449,12 +469,9 @@ static kv_status decode_impl(kv_pool_t pool, const void* q, void* out,
     if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
     if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode(plan)");
     if (workspace_bytes < plan.ws_bytes) return KV_ENOWORKSPACE;
-    // a process-wide call tag for the workspace's piece counters (never 0)
-    static std::atomic<unsigned> next_epoch{1};
-    unsigned epoch = next_epoch.fetch_add(1);
-    if (epoch == 0) epoch = next_epoch.fetch_add(1);
     pagedkv::DecodeCall call{q,     out,   block_tables, max_blocks_per_seq, seq_lens, batch,
-                             num_q_heads, scale, workspace, workspace_bytes, epoch};
+                             num_q_heads, scale, workspace, workspace_bytes};
+    call.tag = tag ? tag : pagedkv::new_counter_tag();
     call.g_first = g_first;
     call.g_size = g_size;
     call.g_blocks = g_blocks;
@@ -473,7 +490,13 @@ kv_status paged_attention_decode(kv_pool_t pool, const void* q, void* out,
     const pagedkv::NvtxRange range("paged_attention_decode");
     return decode_impl(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
                        num_q_heads, scale, num_kv_heads, workspace, workspace_bytes, nullptr,
-                       nullptr, nullptr, 0, nullptr, nullptr, stream);
+                       nullptr, nullptr, 0, nullptr, nullptr, 0, stream);
+}
+
+kv_status kv_pool_set_wait_limit(kv_pool_t pool, unsigned long long limit_ns) {
+    if (!pool) return KV_EINVAL;
+    pool->wait_ns = limit_ns < pagedkv::kWaitLimitNs ? limit_ns : pagedkv::kWaitLimitNs;
+    return KV_OK;
 }
 
 kv_status kv_pool_get_error(kv_pool_t pool, int* device_error_bits) {
@@ -519,7 +542,17 @@ kv_status decode_after_prefix(kv_pool* pool, const void* q, void* out, const int
                               const float* pst_lse, cudaStream_t stream) {
     return decode_impl(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
                        num_q_heads, scale, pool->num_kv_heads, workspace, plain_ws_bytes, g_first,
-                       g_size, g_blocks, num_groups, pst_o, pst_lse, stream);
+                       g_size, g_blocks, num_groups, pst_o, pst_lse, 0, stream);
+}
+
+kv_status decode_with_workspace(kv_pool* pool, const void* q, void* out,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                                int num_kv_heads, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    return decode_impl(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                       num_q_heads, scale, num_kv_heads, workspace, workspace_bytes, nullptr,
+                       nullptr, nullptr, 0, nullptr, nullptr, 0, stream);
 }
 
 }  // namespace pagedkv

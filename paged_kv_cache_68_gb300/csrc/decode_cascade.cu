@@ -30,6 +30,18 @@ struct PrefixPlan {
     size_t off_pst_o, off_pst_lse, off_ctr, off_part_o, off_part_lse, end;
 };
 
+// The split kernel's part at the start of a cascade workspace: as large as
+// both its plans need (with and without the groups' shared-memory tables;
+// the grids can differ), given the plain plan's need in *bytes.
+kv_status split_part(kv_pool* pool, int batch, int num_q_heads, int num_groups, size_t* bytes) {
+    DecodePlan dp;
+    cudaError_t e = plan_decode(*pool, batch, num_q_heads, num_groups, &dp);
+    if (e == cudaErrorNotSupported) return KV_EUNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode_cascade(plan)");
+    if (dp.ws_bytes > *bytes) *bytes = dp.ws_bytes;
+    return KV_OK;
+}
+
 bool cascade_shape(const kv_pool& pool, int group) {
     return pool.elem_bytes == 2 && pool.head_dim == 128 && (group == 4 || group == 8) &&
            (pool.block_size == 16 || pool.block_size == 32) && pool.has_h2_maps;
@@ -106,7 +118,7 @@ cudaError_t plan_prefix(const kv_pool& pool, int batch, int num_q_heads, int num
     size_t off = align_up(base, 256);
     pp->off_pst_o = off;     off = align_up(off + 4ull * batch * num_q_heads * D, 256);
     pp->off_pst_lse = off;   off = align_up(off + 4ull * batch * num_q_heads, 256);
-    pp->off_ctr = off;       off = align_up(off + 8ull * batch * pool.num_kv_heads, 256);
+    pp->off_ctr = off;       off = align_up(off + 16ull * batch * pool.num_kv_heads, 256);
     pp->off_part_o = off;    off = align_up(off + 4ull * pp->num_ctas * 2 * dec::kRows * D, 256);
     pp->off_part_lse = off;  off = align_up(off + 4ull * pp->num_ctas * 2 * dec::kRows, 256);
     pp->end = off;
@@ -129,6 +141,8 @@ kv_status paged_attention_cascade_workspace_size(kv_pool_t pool, int batch, int 
         *bytes = plain;
         return KV_OK;
     }
+    st = pagedkv::split_part(pool, batch, num_q_heads, num_groups, &plain);
+    if (st != KV_OK) return st;
     pagedkv::PrefixPlan pp;
     cudaError_t e = pagedkv::plan_prefix(*pool, batch, num_q_heads, num_groups, plain, &pp);
     if (e == cudaErrorNotSupported) {
@@ -159,27 +173,28 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
         return KV_EINVAL;
     const int G = num_q_heads / num_kv_heads;
     if (num_groups == 0 || !pagedkv::cascade_shape(*pool, G))
-        return paged_attention_decode(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
-                                      batch, num_q_heads, scale, num_kv_heads, workspace,
-                                      workspace_bytes, stream);
+        return pagedkv::decode_with_workspace(pool, q, out, block_tables, max_blocks_per_seq,
+                                              seq_lens, batch, num_q_heads, scale, num_kv_heads,
+                                              workspace, workspace_bytes,
+                                              static_cast<cudaStream_t>(stream));
     size_t plain = 0;
     kv_status st = paged_attention_workspace_size(pool, batch, num_q_heads, &plain);
+    if (st != KV_OK) return st;
+    st = pagedkv::split_part(pool, batch, num_q_heads, num_groups, &plain);
     if (st != KV_OK) return st;
     pagedkv::PrefixPlan pp;
     cudaError_t e = pagedkv::plan_prefix(*pool, batch, num_q_heads, num_groups, plain, &pp);
     if (e == cudaErrorNotSupported)
-        return paged_attention_decode(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
-                                      batch, num_q_heads, scale, num_kv_heads, workspace,
-                                      workspace_bytes, stream);
+        return pagedkv::decode_with_workspace(pool, q, out, block_tables, max_blocks_per_seq,
+                                              seq_lens, batch, num_q_heads, scale, num_kv_heads,
+                                              workspace, workspace_bytes,
+                                              static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_cascade(plan)");
     if (!workspace || workspace_bytes < pp.end) return KV_ENOWORKSPACE;
     // the plain decode checks the remaining arguments before anything is enqueued
     if (!q || !out || !block_tables || !seq_lens) return KV_EINVAL;
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    static std::atomic<unsigned> next_epoch{1u << 31};
-    unsigned epoch = next_epoch.fetch_add(1);
-    if (epoch == 0) epoch = next_epoch.fetch_add(1);
     pagedkv::dec::PParams p;
     p.q = q;
     p.block_tables = block_tables;
@@ -191,6 +206,7 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
     p.pst_o = reinterpret_cast<float*>(ws + pp.off_pst_o);
     p.pst_lse = reinterpret_cast<float*>(ws + pp.off_pst_lse);
     p.counters = reinterpret_cast<unsigned long long*>(ws + pp.off_ctr);
+    p.tag = pagedkv::new_counter_tag();
     p.part_o = reinterpret_cast<float*>(ws + pp.off_part_o);
     p.part_lse = reinterpret_cast<float*>(ws + pp.off_part_lse);
     p.num_groups = num_groups;
@@ -203,7 +219,7 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
     p.stages = pp.stages;
     p.num_ctas = pp.num_ctas;
     p.qscale = scale * 1.4426950408889634f;
-    p.epoch = epoch;
+    p.wait_ns = pool->wait_ns;
     // argument checks of the second pass first, so nothing is enqueued on error
     if (batch < 1 || batch > pagedkv::kMaxBatch || max_blocks_per_seq < 1 ||
         (long long)batch * max_blocks_per_seq * num_kv_heads >= (1ll << 31) ||

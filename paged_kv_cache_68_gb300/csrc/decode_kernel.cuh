@@ -21,8 +21,9 @@
 // the warp and written to `out`; a piece cut by a range boundary is written
 // as a partial (normalised o, log2-sum-exp) to one of two workspace slots of
 // its warp -- slot 0 for the warp's first piece, slot 1 for its last -- and
-// counted in an epoch-tagged per-(b, g) counter; the warp that completes the
-// count merges the partials by log-sum-exp (no second kernel).
+// counted in a per-(b, g) counter tagged with a random per-call value (a
+// counter of another tag counts as zero); the warp that completes the count
+// merges the partials by log-sum-exp (no second kernel).
 //
 // Each warp loads its own units: it owns S / NCW stages of the CTA's
 // shared-memory ring (one full mbarrier each), looks the block ids of its
@@ -71,7 +72,8 @@ struct Params {
     const int32_t* block_tables;
     const int32_t* seq_lens;
     int* err;
-    unsigned long long* counters;  // [batch][num_kv_heads]: (epoch << 32) | pieces done
+    unsigned long long* counters;  // [batch][num_kv_heads][2]: {tag, pieces done}
+    unsigned long long tag;        // this call's random counter tag
     float* part_o;         // [num_ctas][2][G][D]
     float* part_lse;       // [num_ctas][2][G]
     int max_blocks;
@@ -83,7 +85,7 @@ struct Params {
     int stages;
     int num_ctas;
     float qscale;          // scale * log2(e)
-    unsigned epoch;        // nonzero tag of this call (stale counters read as zero)
+    unsigned long long wait_ns;   // limit of one wait for a tile (the pool's setting)
     // Cascade decode (num_groups > 0): the groups of sequences sharing leading
     // blocks, and the shared-prefix pass's states for their members; this pass
     // then covers only each member's remaining blocks.
@@ -182,22 +184,39 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Whether the phase of `bar` with `parity` has completed, without waiting
+// (try_wait may wait for a while before it answers no; test_wait does not).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase of `bar` with `parity` to complete; give up after
-// kWaitLimitNs and return false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// `limit_ns` nanoseconds and return false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
-// mbar_wait with suspended (not spinning) retries; same limit and result.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+// mbar_wait with suspended (not spinning) retries; same limit and result.  A
+// retry is never suspended for longer than the limit itself, and a limit of
+// 0 gives up as soon as the phase is found incomplete.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                unsigned long long limit_ns = kWaitLimitNs) {
+    if (limit_ns == 0) return mbar_test(bar, parity);
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_for(bar, parity, 200000u)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+    const uint32_t hint = limit_ns < 200000ull ? (uint32_t)limit_ns : 200000u;
+    while (!mbar_try_for(bar, parity, hint)) {
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -458,6 +477,45 @@ __host__ __device__ __forceinline__ int unit_chunk(int U, int num_ctas) {
     return c < kMinChunk ? kMinChunk : c;
 }
 
+// How the split kernel cuts the units into one range per warp.  A piece of a
+// (b, g) costs a warp more than its units -- loading the query rows,
+// finishing the softmax, writing the result -- so the ranges are equal in
+// cost, not in units: each (b, g) segment s (s = b H + g, its nb units
+// starting at unit first) counts kPieceCost units more, placed before its
+// first unit, and unit u of segment s sits at cost u + kPieceCost (s + 1).
+// Warp c's range is the units whose cost falls in [c chunk, (c + 1) chunk).
+constexpr int kPieceCost = 2;
+struct WorkCut {
+    const int* prefix;     // [B + 1] units of KV head 0 before each sequence
+    int B, H, chunk;
+    __host__ __device__ __forceinline__ WorkCut(const int* pre, int B_, int H_, int W)
+        : prefix(pre), B(B_), H(H_) {
+        chunk = unit_chunk(pre[B_] * H_ + kPieceCost * B_ * H_, W);
+    }
+    // the range holding unit u of segment s
+    __host__ __device__ __forceinline__ int range_of(int u, int s) const {
+        return (u + kPieceCost * (s + 1)) / chunk;
+    }
+    // the first unit of range c (the total U when the range is empty at the end)
+    __host__ __device__ __forceinline__ int start_unit(int c) const {
+        const long long x = (long long)c * chunk;          // cost position
+        const long long total = (long long)prefix[B] * H + (long long)kPieceCost * B * H;
+        if (x >= total) return prefix[B] * H;
+        // the sequence b whose cost interval holds x: prefix[b] H + kPieceCost H b
+        int lo = 0, hi = B;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long long)prefix[mid] * H + (long long)kPieceCost * H * mid <= x) lo = mid; else hi = mid;
+        }
+        const int nb = prefix[lo + 1] - prefix[lo];
+        const long long rel = x - ((long long)prefix[lo] * H + (long long)kPieceCost * H * lo);
+        const int g = (int)(rel / (nb + kPieceCost));
+        const int o = (int)(rel - (long long)g * (nb + kPieceCost));
+        // a position in a segment's extra cost starts the range at its first unit
+        return prefix[lo] * H + g * nb + (o > kPieceCost ? o - kPieceCost : 0);
+    }
+};
+
 // ------------------------------------------------------- compute policies --
 // Both policies keep one warp's running softmax state for one (b, g) piece and
 // expose: begin (load the group's query rows), block (fold one KV block in),
@@ -682,7 +740,9 @@ struct TcPolicy {
     static constexpr bool kSwizzled = true;
     // 16-bit tiles come by the 4-D maps: one copy per block for both halves
     static constexpr bool kH2 = sizeof(T) == 2 && D == 128;
-    static constexpr int kMinBlocks = 4;
+    // (the ring of a head_dim-128 16-bit tile allows three CTAs per SM at
+    // most, so the register cap is that of three)
+    static constexpr int kMinBlocks = 3;
     static constexpr int kKvBytes = sizeof(T);
     static constexpr int kScaleBytes = 0;
     static constexpr int kUnitBlocks = 1;  // pool blocks per work unit
@@ -1220,21 +1280,32 @@ struct Tc8Policy2 : Tc8Policy<T, D, G, FMT> {
 // ---------------------------------------------- cross-range partial merge --
 // Pieces of one (b, g) cut across work ranges (a warp's in the split kernel,
 // a CTA's in the prefix pass): range c holds its piece in slot (c, 0) when
-// the piece is its first, else (c, 1).  The piece counter is tagged with the
-// call's epoch, so a value left by an earlier call (or never written) counts
-// as zero; the worker that completes the count resets it.
-__device__ __forceinline__ int count_piece(unsigned long long* ctr, unsigned epoch, int pieces) {
-    const unsigned long long tag = (unsigned long long)epoch << 32;
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
+// the piece is its first, else (c, 1).  Each cut piece is counted in the
+// (b, g)'s 16-byte counter {tag, count}: `tag` is a 64-bit value drawn at
+// random for every call, and a counter whose tag is not the call's counts as
+// zero -- so the workspace needs no clearing: a stale counter of an earlier
+// call has that call's tag, and leftover data holds the call's tag only with
+// probability 2^-64.  Counting is a 128-bit compare-and-swap; the worker
+// whose count completes the set merges.
+__device__ __forceinline__ void cas128(unsigned long long* p, unsigned long long& lo,
+                                       unsigned long long& hi, unsigned long long nlo,
+                                       unsigned long long nhi) {
+    asm volatile(
+        "{ .reg .b128 d, b, c; mov.b128 b, {%0, %1}; mov.b128 c, {%2, %3};"
+        " atom.relaxed.gpu.global.cas.b128 d, [%4], b, c; mov.b128 {%0, %1}, d; }"
+        : "+l"(lo), "+l"(hi)
+        : "l"(nlo), "l"(nhi), "l"(p)
+        : "memory");
+}
+__device__ __forceinline__ bool count_piece(unsigned long long* ctr, unsigned long long tag,
+                                            int pieces) {
+    unsigned long long lo = tag, hi = 0;           // a first guess: this call's, none counted
     while (true) {
-        next = ((old >> 32) == epoch ? old : tag) + 1;
-        const unsigned long long seen = atomicCAS(ctr, old, next);
-        if (seen == old) break;
-        old = seen;
+        const unsigned long long elo = lo, ehi = hi;
+        const unsigned long long next = (lo == tag ? hi : 0ull) + 1ull;
+        cas128(ctr, lo, hi, tag, next);            // lo, hi: the value found
+        if (lo == elo && hi == ehi) return next == (unsigned long long)pieces;
     }
-    const int done = (int)(next & 0xffffffffu);
-    if (done == pieces) atomicExch(ctr, tag);          // ready for a replay of this call
-    return done == pieces;
 }
 
 // Fold one normalised state (log2-sum-exp l, output o[0..N)) into a running
@@ -1534,9 +1605,9 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
     // another of its CTA from here on.
     const int U = prefix[B] * H;
     const int worker = blockIdx.x * NCW + warp;
-    const int chunk = unit_chunk(U, p.num_ctas * NCW);
-    const int start = worker * chunk;
-    const int end = min(U, start + chunk);
+    const WorkCut cut(prefix, B, H, p.num_ctas * NCW);
+    const int start = cut.start_unit(worker);
+    const int end = cut.start_unit(worker + 1);
     if (start >= end) return;
 
     // ------------------------------------------------------ the warp's work --
@@ -1580,6 +1651,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         }
     };
     int nx = 0;                                    // issues made (= unit nx)
+    int na = 0;                                    // lane 0: issues that reached the barrier
     int ib = 0;                                    // first issue of the fetched batch
     int is = w;                                    // stage of issue nx
     // lane l holds issue ib + l and, one batch ahead (its table loads in
@@ -1603,11 +1675,14 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         ++nx;
         is += NCW;
         if (is >= S) is -= S;
-        if (lane == 0) {
+        // After an abort a stage's barrier is not touched again: its last
+        // phase may still be waiting for bytes, and an arrival on it would
+        // be one too many.  The issues before that are drained at the end.
+        if (lane == 0 && *abort_flag == 0) {
             const uint32_t fb = smem_u32(&full[st]);
             const bool second = UB == 2 && id2 != -2;   // the unit's second block
-            if (*abort_flag == 0 && id >= 0 && id < p.num_blocks &&
-                (!second || (id2 >= 0 && id2 < p.num_blocks))) {
+            ++na;
+            if (id >= 0 && id < p.num_blocks && (!second || (id2 >= 0 && id2 < p.num_blocks))) {
                 valid[st] = 1;
                 // No proxy fence: every read of the stage fed an MMA or FMA that
                 // the warp issued before this point, so the reads are complete;
@@ -1653,7 +1728,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                 }
             } else {
                 valid[st] = 0;
-                if (*abort_flag == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
                 mbar_arrive(fb);
             }
         }
@@ -1693,7 +1768,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                 cpar ^= 1;
             }
             bool ok = *abort_flag == 0;
-            if (ok && !mbar_wait_sleep(smem_u32(&full[s]), par)) {
+            if (ok && !mbar_wait_sleep(smem_u32(&full[s]), par, p.wait_ns)) {
                 *abort_flag = 1;
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
                 ok = false;
@@ -1733,15 +1808,16 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
                 // merge_wpp > 0 the partials wait for paged_decode_merge.)
                 __threadfence();
                 __syncwarp();
-                const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
+                const int c0 = cut.range_of(seg_start, b * H + g);
+                const int c1 = cut.range_of(seg_start + nb - 1, b * H + g);
                 int last = 0;
                 if (lane == 0)
-                    last = count_piece(p.counters + (size_t)b * H + g, p.epoch, c1 - c0 + 1);
+                    last = count_piece(p.counters + 2 * ((size_t)b * H + g), p.tag, c1 - c0 + 1);
                 if (__shfl_sync(FULL, last, 0)) {
                     __threadfence();
                     T* ob = obase + head0 * D;
                     merge_cut<G, D>(p.part_o, p.part_lse, c0, c1,
-                                    seg_start == c0 * chunk ? 0 : 1, po.pst_o, po.pst_lse, lane,
+                                    seg_start == cut.start_unit(c0) ? 0 : 1, po.pst_o, po.pst_lse, lane,
                                     [&](int r, int d0, const float* v, float) {
 #pragma unroll
                                         for (int k = 0; k < merge_epl<G, D>(); ++k)
@@ -1753,11 +1829,16 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         u = piece_end;
     }
     // Drain: no copy may still be landing in shared memory at exit (after a
-    // timeout the waits above were skipped).  The last per_warp issues hold
-    // distinct stages; a phase already waited on passes at once.
+    // timeout the waits above were skipped).  The issues that reached a
+    // barrier are the first na; their last per_warp hold distinct stages,
+    // each with at most that one phase outstanding (a stage is refilled only
+    // after its previous phase was waited on), and a phase already waited on
+    // passes at once.  These waits take the full limit whatever the pool's
+    // setting, so every copy in flight lands before the CTA exits.
     if (lane == 0)
-        for (int i = max(0, nx - per_warp); i < nx; ++i) {
-            if (!mbar_wait_sleep(smem_u32(&full[w + NCW * (i % per_warp)]), (i / per_warp) & 1))
+        for (int i = max(0, na - per_warp); i < na; ++i) {
+            if (!mbar_wait_sleep(smem_u32(&full[w + NCW * (i % per_warp)]), (i / per_warp) & 1,
+                                 kWaitLimitNs))
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
         }
 }
@@ -1828,8 +1909,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
     pdl_wait();                                    // the split kernel's partials are visible
     unit_prefix(p, smem, lay, bsu, cascade, false);
     __syncthreads();
-    const int U = prefix[B] * H;
-    const int chunk = unit_chunk(U, p.num_ctas * NCW);
+    const WorkCut cut(prefix, B, H, p.num_ctas * NCW);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     T* obase = static_cast<T*>(p.out);
     auto store = [&](T* ob, int r, int d0, const float* v) {
@@ -1842,9 +1922,9 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
             const int nb = prefix[b + 1] - prefix[b];
             if (nb == 0) continue;
             const int seg_start = prefix[b] * H + g * nb;
-            const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
+            const int c0 = cut.range_of(seg_start, pair), c1 = cut.range_of(seg_start + nb - 1, pair);
             if (c0 == c1) continue;                // one warp's: written by the split kernel
-            const int slot0 = seg_start == c0 * chunk ? 0 : 1;
+            const int slot0 = seg_start == cut.start_unit(c0) ? 0 : 1;
             const int per = (c1 - c0 + NCW) / NCW;
             const int lo = c0 + warp * per, hi = min(c1, lo + per - 1);
 #pragma unroll
@@ -1898,12 +1978,12 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
         const int nb = prefix[b + 1] - prefix[b];
         if (nb == 0) continue;
         const int seg_start = prefix[b] * H + g * nb;
-        const int c0 = seg_start / chunk, c1 = (seg_start + nb - 1) / chunk;
+        const int c0 = cut.range_of(seg_start, pair), c1 = cut.range_of(seg_start + nb - 1, pair);
         if (c0 == c1) continue;                    // one warp's: written by the split kernel
         const size_t head0 = (size_t)b * p.num_q_heads + (size_t)g * G;
         const bool pst = cascade && skip_s[b] > 0;
         T* ob = obase + head0 * D;
-        merge_slots<G, D, 4>(p.part_o, p.part_lse, c0, c1, seg_start == c0 * chunk ? 0 : 1,
+        merge_slots<G, D, 4>(p.part_o, p.part_lse, c0, c1, seg_start == cut.start_unit(c0) ? 0 : 1,
                              pst ? p.pst_o + head0 * D : nullptr, pst ? p.pst_lse + head0 : nullptr,
                              lane, 0, 1, [&](int r, int d0, const float* v, float) {
                                  store(ob, r, d0, v);
@@ -1927,6 +2007,7 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.err = pool.d_err;
     unsigned char* ws = static_cast<unsigned char*>(call.workspace);
     p.counters = reinterpret_cast<unsigned long long*>(ws + plan.ws_counter_off);
+    p.tag = call.tag;
     p.part_o = reinterpret_cast<float*>(ws + plan.ws_part_o_off);
     p.part_lse = reinterpret_cast<float*>(ws + plan.ws_part_lse_off);
     p.max_blocks = call.max_blocks;
@@ -1938,7 +2019,7 @@ cudaError_t launch_typed(const kv_pool& pool, const DecodeCall& call, const Deco
     p.stages = plan.stages;
     p.num_ctas = plan.num_ctas;
     p.qscale = call.scale * 1.4426950408889634f;
-    p.epoch = call.epoch;
+    p.wait_ns = pool.wait_ns;
     p.g_first = call.g_first;
     p.g_size = call.g_size;
     p.g_blocks = call.g_blocks;

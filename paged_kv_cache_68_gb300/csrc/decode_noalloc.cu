@@ -16,10 +16,13 @@
 // per device, with that device current, on the first call made on it, and
 // cached.  That first call on a device should come before any stream capture.
 //
-// The kernels keep no state in the scratch between calls: every call writes
-// what it later reads, so nothing needs clearing.  All calls share the one
+// The kernels keep no state in the scratch between calls: each call tags its
+// piece counters with a fresh random 64-bit value (a counter of another tag
+// counts as zero), and every partial result is written before it is read,
+// so what an earlier call of another shape left there does not matter.  All calls share the one
 // array, so calls whose work overlaps on the GPU (two streams, or two host
-// threads) race on it and must be serialised by the caller.
+// threads) race on it and must be serialised by the caller.  The calling
+// thread's current device must be the pool's (KV_EINVAL otherwise).
 //
 // This file calls no cudaMalloc, cudaFree or allocating library routine.
 #include <mutex>
@@ -36,16 +39,14 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on the current device (set up once).
-cudaError_t scratch_for_current_device(void** out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+// Device address of g_decode_scratch on device `dev`, which must be the
+// current device (set up once per device).
+cudaError_t scratch_for_device(int dev, void** out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (g_scratch_addr[dev] == nullptr) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
     }
@@ -61,12 +62,20 @@ extern "C" kv_status paged_attention_decode_noalloc(kv_pool_t pool, const void* 
                                                     int batch, int num_q_heads, float scale,
                                                     int num_kv_heads, void* stream) {
     const pagedkv::NvtxRange range("paged_attention_decode_noalloc");
+    if (!pool) return KV_EINVAL;
+    // the scratch, like the pool's tensor maps, must be the pool's device's
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_noalloc");
+    if (dev != pool->device) return KV_EINVAL;
     size_t need = 0;
     kv_status st = paged_attention_workspace_size(pool, batch, num_q_heads, &need);
     if (st != KV_OK) return st;
     if (need > kScratchBytes) return KV_ENOWORKSPACE;     // beyond the static maximum
     void* scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != cudaSuccess) return KV_ECUDA;
-    return paged_attention_decode(pool, q, out, block_tables, max_blocks_per_seq, seq_lens, batch,
-                                  num_q_heads, scale, num_kv_heads, scratch, kScratchBytes, stream);
+    e = scratch_for_device(dev, &scratch);
+    if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_noalloc(scratch)");
+    return pagedkv::decode_with_workspace(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
+                                          batch, num_q_heads, scale, num_kv_heads, scratch,
+                                          kScratchBytes, static_cast<cudaStream_t>(stream));
 }

@@ -19,8 +19,8 @@
 // The frame is the split kernel's: a persistent grid cut into equal unit
 // ranges, one TMA producer warp feeding a ring of 128-byte-swizzled tiles,
 // four consumer warps (unit k to stage k % S and warp k % 4), a per-piece warp
-// merge, and epoch-tagged counters so the CTA that finishes the last piece of
-// a (group, sub-group, head) segment merges the pieces cut across CTAs.
+// merge, and tagged piece counters so the CTA that finishes the last piece
+// of a (group, sub-group, head) segment merges the pieces cut across CTAs.
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -40,7 +40,9 @@ struct PParams {
     int* err;
     float* pst_o;                  // out [batch][num_q_heads][D], members of used groups
     float* pst_lse;                // out [batch][num_q_heads]
-    unsigned long long* counters;  // [batch][num_kv_heads], by a sub-group's first member
+    unsigned long long* counters;  // [batch][num_kv_heads][2], by a sub-group's first
+                                   // member: {tag, pieces done}
+    unsigned long long tag;        // this call's random counter tag
     float* part_o;                 // [num_ctas][2][kRows][D]
     float* part_lse;               // [num_ctas][2][kRows]
     int num_groups;
@@ -53,7 +55,7 @@ struct PParams {
     int stages;
     int num_ctas;
     float qscale;
-    unsigned epoch;
+    unsigned long long wait_ns;    // limit of one pipeline wait (the pool's setting)
 };
 
 struct PLayout {
@@ -435,16 +437,22 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
             for (int i = 0; i < n; ++i, ++k) {
                 const int id = __shfl_sync(FULL, id_cur, i);
                 const int gg = __shfl_sync(FULL, g_cur, i);
+                int stop = 0;
                 if (lane == 0) {
                     const int s = k % S, ph = k / S;
                     bool ok = *abort_flag == 0;
-                    if (ok && ph > 0 && !mbar_wait_sleep(smem_u32(&empty[s]), (ph - 1) & 1)) {
+                    if (ok && ph > 0 &&
+                        !mbar_wait_sleep(smem_u32(&empty[s]), (ph - 1) & 1, p.wait_ns)) {
                         *abort_flag = 1;
                         atomicOr(p.err, KV_DEVERR_TIMEOUT);
                         ok = false;
                     }
                     const uint32_t fb = smem_u32(&full[s]);
-                    if (ok && id >= 0 && id < p.num_blocks) {
+                    // after an abort no barrier is touched again (a full
+                    // stage's last phase may still be waiting for bytes)
+                    stop = !ok;
+                    if (stop) {
+                    } else if (id >= 0 && id < p.num_blocks) {
                         valid[s] = 1;
                         mbar_arrive_tx(fb, lay.stage_bytes);
                         const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
@@ -453,18 +461,23 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                         tma_load_4d(dst + lay.stage_bytes / 2, &tmap_v, 0, id * BSC, 0, gg, fb);
                     } else {
                         valid[s] = 0;
-                        if (ok) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                        atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
                         mbar_arrive(fb);
                     }
                 }
+                if (__shfl_sync(FULL, stop, 0)) break;
             }
             __syncwarp();
+            if (k < base + n - start) break;      // stopped early (abort)
             id_cur = id_nxt;
             g_cur = g_nxt;
         }
+        // Drain (full limit whatever the pool's setting): the issues that
+        // reached a barrier are the first k, each stage with at most its last
+        // phase outstanding (a stage is refilled only after it was released).
         if (lane == 0)
             for (int kk = max(0, k - S); kk < k; ++kk)
-                if (!mbar_wait_sleep(smem_u32(&full[kk % S]), (kk / S) & 1))
+                if (!mbar_wait_sleep(smem_u32(&full[kk % S]), (kk / S) & 1, kWaitLimitNs))
                     atomicOr(p.err, KV_DEVERR_TIMEOUT);
         return;
     }
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
         for (int uu = first; uu < piece_end; uu += NCW) {
             const int kk = uu - start, s = kk % S;
             bool ok = *abort_flag == 0;
-            if (ok && !mbar_wait_sleep(smem_u32(&full[s]), (kk / S) & 1)) {
+            if (ok && !mbar_wait_sleep(smem_u32(&full[s]), (kk / S) & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
                 ok = false;
@@ -523,7 +536,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                 const int c0 = seg_start / chunk, c1 = (seg_start + P - 1) / chunk;
                 int last = 0;
                 if (lane == 0)
-                    last = count_piece(p.counters + (size_t)m0 * H + g, p.epoch, c1 - c0 + 1);
+                    last = count_piece(p.counters + 2 * ((size_t)m0 * H + g), p.tag, c1 - c0 + 1);
                 if (__shfl_sync(FULL, last, 0)) {
                     __threadfence();
                     merge_prefix_partials<D, G>(p, seg_start, chunk, c0, c1, rows, m0, g, lane);

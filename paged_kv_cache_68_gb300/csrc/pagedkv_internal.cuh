@@ -12,6 +12,11 @@
 #include "pagedkv.h"
 
 namespace pagedkv {
+// Bounded waits: a pipeline wait gives up after this many nanoseconds (by
+// default; kv_pool_set_wait_limit lowers it for the decode kernels), sets
+// KV_DEVERR_TIMEOUT and lets the kernel finish without the missing data.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
 // Launch plan of one decode: grid size, ring depth, shared memory, workspace.
 struct DecodePlan {
     int group;
@@ -49,6 +54,8 @@ struct kv_pool {
                                 // one after the other, in shared memory
     int device;
     int num_sms;
+    // limit of one pipeline wait in the decode kernels (kv_pool_set_wait_limit)
+    unsigned long long wait_ns = pagedkv::kWaitLimitNs;
     // last decode plan, keyed by (batch, num_q_heads)
     std::mutex plan_mu;
     int plan_batch = -1;
@@ -129,9 +136,18 @@ kv_status decode_after_prefix(kv_pool* pool, const void* q, void* out, const int
                               const int32_t* g_blocks, int num_groups, const float* pst_o,
                               const float* pst_lse, cudaStream_t stream);
 
-// Bounded waits: a pipeline wait gives up after this many nanoseconds, sets
-// KV_DEVERR_TIMEOUT and lets the kernel finish without the missing data.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// paged_attention_decode without its NVTX range (for the entry points built
+// on it, which open their own).
+kv_status decode_with_workspace(kv_pool* pool, const void* q, void* out,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                                int num_kv_heads, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+// A fresh random 64-bit tag for one call's piece counters (never 0): a
+// process-wide counter through the splitmix64 finaliser, keyed once per
+// process from the clock and a random device.
+unsigned long long new_counter_tag();
 
 cudaError_t launch_append(const kv_pool& pool, const void* k_new, const void* v_new,
                           const int64_t* slots, int num_tokens, cudaStream_t stream);
@@ -155,7 +171,7 @@ struct DecodeCall {
     float scale;
     void* workspace;
     size_t workspace_bytes;
-    unsigned epoch;        // nonzero, distinct for consecutive calls
+    unsigned long long tag = 0;      // random per-call tag of the piece counters
     // cascade decode: the groups and the shared-prefix pass's states
     const int32_t* g_first = nullptr;
     const int32_t* g_size = nullptr;

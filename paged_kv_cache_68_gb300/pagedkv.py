@@ -81,6 +81,7 @@ def load(build: bool = True) -> ctypes.CDLL:
             "paged_attention_decode_cascade": ([P, P, P, P, I, P, I, I, F, I, P, P, P, I, P, S, P], I),
             "kv_swap_blocks": ([P, P, P, P, P, I, P, I, I, P], I),
             "paged_attention_prefill": ([P, P, P, P, I, I, P, I, P, I, I, F, I, P], I),
+            "kv_pool_set_wait_limit": ([P, ctypes.c_ulonglong], I),
             "kv_pool_get_error": ([P, ctypes.POINTER(I)], I),
             "kv_pool_clear_error": ([P], I),
             "kv_strerror": ([I], ctypes.c_char_p),
@@ -263,6 +264,12 @@ def paged_attention_prefill(handle, q, out, cu_seqlens, max_query_len: int, bloc
         _stream(stream)), "paged_attention_prefill")
 
 
+def kv_pool_set_wait_limit(handle, limit_ns: int) -> None:
+    """Limit of one pipeline wait in the decode kernels (default and largest
+    2 s; 0 makes every wait that is not already satisfied give up)."""
+    _check(load().kv_pool_set_wait_limit(handle, int(limit_ns)), "kv_pool_set_wait_limit")
+
+
 def kv_pool_get_error(handle) -> int:
     bits = ctypes.c_int()
     st = load().kv_pool_get_error(handle, ctypes.byref(bits))
@@ -381,6 +388,9 @@ class KVPool:
         paged_attention_prefill(self.handle, q, out, cu_seqlens, max_query_len, block_tables,
                                 seq_lens, scale, self.num_kv_heads, self.dtype, stream)
         return out
+
+    def set_wait_limit(self, limit_ns: int) -> None:
+        kv_pool_set_wait_limit(self.handle, limit_ns)
 
     def get_error(self) -> int:
         return kv_pool_get_error(self.handle)

@@ -19,9 +19,16 @@ def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
     assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["dtype"] == "f64" and d["data"] == "synthetic"
     assert d["config"]["workload"] == bench.WORKLOAD_TEXT["tiny"]
+    # the same workload description as the library's own arm prints
+    from paged_kv_cache_68_gb300 import workloads as wl
+    args = bench.parse_args(["--workload", "tiny"])
+    w = wl.on_host(bench.make_workload("tiny", 0, None))
+    assert d["config"] == bench.decode_config(args, w, None, 1)
+    assert d["config"]["global_batch"] == 4 and d["config"]["parallelism"] == "replicas x1"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["unit"] == d["unit"] and cb["sample"]
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
