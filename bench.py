@@ -81,6 +81,10 @@ def parse_args(argv=None):
                     help="override the workload's batch (profiling a smaller case)")
     ap.add_argument("--block-size", type=int, default=None,
                     help="block size of the long-context workload (8, 16 or 32)")
+    ap.add_argument("--fresh-fork", action="store_true",
+                    help="shared-prefix workload: the first decode step after the fork (every "
+                         "sample still shares its prompt's partial last block, so with a "
+                         "2008-token prompt the step makes 3 copy-on-write copies per prompt)")
     ap.add_argument("--prompt-len", type=int, default=None,
                     help="prompt length of the shared-prefix workload (2000 or 2008)")
     ap.add_argument("--kv-cache", choices=["fp8_e4m3", "int8"], default=None,
@@ -99,7 +103,7 @@ def parse_args(argv=None):
 
 
 def make_workload(name: str, seed: int, device, placement: str = "random", batch=None,
-                  block_size=None, prompt_len=None, decodes=0, chunk=None):
+                  block_size=None, prompt_len=None, decodes=0, chunk=None, fresh_fork=False):
     from paged_kv_cache_68_gb300 import workloads as wl
     kw = {} if batch is None else {"batch": batch}
     if name == "llama3_8b_gqa":
@@ -111,6 +115,9 @@ def make_workload(name: str, seed: int, device, placement: str = "random", batch
             kw = {"prompts": batch}
         if prompt_len is not None:
             kw["prompt_len"] = prompt_len
+        if fresh_fork:                     # the first step after the fork: no divergent tokens
+            import numpy as np
+            kw["divergent"] = np.zeros(kw.get("prompts", 32) * 4, np.int64)
         return wl.shared_prefix(seed, device=device, **kw)
     if name == "tiny":
         return wl.tiny(seed, device=device)
@@ -345,6 +352,7 @@ def decode_config(args, w, q8, world):
             + ("" if args.batch is None else f" (batch overridden to {args.batch})")
             + ("" if args.block_size is None else f" (block_size {args.block_size})")
             + ("" if args.prompt_len is None else f" (prompt_len {args.prompt_len})")
+            + (" (fresh fork: no divergent tokens yet)" if args.fresh_fork else "")
             + ("" if q8 is None else f", K/V stored as {q8.cache} codes"),
             "seed": args.seed, "placement": args.placement, "global_batch": w.batch * world,
             "kv_cache": q8.cache if q8 is not None else w.dtype,
@@ -510,7 +518,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     pagedkv.load()
     w = make_workload(args.workload, args.seed, dev, args.placement, args.batch,
-                      args.block_size, args.prompt_len)
+                      args.block_size, args.prompt_len, fresh_fork=args.fresh_fork)
     tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
     k_pool, v_pool = w.k_pool, w.v_pool
     # the step's inputs live back to back in one device buffer (256-byte
@@ -942,7 +950,7 @@ def run_reference(args):
     c_oracle.build()
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
     wd = make_workload(args.workload, args.seed, dev, args.placement, args.batch,
-                       args.block_size, args.prompt_len)
+                       args.block_size, args.prompt_len, fresh_fork=args.fresh_fork)
     q8 = None if not args.kv_cache else q8_on_host(wl.q8_pools(wd, args.kv_cache, args.seed))
     w = wl.on_host(wd)
     del wd

@@ -290,9 +290,10 @@ kv_status paged_attention_cascade_workspace_size(kv_pool_t pool, int batch, int 
  *   A group outside the batch, overlapping its predecessor or out of order is
  *   ignored (its members are decoded plainly) and sets KV_DEVERR_GROUP_RANGE;
  *   the shared-block count is clamped to every member's own block count.
- * num_groups <= 1024.  Pools that are not 16-bit head_dim-128, query/KV head
- *   ratios other than 4 and 8, block sizes other than 16 and 32, and
- *   num_groups = 0 are decoded by paged_attention_decode (same result).
+ * num_groups <= 1024.  Pools that are not 16-bit head_dim-128, block sizes
+ *   other than 16 and 32, and num_groups = 0 are decoded by
+ *   paged_attention_decode (same result); every query/KV head ratio (1, 2, 4,
+ *   8) has a prefix pass, whose tiles hold 16 / ratio members' query rows.
  * workspace: at least paged_attention_cascade_workspace_size bytes.
  * Two kernels are enqueued (the shared-prefix pass, then the per-sequence
  * pass); the other arguments, errors and device error bits are those of
@@ -381,11 +382,12 @@ kv_status paged_attention_decode_noalloc(kv_pool_t pool, const void* q, void* ou
                                          float scale, int num_kv_heads, void* stream);
 
 /*
- * kv_pool_set_wait_limit -- how long one pipeline wait of the decode kernels
- * (paged_attention_decode, _cascade, _noalloc) may last before the kernel
- * gives up: it sets KV_DEVERR_TIMEOUT, stops loading and attending, lets the
- * copies already in flight land (those waits always take the default limit)
- * and returns; the outputs of that call are then unspecified.  The default
+ * kv_pool_set_wait_limit -- how long one pipeline wait of the attention
+ * kernels (paged_attention_decode, _cascade, _noalloc, paged_attention_prefill)
+ * may last before the kernel gives up: it sets KV_DEVERR_TIMEOUT, stops
+ * loading and attending, lets the copies and tensor-core products already in
+ * flight finish (those waits always take the default limit) and returns; the
+ * outputs of that call are then unspecified.  The default
  * and largest value is 2 s (2e9 ns); larger values are clamped to it.  A
  * limit of 0 makes every wait that does not find its tile already there give
  * up, which exercises the failure path with valid inputs.  Host-side only,

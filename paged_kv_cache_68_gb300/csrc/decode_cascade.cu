@@ -4,9 +4,8 @@
 // (paged_decode_prefix) leaves per-(sequence, head) prefix states in the
 // workspace, then the split kernel attends each sequence's remaining blocks
 // and folds the prefix state into its log-sum-exp merge.  Shapes without a
-// prefix kernel (fp32 pools, head_dim 64, groups of 1 or 2, block sizes other
-// than 16 and 32) and calls with no groups run the plain decode, which gives
-// the same result.
+// prefix kernel (fp32 pools, head_dim 64, block sizes other than 16 and 32)
+// and calls with no groups run the plain decode, which gives the same result.
 #include <atomic>
 #include <cstdio>
 #include <mutex>
@@ -43,7 +42,8 @@ kv_status split_part(kv_pool* pool, int batch, int num_q_heads, int num_groups, 
 }
 
 bool cascade_shape(const kv_pool& pool, int group) {
-    return pool.elem_bytes == 2 && pool.head_dim == 128 && (group == 4 || group == 8) &&
+    return pool.elem_bytes == 2 && pool.head_dim == 128 &&
+           (group == 1 || group == 2 || group == 4 || group == 8) &&
            (pool.block_size == 16 || pool.block_size == 32) && pool.has_h2_maps;
 }
 
@@ -81,8 +81,14 @@ cudaError_t by_shape(const kv_pool& pool, int group, F&& f) {
     const int bs = pool.block_size;
 #define PKV_P(TT, GG, BB) \
     if (group == GG && bs == BB) return f.template operator()<TT, GG, BB>();
-    if (bf) { PKV_P(__nv_bfloat16, 4, 16) PKV_P(__nv_bfloat16, 4, 32) PKV_P(__nv_bfloat16, 8, 16) PKV_P(__nv_bfloat16, 8, 32) }
-    else    { PKV_P(__half, 4, 16) PKV_P(__half, 4, 32) PKV_P(__half, 8, 16) PKV_P(__half, 8, 32) }
+    if (bf) {
+        PKV_P(__nv_bfloat16, 1, 16) PKV_P(__nv_bfloat16, 1, 32) PKV_P(__nv_bfloat16, 2, 16)
+        PKV_P(__nv_bfloat16, 2, 32) PKV_P(__nv_bfloat16, 4, 16) PKV_P(__nv_bfloat16, 4, 32)
+        PKV_P(__nv_bfloat16, 8, 16) PKV_P(__nv_bfloat16, 8, 32)
+    } else {
+        PKV_P(__half, 1, 16) PKV_P(__half, 1, 32) PKV_P(__half, 2, 16) PKV_P(__half, 2, 32)
+        PKV_P(__half, 4, 16) PKV_P(__half, 4, 32) PKV_P(__half, 8, 16) PKV_P(__half, 8, 32)
+    }
 #undef PKV_P
     return cudaErrorNotSupported;
 }

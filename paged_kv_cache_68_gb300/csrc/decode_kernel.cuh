@@ -199,6 +199,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // `limit_ns` nanoseconds and return false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           unsigned long long limit_ns = kWaitLimitNs) {
+    if (limit_ns == 0) return mbar_test(bar, parity);
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try(bar, parity)) {

@@ -95,7 +95,8 @@ __device__ __forceinline__ int find_le(const int* a, int n, int u) {
 // output) nt*8 + 2 tig + {0, 1}; column c is member c / G, head c % G.
 template <typename T, int D, int G, int BSC>
 struct TcRows {
-    static_assert(sizeof(T) == 2 && BSC % 16 == 0 && (G == 4 || G == 8), "tensor-core shapes");
+    static_assert(sizeof(T) == 2 && BSC % 16 == 0 && (G == 1 || G == 2 || G == 4 || G == 8),
+                  "tensor-core shapes");
     static constexpr int NT = kRows / 8;
     static constexpr int KS = D / 16;
     static constexpr int MT = D / 16;

@@ -56,6 +56,7 @@ cudaError_t launch_typed(const kv_pool& pool, const PrefillCall& c, cudaStream_t
     p.max_q = c.max_query_len;
     p.box_rows = pool.block_size < BN ? pool.block_size : BN;
     p.qscale = c.scale * 1.4426950408889634f;
+    p.wait_ns = pool.wait_ns;
     cudaLaunchConfig_t cfg = {};
     // one CTA per pair of query tiles
     cfg.gridDim = dim3((unsigned)((c.max_query_len + 2 * QT - 1) / (2 * QT)),

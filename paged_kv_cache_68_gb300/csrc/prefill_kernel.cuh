@@ -113,6 +113,7 @@ struct Params {
     int max_q;                    // the largest C_b the grid covers
     int box_rows;                 // rows of one K/V box: min(bs, BN)
     float qscale;                 // scale * log2(e), > 0
+    unsigned long long wait_ns;   // limit of one pipeline wait (the pool's setting)
 };
 
 // ------------------------------------------------------------ tcgen05 PTX --
@@ -257,13 +258,14 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 
-// Bounded wait; on expiry (or when another role already gave up) raise the
-// abort flag and return false.
+// Bounded wait (limit_ns); on expiry (or when another role already gave up)
+// raise the abort flag and return false.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag, int* err) {
-    if (dec::mbar_try(bar, parity)) return true;
+                                              volatile int* abort_flag, int* err,
+                                              unsigned long long limit_ns) {
+    if (limit_ns == 0 ? dec::mbar_test(bar, parity) : dec::mbar_try(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (dec::mbar_wait(bar, parity)) return true;
+    if (limit_ns > 0 && dec::mbar_wait(bar, parity, limit_ns)) return true;
     *abort_flag = 1;
     atomicOr(err, KV_DEVERR_TIMEOUT);
     return false;
@@ -396,7 +398,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // tile j reuses the buffer of tile j - nst: freed when every
                 // stream's S (K) or PV (V) of that tile is done
                 if (lane == 0 && j >= nst)
-                    ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err);
+                    ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err,
+                                       p.wait_ns);
                 if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
                 const int t = j * BN + lane * R;   // first token of this lane's box
                 int row = -1;
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t dk = sdesc_sw128(sbase + OFF_K, 16u, 1024u);
             const uint64_t dv = sdesc_sw128(sbase + OFF_V, KVHALF, 1024u);
             auto wait_all = [&](uint32_t bb, uint32_t parity) {
-                return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
+                return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err, p.wait_ns));
             };
             bool ok = wait_all(bar(BAR_Q), 0);
             int done_pv = 0;                       // PV products issued
@@ -489,10 +492,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j > 0 && !pv(j - 1)) break;
             }
             if (ok && *abort_flag == 0 && done_pv == ntiles - 1) pv(ntiles - 1);
-            // Drain: every MMA issued has completed before TMEM is freed.
+            // Drain: every MMA issued has completed before TMEM is freed --
+            // after an abort too, so this wait takes the full limit and does
+            // not give up because another role did.
             if (elect_one()) mma_commit(sbar(x, SB_DR));
             __syncwarp();
-            if (!wait_all(sbar(x, SB_DR), 0)) atomicOr(p.err, KV_DEVERR_TIMEOUT);
+            if (!__all_sync(FULL, dec::mbar_wait(sbar(x, SB_DR), 0, kWaitLimitNs)))
+                atomicOr(p.err, KV_DEVERR_TIMEOUT);
         }
         __syncwarp();
     } else if (warp / NSOFT < nstreams) {
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // uniform across the warp; after a failed wait the warp touches
         // neither TMEM nor the pipeline barriers again.
         auto wait_warp = [&](uint32_t bb, uint32_t parity) {
-            return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err));
+            return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err, p.wait_ns));
         };
         for (int j = 0; ok && j < ntiles; ++j) {
             const int t0 = j * BN;

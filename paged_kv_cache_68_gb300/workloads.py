@@ -420,8 +420,10 @@ def chunked_prefill(seed: int = 0, batch: int = 16, chunk: int = 256, max_prefix
 def shared_prefix(seed: int = 0, prompts: int = 32, prompt_len: int = 2000, n: int = 4,
                   max_divergent: int = 256, block_size: int = 16,
                   divergent: Optional[np.ndarray] = None, pool_factor: float = 1.5,
-                  device: Optional[str] = None) -> Workload:
-    """Parallel sampling over shared prompts (Llama-3-8B GQA shape, bf16).
+                  device: Optional[str] = None, num_q_heads: int = 32, num_kv_heads: int = 8,
+                  dtype: str = "bf16") -> Workload:
+    """Parallel sampling over shared prompts (Llama-3-8B GQA shape, bf16, by
+    default; other head counts and 16-bit types for the cascade's shapes).
 
     Each prompt is prefilled once and forked into n samples (every prompt
     block has reference count n).  Sample s then holds d_s ~ U[0,
@@ -451,8 +453,8 @@ def shared_prefix(seed: int = 0, prompts: int = 32, prompt_len: int = 2000, n: i
                 bm.append_slot(s)
     history_copies = bm.copies_made
     bm.check_invariant()
-    inner = (8, 128)
-    val = _values(seed, rng, "bf16", device)
+    inner = (num_kv_heads, 128)
+    val = _values(seed, rng, dtype, device)
     k_pool = val.nan((N, bs) + inner)
     v_pool = val.nan((N, bs) + inner)
     pk = val.randn((prompts, prompt_len) + inner)
@@ -469,7 +471,7 @@ def shared_prefix(seed: int = 0, prompts: int = 32, prompt_len: int = 2000, n: i
         val.set_rows(k_pool, rows[prompt_len:], dk[off:off + int(d[s])])
         val.set_rows(v_pool, rows[prompt_len:], dv[off:off + int(d[s])])
         off += int(d[s])
-    q = val.randn((S, 32, 128))
+    q = val.randn((S, num_q_heads, 128))
     k_new = val.randn((S,) + inner)
     v_new = val.randn((S,) + inner)
     slots, pairs = [], []
@@ -480,7 +482,8 @@ def shared_prefix(seed: int = 0, prompts: int = 32, prompt_len: int = 2000, n: i
             pairs.append(cow)
     bm.check_invariant()
     seq_lens = np.asarray([bm.lens[s] for s in range(S)], dtype=np.int32)
-    w = Workload(name=f"shared_prefix_p{prompt_len}", dtype="bf16", num_q_heads=32, num_kv_heads=8,
+    w = Workload(name=f"shared_prefix_p{prompt_len}", dtype=dtype, num_q_heads=num_q_heads,
+                 num_kv_heads=num_kv_heads,
                  head_dim=128, block_size=bs, num_blocks=N, scale=1.0 / math.sqrt(128),
                  k_pool=k_pool, v_pool=v_pool, q=q, k_new=k_new, v_new=v_new,
                  slot_mapping=np.asarray(slots, dtype=np.int64),

@@ -97,6 +97,19 @@ def test_cascade_group8_and_members_without_suffix():
     _check(w, groups, "group 8, empty suffix")
 
 
+@pytest.mark.parametrize("dtype,hq,hkv,bs,n", [("f16", 16, 16, 16, 4),   # MHA (OPT-13B kind)
+                                               ("bf16", 16, 8, 32, 6),   # ratio 2
+                                               ("f16", 8, 8, 32, 17)])   # two sub-groups of 16
+def test_cascade_group_ratios_1_and_2(dtype, hq, hkv, bs, n):
+    """Query/KV head ratios 1 and 2: a prefix tile holds 16 and 8 members'
+    query rows; 17 samples of one prompt at ratio 1 fill a sub-group and
+    spill one member into a second."""
+    w = wl.shared_prefix(8, prompts=3, prompt_len=600, n=n, max_divergent=50, block_size=bs,
+                         num_q_heads=hq, num_kv_heads=hkv, dtype=dtype)
+    assert (w.groups[:, 2] >= 600 // bs).all()
+    _check(w, w.groups, f"cascade {dtype} {hq}/{hkv} bs{bs} n{n}")
+
+
 def test_cascade_rejects_overlapping_groups_but_stays_correct():
     w = wl.shared_prefix(6, prompts=2, prompt_len=300, n=4, max_divergent=20)
     g = w.groups.copy()

@@ -73,3 +73,39 @@ def test_cascade_decode_wait_gives_up():
     w = wl.shared_prefix(43, prompts=6, prompt_len=2000, n=4, max_divergent=200)
     groups = torch.from_numpy(np.ascontiguousarray(w.groups, dtype=np.int32)).to("cuda")
     _expire_then_recover(w, lambda pool, q, t, l: pool.decode_cascade(q, t, l, w.scale, groups))
+
+
+def test_prefill_wait_gives_up():
+    """The tensor-core prefill kernel (TMA producers, MMA issuers, softmax
+    warps, TMEM): with the limit at 0 its roles give up, the MMA issuers still
+    wait (with the full limit) for the products already issued before TMEM is
+    freed, and the call returns with the timeout bit set; then a normal call
+    matches the oracle."""
+    from parity import oracle_prefill_step
+    w = wl.chunked_prefill(44, batch=6, chunk=256, max_prefix=2000, decodes=4)
+    _, _, ref, rows = oracle_prefill_step(w)
+    dev = torch.device("cuda")
+    tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
+    pool = pagedkv.KVPool(tv(w.k_pool).clone(), tv(w.v_pool).clone())
+    try:
+        q = tv(w.q)
+        tables = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev)
+        lens = torch.from_numpy(w.seq_lens).to(dev)
+        cu = torch.from_numpy(np.ascontiguousarray(w.cu_seqlens, dtype=np.int32)).to(dev)
+        mq = int(np.diff(w.cu_seqlens).max())
+        pool.append(tv(w.k_new), tv(w.v_new), torch.from_numpy(w.slot_mapping).to(dev))
+        torch.cuda.synchronize()
+        assert pool.get_error() == 0
+        pool.set_wait_limit(0)
+        pool.prefill(q, cu, mq, tables, lens, w.scale, out=torch.zeros_like(q))
+        torch.cuda.synchronize()                      # the kernel returned
+        bits = pool.get_error()
+        assert bits & pagedkv.KV_DEVERR_TIMEOUT, f"no timeout reported ({bits:#x})"
+        pool.clear_error()
+        pool.set_wait_limit(2_000_000_000)
+        out = pool.prefill(q, cu, mq, tables, lens, w.scale, out=torch.zeros_like(q))
+        torch.cuda.synchronize()
+        assert pool.get_error() == 0
+        check_attention(wl.value_to_numpy(out, w.dtype)[rows], ref, w.dtype, "after recovery")
+    finally:
+        pool.close()
