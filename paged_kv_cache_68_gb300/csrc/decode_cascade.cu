@@ -6,6 +6,7 @@
 // and folds the prefix state into its log-sum-exp merge.  Shapes without a
 // prefix kernel (fp32 pools, head_dim 64, block sizes other than 16 and 32)
 // and calls with no groups run the plain decode, which gives the same result.
+// 16-bit and 8-bit (FP8 E4M3, INT8) pools alike.
 #include <atomic>
 #include <cstdio>
 #include <mutex>
@@ -41,46 +42,36 @@ kv_status split_part(kv_pool* pool, int batch, int num_q_heads, int num_groups, 
     return KV_OK;
 }
 
+// The shapes with a prefix kernel.  16-bit pools: block size 16 or 32 (one
+// block per unit), a pool with one-copy (4-D) tensor maps.  8-bit pools: 32-row
+// units (two blocks of 16, or one of 32 -- the split kernel's 8-bit unit of
+// the same pool, so the second pass skips whole units).
 bool cascade_shape(const kv_pool& pool, int group) {
-    return pool.elem_bytes == 2 && pool.head_dim == 128 &&
-           (group == 1 || group == 2 || group == 4 || group == 8) &&
-           (pool.block_size == 16 || pool.block_size == 32) && pool.has_h2_maps;
+    if (pool.head_dim != 128 || !(group == 1 || group == 2 || group == 4 || group == 8) ||
+        !(pool.block_size == 16 || pool.block_size == 32))
+        return false;
+    if (is_q8(pool))
+        return pool.has_swizzled_maps && (pool.dtype == KV_BF16 || pool.dtype == KV_F16);
+    return pool.elem_bytes == 2 && pool.has_h2_maps;
 }
 
-template <typename T, int G, int BSC>
-cudaError_t prefix_attrs(size_t smem, int* occ) {
-    auto k = dec::paged_decode_prefix<T, 128, G, BSC>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, dec::NTHREADS, smem);
+// Token rows of a unit's tile, bytes per element, scale rows (INT8).
+struct PrefixTile {
+    int rows, elt;
+    bool scales;
+};
+PrefixTile prefix_tile(const kv_pool& pool) {
+    if (is_q8(pool)) return {32, 1, pool.cache_dtype == KV_INT8};
+    return {pool.block_size, pool.elem_bytes, false};
 }
 
-template <typename T, int G, int BSC>
-cudaError_t prefix_launch(const kv_pool& pool, const dec::PParams& p, size_t smem, int grid,
-                          cudaStream_t stream) {
-    auto k = dec::paged_decode_prefix<T, 128, G, BSC>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(dec::NTHREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, pool.tmap_k_h2, pool.tmap_v_h2, p);
-}
-
-// Dispatch on (dtype, group, block size) for one of the two functions above.
+// Dispatch of the 16-bit instances on (dtype, group, block size).
 template <class F>
-cudaError_t by_shape(const kv_pool& pool, int group, F&& f) {
+cudaError_t by_shape16(const kv_pool& pool, int group, F&& f) {
     const bool bf = pool.dtype == KV_BF16;
     const int bs = pool.block_size;
 #define PKV_P(TT, GG, BB) \
-    if (group == GG && bs == BB) return f.template operator()<TT, GG, BB>();
+    if (group == GG && bs == BB) return f.template operator()<TT, GG, BB, dec::TcRows<TT, 128, GG, BB>>();
     if (bf) {
         PKV_P(__nv_bfloat16, 1, 16) PKV_P(__nv_bfloat16, 1, 32) PKV_P(__nv_bfloat16, 2, 16)
         PKV_P(__nv_bfloat16, 2, 32) PKV_P(__nv_bfloat16, 4, 16) PKV_P(__nv_bfloat16, 4, 32)
@@ -93,21 +84,41 @@ cudaError_t by_shape(const kv_pool& pool, int group, F&& f) {
     return cudaErrorNotSupported;
 }
 
+cudaError_t prefix_attrs_any(const kv_pool& pool, int group, size_t smem, int* occ) {
+    if (is_q8(pool))
+        return pool.dtype == KV_BF16 ? prefix_q8_attrs_bf16(pool, group, smem, occ)
+                                     : prefix_q8_attrs_f16(pool, group, smem, occ);
+    return by_shape16(pool, group, [&]<typename T, int GG, int BB, class Pol>() {
+        return dec::prefix_attrs<T, GG, BB, Pol>(smem, occ);
+    });
+}
+
+cudaError_t prefix_launch_any(const kv_pool& pool, int group, const dec::PParams& p, size_t smem,
+                              int grid, cudaStream_t stream) {
+    if (is_q8(pool))
+        return pool.dtype == KV_BF16 ? prefix_q8_launch_bf16(pool, group, p, smem, grid, stream)
+                                     : prefix_q8_launch_f16(pool, group, p, smem, grid, stream);
+    return by_shape16(pool, group, [&]<typename T, int GG, int BB, class Pol>() {
+        return dec::prefix_launch<T, GG, BB, Pol>(pool.tmap_k_h2, pool.tmap_v_h2, p, smem, grid,
+                                                  stream);
+    });
+}
+
 cudaError_t plan_prefix(const kv_pool& pool, int batch, int num_q_heads, int num_groups,
                         size_t base, PrefixPlan* pp) {
     const int G = num_q_heads / pool.num_kv_heads;
-    const int bs = pool.block_size, D = pool.head_dim, elt = pool.elem_bytes;
-    const size_t stage = 2ull * bs * D * elt;
+    const int D = pool.head_dim;
+    const PrefixTile tile = prefix_tile(pool);
+    const size_t stage = 2ull * tile.rows * D * tile.elt;
     int best_s = 0, best_occ = 0, best_score = -1;
     size_t best_smem = 0;
     for (int S = dec::NCW; S <= 8 * dec::NCW; S += dec::NCW) {
         if (S > dec::NCW && (size_t)S * stage > kMaxRingBytesP) break;
-        const size_t smem = dec::PLayout(S, num_groups, bs, D, elt).total + 1024;
+        const size_t smem =
+            dec::PLayout(S, num_groups, tile.rows, D, tile.elt, tile.scales).total + 1024;
         if (smem > kMaxSmemP) break;
         int occ = 0;
-        cudaError_t e = by_shape(pool, G, [&]<typename T, int GG, int BB>() {
-            return prefix_attrs<T, GG, BB>(smem, &occ);
-        });
+        cudaError_t e = prefix_attrs_any(pool, G, smem, &occ);
         if (e != cudaSuccess) return e;
         const int per_warp = S / dec::NCW > 2 ? 2 : S / dec::NCW;
         if (occ >= 1 && occ * per_warp >= best_score) {
@@ -224,7 +235,12 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
     p.bs = pool->block_size;
     p.stages = pp.stages;
     p.num_ctas = pp.num_ctas;
-    p.qscale = scale * 1.4426950408889634f;
+    p.k_scales = pool->k_scales;
+    p.v_scales = pool->v_scales;
+    // FP8 pools: the K scale multiplies every score, the V scale the output
+    const bool fp8 = pool->cache_dtype == KV_FP8_E4M3;
+    p.qscale = scale * 1.4426950408889634f * (fp8 ? pool->fp8_k_scale : 1.f);
+    p.vscale = fp8 ? pool->fp8_v_scale : 1.f;
     p.wait_ns = pool->wait_ns;
     // argument checks of the second pass first, so nothing is enqueued on error
     if (batch < 1 || batch > pagedkv::kMaxBatch || max_blocks_per_seq < 1 ||
@@ -233,9 +249,7 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
         (reinterpret_cast<uintptr_t>(workspace) & 15u) || !(scale == scale))
         return KV_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = pagedkv::by_shape(*pool, G, [&]<typename T, int GG, int BB>() {
-        return pagedkv::prefix_launch<T, GG, BB>(*pool, p, pp.smem_bytes, pp.num_ctas, s);
-    });
+    e = pagedkv::prefix_launch_any(*pool, G, p, pp.smem_bytes, pp.num_ctas, s);
     if (e != cudaSuccess) return pagedkv::cuda_fail(e, "paged_attention_decode_cascade(prefix)");
     return pagedkv::decode_after_prefix(pool, q, out, block_tables, max_blocks_per_seq, seq_lens,
                                         batch, num_q_heads, scale, workspace, plain,

@@ -1450,13 +1450,16 @@ __device__ __forceinline__ int block_excl_max(int v, int* scratch) {
 // ------------------------------------------- cascade groups (both passes) --
 // A group (first member, members, shared leading blocks) is used when it lies
 // inside the batch, starts at or after the end of every earlier group, and at
-// least one block is shared (the count is clamped to each member's own block
-// count).  Both passes compact the used groups, in order, into shared memory
-// (vg: first[n], size[n], blocks[n]) and return n; unused groups set
-// KV_DEVERR_GROUP_RANGE when malformed.  Every thread of the CTA calls.
+// least one work unit is shared (the block count is clamped to each member's
+// own block count, then counted in whole units of `ub` blocks: both passes
+// must use the same unit).  Both passes compact the used groups, in order,
+// into shared memory (vg: first[n], size[n], shared units[n]) and return n;
+// unused groups set KV_DEVERR_GROUP_RANGE when malformed.  Every thread of
+// the CTA calls.
 __device__ __forceinline__ int load_groups(const int32_t* g_first, const int32_t* g_size,
                                            const int32_t* g_blocks, int K, const int32_t* seq_lens,
-                                           int B, int bs, int cap, int* vg, int* scratch, int* err) {
+                                           int B, int bs, int cap, int ub, int* vg, int* scratch,
+                                           int* err) {
     const int per = (K + (int)blockDim.x - 1) / (int)blockDim.x;
     const int k0 = min(K, (int)threadIdx.x * per), k1 = min(K, k0 + per);
     auto raw_end = [&](int k) {
@@ -1471,7 +1474,7 @@ __device__ __forceinline__ int load_groups(const int32_t* g_first, const int32_t
         if (!ok) return 0;
         for (int m = 0; m < size; ++m)
             blocks = min(blocks, (min(max(seq_lens[first + m], 0), cap) + bs - 1) / bs);
-        return blocks;
+        return blocks / ub;
     };
     int cmax = 0;
     for (int k = k0; k < k1; ++k) cmax = max(cmax, raw_end(k));
@@ -1503,7 +1506,7 @@ __device__ __forceinline__ int load_groups(const int32_t* g_first, const int32_t
     return n;
 }
 
-// Shared leading blocks of sequence b (0 outside every used group).
+// Shared leading units of sequence b (0 outside every used group).
 __device__ __forceinline__ int group_skip(const int* vg, int K, int n, int b) {
     if (n == 0 || b < vg[0]) return 0;
     int lo = 0, hi = n;
@@ -1517,7 +1520,7 @@ __device__ __forceinline__ int group_skip(const int* vg, int K, int n, int b) {
 // -- the units of a call ------------------------------------------------------
 // prefix[b] (shared memory) = the units of KV head 0 in sequences before b:
 // each sequence contributes its blocks (clamped to the table's capacity, in
-// units of bsu tokens) less, for cascade decode, the leading blocks the
+// units of bsu tokens) less, for cascade decode, the leading units the
 // shared-prefix pass attended (skip_s[b]).  prefix[B] is the total.  Every
 // thread of the CTA calls; `report` flags contexts longer than the table.
 __device__ __forceinline__ void unit_prefix(const Params& p, unsigned char* smem, const Layout& lay,
@@ -1527,10 +1530,11 @@ __device__ __forceinline__ void unit_prefix(const Params& p, unsigned char* smem
     int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
     int* prefix = reinterpret_cast<int*>(smem + lay.prefix);
     int* skip_s = reinterpret_cast<int*>(smem + lay.skip);
-    // cascade: the leading blocks the shared-prefix pass attended
+    // cascade: the leading units the shared-prefix pass attended
     int* vg = reinterpret_cast<int*>(smem + lay.groups);
     const int nvg = cascade ? load_groups(p.g_first, p.g_size, p.g_blocks, p.num_groups,
-                                          p.seq_lens, B, p.bs, cap, vg, warp_tot, p.err)
+                                          p.seq_lens, B, p.bs, cap, bsu / p.bs, vg, warp_tot,
+                                          p.err)
                             : 0;
     const int per = (B + nthreads - 1) / nthreads;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);

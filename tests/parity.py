@@ -103,8 +103,9 @@ def _t(a, device):
     return a.to(device) if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
 
-def gpu_step_q8(w: wl.Workload, p: wl.Q8Pools, device="cuda", return_pools=True):
-    """copy_blocks -> kv_append (quantising) -> decode on an 8-bit pool.
+def gpu_step_q8(w: wl.Workload, p: wl.Q8Pools, device="cuda", return_pools=True, groups=None):
+    """copy_blocks -> kv_append (quantising) -> decode on an 8-bit pool (cascade
+    decode over `groups` [first, size, shared blocks] rows when given).
     Returns (k_codes, v_codes, k_scales, v_scales, out, error_bits) on the host."""
     tv = lambda a: wl.value_to_torch(a, w.dtype, device)
     kc, vc = _t(p.k_codes, device).clone(), _t(p.v_codes, device).clone()
@@ -115,8 +116,13 @@ def gpu_step_q8(w: wl.Workload, p: wl.Q8Pools, device="cuda", return_pools=True)
     try:
         pool.copy_blocks(torch.from_numpy(np.ascontiguousarray(w.pairs, dtype=np.int32)).to(device))
         pool.append(tv(w.k_new), tv(w.v_new), torch.from_numpy(w.slot_mapping).to(device))
-        out = pool.decode(tv(w.q), torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device),
-                          torch.from_numpy(w.seq_lens).to(device), w.scale)
+        tables = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device)
+        lens = torch.from_numpy(w.seq_lens).to(device)
+        if groups is None:
+            out = pool.decode(tv(w.q), tables, lens, w.scale)
+        else:
+            g = torch.from_numpy(np.ascontiguousarray(groups, dtype=np.int32)).to(device)
+            out = pool.decode_cascade(tv(w.q), tables, lens, w.scale, g)
         torch.cuda.synchronize()
         err = pool.get_error()
     finally:
