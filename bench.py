@@ -332,12 +332,12 @@ def reduce_max_sum(local_ms: float, local_units: float):
     return float(t.item()), float(u.item())
 
 
-def unique_bytes_fields(w, world, dec_ms):
+def unique_bytes_fields(w, world, dec_ms, q8=None):
     """Shared-prefix steps: decode GB/s against the K/V bytes stored once (the
     prefix counted once per prompt) beside the logical bytes."""
     if "unique_tokens" not in w.info:
         return {}
-    row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2
+    row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2 if q8 is None else q8.row_bytes(w)
     ub = int(w.info["unique_tokens"]) * row
     return {"unique_kv_bytes_per_replica": ub,
             "attention_gbs_unique": round(ub * world / (dec_ms * 1e-3) / 1e9, 2),
@@ -648,8 +648,8 @@ def run_ours(args):
     # bytes count the stored (unique) K/V, not the logical per-sequence K/V.
     roof_bytes = att_bytes
     if cascade and "unique_tokens" in w.info:
-        row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2
-        roof_bytes = att_bytes - w.kv_bytes() + int(w.info["unique_tokens"]) * row
+        row = w.num_kv_heads * w.head_dim * w.elem_bytes * 2 if q8 is None else q8.row_bytes(w)
+        roof_bytes = att_bytes - kv_bytes + int(w.info["unique_tokens"]) * row
     achieved = roof_bytes / (dec_ms * 1e-3) / 1e9
 
     cpu = None
@@ -688,7 +688,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": decode_config(args, w, q8, world),
         "seq_steps_per_s": round(total_seqs / (max_step_ms * 1e-3), 1),
-        **unique_bytes_fields(w, world, max_dec_ms),
+        **unique_bytes_fields(w, world, max_dec_ms, q8),
         "attention_gbs": round(att_bytes * world / (max_dec_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm",
                      "kernel": ("paged_decode_prefix + paged_decode_split (+ paged_decode_merge) (the whole cascade decode call)"

@@ -137,7 +137,8 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
  * Limits: head_dim 128; block_size a multiple of 16, at most 256; the rest as
  *   kv_pool_create.  copy_blocks moves codes and INT8 scales together; decode
  *   computes with the dequantised values (fp32 scores and softmax, as for
- *   16-bit pools).  paged_attention_decode_cascade decodes 8-bit pools plainly.
+ *   16-bit pools).  paged_attention_decode_cascade has a prefix pass for 8-bit
+ *   pools of block size 16 and 32.
  * Errors: KV_EINVAL, KV_EUNSUPPORTED, KV_ECUDA.
  */
 kv_status kv_pool_create_quantized(int num_blocks, int block_size, int num_kv_heads,
@@ -286,14 +287,19 @@ kv_status paged_attention_cascade_workspace_size(kv_pool_t pool, int batch, int 
  *   group_shared_blocks[k] entries.  Groups are disjoint and sorted by their
  *   first member; sequences outside every group are decoded plainly.
  *   Preconditions the kernel cannot check: the shared entries are identical
- *   across members (otherwise the first member's blocks are used for all).
- *   A group outside the batch, overlapping its predecessor or out of order is
- *   ignored (its members are decoded plainly) and sets KV_DEVERR_GROUP_RANGE;
- *   the shared-block count is clamped to every member's own block count.
- * num_groups <= 1024.  Pools that are not 16-bit head_dim-128, block sizes
- *   other than 16 and 32, and num_groups = 0 are decoded by
- *   paged_attention_decode (same result); every query/KV head ratio (1, 2, 4,
- *   8) has a prefix pass, whose tiles hold 16 / ratio members' query rows.
+ *   across members (otherwise the first member's blocks are used for all of
+ *   the prefix pass's blocks).  A group outside the batch, overlapping its
+ *   predecessor or out of order is ignored (its members are decoded plainly)
+ *   and sets KV_DEVERR_GROUP_RANGE.  The prefix pass attends the shared
+ *   blocks that are full for every member (the count is clamped to each
+ *   member's length / block size), in whole work units of the per-sequence
+ *   pass: one block, or two for 8-bit pools of block size 16; shared blocks
+ *   past those are read through each member's own table.
+ * num_groups <= 1024.  head_dim 128, block size 16 or 32, 16-bit pools and
+ *   8-bit pools with 16-bit queries have a prefix pass for every query/KV head
+ *   ratio (1, 2, 4, 8), whose tiles hold 16 / ratio members' query rows and
+ *   128 shared tokens; other shapes and num_groups = 0 are decoded by
+ *   paged_attention_decode (same result).
  * workspace: at least paged_attention_cascade_workspace_size bytes.
  * Two kernels are enqueued (the shared-prefix pass, then the per-sequence
  * pass); the other arguments, errors and device error bits are those of

@@ -11,7 +11,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "decode_prefix.cuh"
+#include "decode_prefix_tc.cuh"
 #include "pagedkv_internal.cuh"
 
 namespace pagedkv {
@@ -42,54 +42,27 @@ kv_status split_part(kv_pool* pool, int batch, int num_q_heads, int num_groups, 
     return KV_OK;
 }
 
-// The shapes with a prefix kernel.  16-bit pools: block size 16 or 32 (one
-// block per unit), a pool with one-copy (4-D) tensor maps.  8-bit pools: 32-row
-// units (two blocks of 16, or one of 32 -- the split kernel's 8-bit unit of
-// the same pool, so the second pass skips whole units).
+// The shapes with a prefix kernel: head_dim 128, groups of 1, 2, 4 or 8, block
+// size 16 or 32, a pool with 128-byte-swizzled tensor maps; 16-bit pools, and
+// 8-bit pools with 16-bit queries.
 bool cascade_shape(const kv_pool& pool, int group) {
     if (pool.head_dim != 128 || !(group == 1 || group == 2 || group == 4 || group == 8) ||
-        !(pool.block_size == 16 || pool.block_size == 32))
+        !(pool.block_size == 16 || pool.block_size == 32) || !pool.has_swizzled_maps)
         return false;
-    if (is_q8(pool))
-        return pool.has_swizzled_maps && (pool.dtype == KV_BF16 || pool.dtype == KV_F16);
-    return pool.elem_bytes == 2 && pool.has_h2_maps;
+    if (is_q8(pool)) return pool.dtype == KV_BF16 || pool.dtype == KV_F16;
+    return pool.elem_bytes == 2;
 }
 
-// Token rows of a unit's tile, bytes per element, scale rows (INT8).
-struct PrefixTile {
-    int rows, elt;
-    bool scales;
-};
-PrefixTile prefix_tile(const kv_pool& pool) {
-    if (is_q8(pool)) return {32, 1, pool.cache_dtype == KV_INT8};
-    return {pool.block_size, pool.elem_bytes, false};
-}
-
-// Dispatch of the 16-bit instances on (dtype, group, block size).
-template <class F>
-cudaError_t by_shape16(const kv_pool& pool, int group, F&& f) {
-    const bool bf = pool.dtype == KV_BF16;
-    const int bs = pool.block_size;
-#define PKV_P(TT, GG, BB) \
-    if (group == GG && bs == BB) return f.template operator()<TT, GG, BB, dec::TcRows<TT, 128, GG, BB>>();
-    if (bf) {
-        PKV_P(__nv_bfloat16, 1, 16) PKV_P(__nv_bfloat16, 1, 32) PKV_P(__nv_bfloat16, 2, 16)
-        PKV_P(__nv_bfloat16, 2, 32) PKV_P(__nv_bfloat16, 4, 16) PKV_P(__nv_bfloat16, 4, 32)
-        PKV_P(__nv_bfloat16, 8, 16) PKV_P(__nv_bfloat16, 8, 32)
-    } else {
-        PKV_P(__half, 1, 16) PKV_P(__half, 1, 32) PKV_P(__half, 2, 16) PKV_P(__half, 2, 32)
-        PKV_P(__half, 4, 16) PKV_P(__half, 4, 32) PKV_P(__half, 8, 16) PKV_P(__half, 8, 32)
-    }
-#undef PKV_P
-    return cudaErrorNotSupported;
-}
+// The 16-bit pools' prefix pass runs on tcgen05 (one CTA per SM), the 8-bit
+// pools' on mma.sync (decode_prefix.cuh; codes convert in registers).
+bool tc_prefix(const kv_pool& pool) { return !is_q8(pool); }
 
 cudaError_t prefix_attrs_any(const kv_pool& pool, int group, size_t smem, int* occ) {
     if (is_q8(pool))
         return pool.dtype == KV_BF16 ? prefix_q8_attrs_bf16(pool, group, smem, occ)
                                      : prefix_q8_attrs_f16(pool, group, smem, occ);
-    return by_shape16(pool, group, [&]<typename T, int GG, int BB, class Pol>() {
-        return dec::prefix_attrs<T, GG, BB, Pol>(smem, occ);
+    return ptc::by_tc_shape(pool, group, [&]<typename T, int GG, int BB>() {
+        return ptc::prefix_tc_attrs<T, GG, BB>(smem, occ);
     });
 }
 
@@ -98,34 +71,54 @@ cudaError_t prefix_launch_any(const kv_pool& pool, int group, const dec::PParams
     if (is_q8(pool))
         return pool.dtype == KV_BF16 ? prefix_q8_launch_bf16(pool, group, p, smem, grid, stream)
                                      : prefix_q8_launch_f16(pool, group, p, smem, grid, stream);
-    return by_shape16(pool, group, [&]<typename T, int GG, int BB, class Pol>() {
-        return dec::prefix_launch<T, GG, BB, Pol>(pool.tmap_k_h2, pool.tmap_v_h2, p, smem, grid,
-                                                  stream);
+    return ptc::by_tc_shape(pool, group, [&]<typename T, int GG, int BB>() {
+        return ptc::prefix_tc_launch<T, GG, BB>(pool.tmap_k_swz, pool.tmap_v_swz, p, smem, grid,
+                                                stream);
     });
 }
 
+// Shared memory and grid of the prefix pass.  tcgen05 (16-bit pools): one CTA
+// per SM with the deepest K and V rings that fit (three tiles each, else
+// two).  mma.sync (8-bit pools): the ring depth with the most resident CTAs
+// x stages per consumer warp (counted up to 2), then the deepest.
 cudaError_t plan_prefix(const kv_pool& pool, int batch, int num_q_heads, int num_groups,
                         size_t base, PrefixPlan* pp) {
     const int G = num_q_heads / pool.num_kv_heads;
     const int D = pool.head_dim;
-    const PrefixTile tile = prefix_tile(pool);
-    const size_t stage = 2ull * tile.rows * D * tile.elt;
     int best_s = 0, best_occ = 0, best_score = -1;
     size_t best_smem = 0;
-    for (int S = dec::NCW; S <= 8 * dec::NCW; S += dec::NCW) {
-        if (S > dec::NCW && (size_t)S * stage > kMaxRingBytesP) break;
-        const size_t smem =
-            dec::PLayout(S, num_groups, tile.rows, D, tile.elt, tile.scales).total + 1024;
-        if (smem > kMaxSmemP) break;
-        int occ = 0;
-        cudaError_t e = prefix_attrs_any(pool, G, smem, &occ);
-        if (e != cudaSuccess) return e;
-        const int per_warp = S / dec::NCW > 2 ? 2 : S / dec::NCW;
-        if (occ >= 1 && occ * per_warp >= best_score) {
-            best_s = S;
-            best_occ = occ;
-            best_score = occ * per_warp;
-            best_smem = smem;
+    if (tc_prefix(pool)) {
+        for (int S = 3; S >= 2 && best_s == 0; --S) {
+            const size_t smem = ptc::TLayout(S, S, num_groups).total + 1024;
+            if (smem > kMaxSmemP) continue;
+            int occ = 0;
+            cudaError_t e = prefix_attrs_any(pool, G, smem, &occ);
+            if (e != cudaSuccess) return e;
+            if (occ >= 1) {
+                best_s = S;
+                best_occ = 1;
+                best_smem = smem;
+            }
+        }
+    } else {
+        // 32-row units of 128-byte code rows; INT8 adds the rows' scales
+        constexpr int rows = 32;
+        const bool scales = pool.cache_dtype == KV_INT8;
+        const size_t stage = 2ull * rows * D;
+        for (int S = dec::NCW; S <= 8 * dec::NCW; S += dec::NCW) {
+            if (S > dec::NCW && (size_t)S * stage > kMaxRingBytesP) break;
+            const size_t smem = dec::PLayout(S, num_groups, rows, D, 1, scales).total + 1024;
+            if (smem > kMaxSmemP) break;
+            int occ = 0;
+            cudaError_t e = prefix_attrs_any(pool, G, smem, &occ);
+            if (e != cudaSuccess) return e;
+            const int per_warp = S / dec::NCW > 2 ? 2 : S / dec::NCW;
+            if (occ >= 1 && occ * per_warp >= best_score) {
+                best_s = S;
+                best_occ = occ;
+                best_score = occ * per_warp;
+                best_smem = smem;
+            }
         }
     }
     if (best_s == 0) return cudaErrorNotSupported;

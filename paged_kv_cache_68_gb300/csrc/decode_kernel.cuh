@@ -1451,8 +1451,9 @@ __device__ __forceinline__ int block_excl_max(int v, int* scratch) {
 // A group (first member, members, shared leading blocks) is used when it lies
 // inside the batch, starts at or after the end of every earlier group, and at
 // least one work unit is shared (the block count is clamped to each member's
-// own block count, then counted in whole units of `ub` blocks: both passes
-// must use the same unit).  Both passes compact the used groups, in order,
+// count of full blocks -- blocks whose every row holds one of its tokens --
+// then counted in whole units of `ub` blocks: both passes must use the same
+// unit).  Both passes compact the used groups, in order,
 // into shared memory (vg: first[n], size[n], shared units[n]) and return n;
 // unused groups set KV_DEVERR_GROUP_RANGE when malformed.  Every thread of
 // the CTA calls.
@@ -1473,7 +1474,7 @@ __device__ __forceinline__ int load_groups(const int32_t* g_first, const int32_t
              first >= before;
         if (!ok) return 0;
         for (int m = 0; m < size; ++m)
-            blocks = min(blocks, (min(max(seq_lens[first + m], 0), cap) + bs - 1) / bs);
+            blocks = min(blocks, min(max(seq_lens[first + m], 0), cap) / bs);
         return blocks / ub;
     };
     int cmax = 0;
@@ -1580,8 +1581,9 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cap = p.max_blocks * bs;              // longest context a table can hold
-    // (cascade shapes have one block per unit; the host never pairs blocks there)
-    const bool cascade = UB == 1 && p.num_groups > 0;
+    // cascade: the groups' shared prefix is counted in whole units of UB
+    // blocks (load_groups), so paired-block units skip it like single ones
+    const bool cascade = p.num_groups > 0;
 
     // -- 1. the blocks-per-sequence prefix of the clamped lengths -----------
     if (tid == 0) {
@@ -1910,7 +1912,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) paged_decode_merge(const Params
     const int* prefix = reinterpret_cast<const int*>(smem + lay.prefix);
     const int* skip_s = reinterpret_cast<const int*>(smem + lay.skip);
     float* red = reinterpret_cast<float*>(smem + lay.pst);   // [NCW][NP][32][EPL + 2]
-    const bool cascade = UB == 1 && p.num_groups > 0;
+    const bool cascade = p.num_groups > 0;
     pdl_wait();                                    // the split kernel's partials are visible
     unit_prefix(p, smem, lay, bsu, cascade, false);
     __syncthreads();

@@ -1,20 +1,23 @@
-// Cascade (shared-prefix) decode, first pass: attention of many sequences'
-// queries over the KV blocks their tables share.
+// Cascade (shared-prefix) decode, first pass, for 8-bit pools: attention of
+// many sequences' queries over the KV blocks their tables share.
 //
 // Parallel samples or beams forked from one prompt point their block tables
 // at the same physical prefix blocks ("Lecture 3", semidirectx.com CS349D
 // notes, sec. 4.1; "Lecture 24", semidirectx.com CMU 11-868 notes, sec. 4.1).
 // Plain decode reads such a block once per sequence.  This pass reads it once
-// for a whole group: a unit is (group k, sub-group s, KV head g, prefix block
-// j), and the block's K/V tile is multiplied against the query rows of every
-// member of the sub-group at once -- up to 16 rows (members x G heads) on the
-// two N tiles of mma.sync m16n8k16.  For each member sequence b and head h the
-// pass leaves a normalised partial output and its log2-sum-exp ("prefix
-// state"); the second pass (the plain split kernel over each sequence's
-// remaining blocks) folds it into the final log-sum-exp merge, the same trick
-// the pages credit to Flash-Decoding ("Lecture 24", sec. 3.2) and that the S06
-// page names for vLLM's cascade path (llminference.xinbetween.com, "In
-// production").  The result equals plain decode up to fp32 rounding.
+// for a whole group: a unit is (group k, sub-group s, KV head g, 32 shared
+// tokens j), and the unit's K/V code tile is multiplied against the query rows
+// of every member of the sub-group at once -- up to 16 rows (members x G
+// heads) on the two N tiles of mma.sync m16n8k16, the codes turned into f16 in
+// registers.  For each member sequence b and head h the pass leaves a
+// normalised partial output and its log2-sum-exp ("prefix state"); the second
+// pass (the plain split kernel over each sequence's remaining blocks) folds it
+// into the final log-sum-exp merge, the same trick the pages credit to
+// Flash-Decoding ("Lecture 24", sec. 3.2) and that the S06 page names for
+// vLLM's cascade path (llminference.xinbetween.com, "In production").  The
+// result equals plain decode up to fp32 rounding.  (16-bit pools take the
+// tcgen05 pass of decode_prefix_tc.cuh; the two share the parameters, the
+// group tables, the partial slots and their merge, defined here.)
 //
 // The frame is the split kernel's: a persistent grid cut into equal unit
 // ranges, one TMA producer warp feeding a ring of 128-byte-swizzled tiles,
@@ -97,10 +100,11 @@ __device__ __forceinline__ int find_le(const int* a, int n, int u) {
     return lo;
 }
 
-// Tensor-core policy over up to 16 rows.  Lane roles as in TcPolicy: gid =
-// lane / 4, tig = lane % 4; on N tile nt the lane holds columns (rows of the
-// output) nt*8 + 2 tig + {0, 1}; column c is member c / G, head c % G.
-// PERM: the accumulators' dims are permuted (the 8-bit policy below).
+// The state of up to 16 query rows on mma.sync tiles, and its merge.  Lane
+// roles as in TcPolicy: gid = lane / 4, tig = lane % 4; on N tile nt the lane
+// holds columns (rows of the output) nt*8 + 2 tig + {0, 1}; column c is member
+// c / G, head c % G.  PERM: the accumulators' dims are permuted (as the 8-bit
+// policy below leaves them).  The policy supplies begin() and block().
 template <typename T, int D, int G, int BSC, bool PERM = false>
 struct TcRows {
     static_assert(sizeof(T) == 2 && BSC % 16 == 0 && (G == 1 || G == 2 || G == 4 || G == 8),
@@ -110,8 +114,6 @@ struct TcRows {
     static constexpr int MT = D / 16;
     static constexpr int TT = BSC / 16;
     static constexpr int kTileRows = BSC;          // token rows of a unit's tile
-    static constexpr bool kQ8 = false;             // 16-bit pool: one 4-D copy per tile
-    static constexpr bool kScales = false;         // no per-token scales
 
     // The output dim of accumulator oacc[mt][.][j + 2 hf] in the lane of row gid.
     __device__ static __forceinline__ int dim(int mt, int gid, int hf) {
@@ -122,172 +124,6 @@ struct TcRows {
     float oacc[MT][NT][4];
     float m_run[NT][2], l_run[NT][2];
     int lc[NT][2];                      // context length of the column's member (0: padding)
-
-    __device__ static __forceinline__ uint32_t swz(uint32_t tile, int r, int c) {
-        return tile + (uint32_t)((c >> 3) * BSC * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-    }
-
-    // members m0 .. m0 + msz - 1, KV head g
-    __device__ __forceinline__ void begin(const T* q, int m0, int msz, int g, int hq,
-                                          const int32_t* seq_lens, int cap, float, int lane) {
-        const int gid = lane >> 2, tig = lane & 3;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int row = nt * 8 + gid, m = row / G, h = row % G;
-            const T* qr = q + ((size_t)(m0 + m) * hq + g * G + h) * D;
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    qb[ks][nt][j] =
-                        m < msz ? __ldg(reinterpret_cast<const uint32_t*>(qr + ks * 16 + j * 8 + tig * 2))
-                                : 0u;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = nt * 8 + 2 * tig + j, mc = c / G;
-                lc[nt][j] = mc < msz ? min(max(seq_lens[m0 + mc], 0), cap) : 0;
-                m_run[nt][j] = -CUDART_INF_F;
-                l_run[nt][j] = 0.f;
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-                oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
-        }
-    }
-
-    __device__ __forceinline__ void block(const unsigned char* Ks, const unsigned char* Vs,
-                                          const float*, int jblk, float qscale, int lane) {
-        const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, r8 = lane & 7;
-        const uint32_t kbase = smem_u32(Ks), vbase = smem_u32(Vs);
-        int nv[NT][2], nvmax = 0;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                nv[nt][j] = min(BSC, lc[nt][j] - jblk * BSC);
-                nvmax = max(nvmax, nv[nt][j]);
-            }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) nvmax = max(nvmax, __shfl_xor_sync(FULL, nvmax, off));
-        if (nvmax < BSC) {
-            // rows no member reaches: P is 0 there, but 0 * NaN would poison the MMA
-            unsigned char* V = const_cast<unsigned char*>(Vs);
-            const int from = max(nvmax, 0);
-            const int nbytes = (BSC - from) * 128;
-            for (int i = lane * 16; i < nbytes; i += 32 * 16)
-#pragma unroll
-                for (int hf = 0; hf < D / 64; ++hf)
-                    *reinterpret_cast<uint4*>(V + hf * BSC * 128 + from * 128 + i) =
-                        make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async();
-            __syncwarp();
-        }
-        // -- S^T = K_blk Q^T over both N tiles --------------------------------
-        float s[TT][NT][4];
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-            // even and odd k-steps accumulate apart: two independent MMA chains
-            float acc[2][NT][4];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    acc[h2][nt][0] = acc[h2][nt][1] = acc[h2][nt][2] = acc[h2][nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(a, swz(kbase, tt * 16 + (mi & 1) * 8 + r8, ks * 2 + (mi >> 1)));
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    Mma<T>::run(acc[ks & 1][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-            }
-            const int t0 = tt * 16 + gid, t1 = t0 + 8;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                s[tt][nt][0] = t0 < nv[nt][0] ? (acc[0][nt][0] + acc[1][nt][0]) * qscale : -CUDART_INF_F;
-                s[tt][nt][1] = t0 < nv[nt][1] ? (acc[0][nt][1] + acc[1][nt][1]) * qscale : -CUDART_INF_F;
-                s[tt][nt][2] = t1 < nv[nt][0] ? (acc[0][nt][2] + acc[1][nt][2]) * qscale : -CUDART_INF_F;
-                s[tt][nt][3] = t1 < nv[nt][1] ? (acc[0][nt][3] + acc[1][nt][3]) * qscale : -CUDART_INF_F;
-            }
-        }
-        // -- online softmax per column ----------------------------------------
-        float alpha[NT][2], mnew[NT][2], lsum[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mx = -CUDART_INF_F;
-#pragma unroll
-                for (int tt = 0; tt < TT; ++tt) mx = fmaxf(mx, fmaxf(s[tt][nt][j], s[tt][nt][j + 2]));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
-                mnew[nt][j] = fmaxf(m_run[nt][j], mx);
-                alpha[nt][j] = mnew[nt][j] == -CUDART_INF_F ? 1.f : fast_exp2(m_run[nt][j] - mnew[nt][j]);
-                lsum[nt][j] = 0.f;
-            }
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = e & 1;
-                    const float pe = mnew[nt][j] == -CUDART_INF_F ? 0.f : fast_exp2(s[tt][nt][e] - mnew[nt][j]);
-                    s[tt][nt][e] = pe;
-                    lsum[nt][j] += pe;
-                }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                lsum[nt][j] += __shfl_xor_sync(FULL, lsum[nt][j], 4);
-                lsum[nt][j] += __shfl_xor_sync(FULL, lsum[nt][j], 8);
-                lsum[nt][j] += __shfl_xor_sync(FULL, lsum[nt][j], 16);
-                l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + lsum[nt][j];
-                m_run[nt][j] = mnew[nt][j];
-            }
-        // rescale the accumulators only when some running maximum moved
-        bool same = true;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) same = same && alpha[nt][0] == 1.f && alpha[nt][1] == 1.f;
-        if (!__all_sync(FULL, same))
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float2 a2 = make_float2(alpha[nt][0], alpha[nt][1]);
-                const float2 lo = __fmul2_rn(make_float2(oacc[mt][nt][0], oacc[mt][nt][1]), a2);
-                const float2 hi = __fmul2_rn(make_float2(oacc[mt][nt][2], oacc[mt][nt][3]), a2);
-                oacc[mt][nt][0] = lo.x; oacc[mt][nt][1] = lo.y;
-                oacc[mt][nt][2] = hi.x; oacc[mt][nt][3] = hi.y;
-            }
-        // -- O^T += V_blk^T P^T, P as hi + lo halves ---------------------------
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-            uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float* sv = s[tt][nt];
-                const uint32_t h01 = Mma<T>::pack(sv[0], sv[1]), h23 = Mma<T>::pack(sv[2], sv[3]);
-                const float2 f01 = Mma<T>::unpack(h01), f23 = Mma<T>::unpack(h23);
-                const uint32_t l01 = Mma<T>::pack(sv[0] - f01.x, sv[1] - f01.y);
-                const uint32_t l23 = Mma<T>::pack(sv[2] - f23.x, sv[3] - f23.y);
-                bh[nt][0] = movm_t(h01); bh[nt][1] = movm_t(h23);
-                bl[nt][0] = movm_t(l01); bl[nt][1] = movm_t(l23);
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint32_t a[4];
-                ldsm_x4_t(a, swz(vbase, tt * 16 + (mi >> 1) * 8 + r8, mt * 2 + (mi & 1)));
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    Mma<T>::run(oacc[mt][nt], a, bh[nt][0], bh[nt][1]);
-                    Mma<T>::run(oacc[mt][nt], a, bl[nt][0], bl[nt][1]);
-                }
-            }
-        }
-    }
 
     // Before the warp merge (the 8-bit policy's accumulators are scaled).
     __device__ __forceinline__ void finish() {}
@@ -377,7 +213,6 @@ struct Tc8Rows : TcRows<T, 128, G, 32, true> {
     using Base = TcRows<T, 128, G, 32, true>;
     static constexpr int NT = Base::NT, KS = Base::KS, MT = Base::MT, TT = Base::TT;
     static constexpr int kTileRows = 32;
-    static constexpr bool kQ8 = true;
     static constexpr bool kScales = FMT == kFmtInt8;
 
     float qinv[NT][2];    // 2^-e of the lane's score columns' query rows
@@ -654,8 +489,7 @@ __device__ __forceinline__ void merge_prefix_partials(const PParams& p, int seg_
                         });
 }
 
-// Pol: TcRows (16-bit pools; 4-D maps of both 64-dim halves) or Tc8Rows
-// (8-bit pools; 3-D swizzled maps of 128-byte code rows, UB blocks of BS
+// Pol: Tc8Rows (3-D swizzled maps of 128-byte code rows, UB blocks of BS
 // rows per unit).
 template <typename T, int D, int G, int BS, class Pol>
 __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
@@ -663,8 +497,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
     const PParams p) {
     constexpr int ROWS = Pol::kTileRows;            // token rows per unit
     constexpr int UB = ROWS / BS;                   // pool blocks per unit
-    static_assert(UB * BS == ROWS && (UB == 1 || Pol::kQ8), "unit shape");
-    constexpr int ELT = Pol::kQ8 ? 1 : (int)sizeof(T);
+    static_assert(UB * BS == ROWS, "unit shape");
+    constexpr int ELT = 1;                          // one code per element
     constexpr bool SCALES = Pol::kScales;
     constexpr int MS = kRows / G;                   // members per sub-group
     extern __shared__ unsigned char smem_raw[];
@@ -769,25 +603,19 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                         mbar_arrive_tx(fb, lay.tx_bytes);
                         const uint32_t dst = smem_u32(ring + (size_t)s * lay.stage_bytes);
                         const uint32_t vdst = dst + lay.stage_bytes / 2;
-                        if constexpr (Pol::kQ8) {
-                            // one 3-D copy per block: BS code rows of 128 bytes
+                        // one 3-D copy per block: BS code rows of 128 bytes
 #pragma unroll
-                            for (int x = 0; x < UB; ++x) {
-                                const int bid = x == 0 ? id : id2;
-                                tma_load_3d(dst + x * BS * 128, &tmap_k, 0, gg, bid * BS, fb);
-                                tma_load_3d(vdst + x * BS * 128, &tmap_v, 0, gg, bid * BS, fb);
-                                if constexpr (SCALES) {
-                                    // the unit's K scales [ROWS], then its V scales [ROWS]
-                                    const size_t srow = ((size_t)bid * H + gg) * BS;
-                                    const uint32_t sdst = smem_u32(sring + s * 2 * ROWS + x * BS);
-                                    bulk_load(sdst, p.k_scales + srow, BS * 4u, fb);
-                                    bulk_load(sdst + ROWS * 4u, p.v_scales + srow, BS * 4u, fb);
-                                }
+                        for (int x = 0; x < UB; ++x) {
+                            const int bid = x == 0 ? id : id2;
+                            tma_load_3d(dst + x * BS * 128, &tmap_k, 0, gg, bid * BS, fb);
+                            tma_load_3d(vdst + x * BS * 128, &tmap_v, 0, gg, bid * BS, fb);
+                            if constexpr (SCALES) {
+                                // the unit's K scales [ROWS], then its V scales [ROWS]
+                                const size_t srow = ((size_t)bid * H + gg) * BS;
+                                const uint32_t sdst = smem_u32(sring + s * 2 * ROWS + x * BS);
+                                bulk_load(sdst, p.k_scales + srow, BS * 4u, fb);
+                                bulk_load(sdst + ROWS * 4u, p.v_scales + srow, BS * 4u, fb);
                             }
-                        } else {
-                            // one 4-D copy per block: both 128-byte halves, [half][rows]
-                            tma_load_4d(dst, &tmap_k, 0, id * BS, 0, gg, fb);
-                            tma_load_4d(vdst, &tmap_v, 0, id * BS, 0, gg, fb);
                         }
                     } else {
                         valid[s] = 0;

@@ -72,6 +72,21 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
+def check_same_attention(a_raw: np.ndarray, b_raw: np.ndarray, dtype: str, what: str = ""):
+    """Two device results of the same attention (e.g. cascade and plain
+    decode), each within the tolerance of the exact value: they may differ by
+    twice the per-element bound -- 2e-3 each below |out| = 1, and for bf16
+    outputs of |out| >= 1 one ulp each (both are rounded once to bf16)."""
+    a, b = np_oracle.to_f64(a_raw, dtype), np_oracle.to_f64(b_raw, dtype)
+    lim = np.full(a.shape, 4e-3)
+    if dtype == "bf16":
+        big = np.maximum(np.abs(a), np.abs(b)) >= 1.0
+        lim[big] = np.maximum(lim[big], 2.0 * bf16_ulp(np.maximum(np.abs(a), np.abs(b))[big]))
+    diff = np.abs(a - b)
+    assert (diff <= lim).all(), f"{what}: results differ by {diff.max():.3e}"
+    return float(diff.max())
+
+
 def check_attention(out_raw: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
     got = np_oracle.to_f64(out_raw, dtype)
     assert got.shape == ref.shape, (got.shape, ref.shape)

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity import check_attention, oracle_step
+from parity import check_attention, check_same_attention, oracle_step
 from oracle import np_oracle
 from paged_kv_cache_68_gb300 import pagedkv
 from paged_kv_cache_68_gb300 import workloads as wl
@@ -48,8 +48,7 @@ def _check(w, groups, what):
     _, _, ref = oracle_step(w)
     rep = check_attention(out, ref, w.dtype, what)
     plain, _ = _run(w, groups, cascade=False)
-    diff = np.abs(np_oracle.to_f64(out, w.dtype) - np_oracle.to_f64(plain, w.dtype)).max()
-    assert diff <= 4e-3, f"{what}: cascade and plain decode differ by {diff:.3e}"
+    check_same_attention(out, plain, w.dtype, f"{what}: cascade vs plain decode")
     return rep
 
 

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 from oracle import np_oracle
-from parity import check_attention, gpu_step_q8, oracle_step_q8
+from parity import check_attention, check_same_attention, gpu_step_q8, oracle_step_q8
 from paged_kv_cache_68_gb300 import pagedkv
 from paged_kv_cache_68_gb300 import workloads as wl
 
@@ -40,8 +40,7 @@ def _check(w, cache, groups, sk=1.0, sv=1.0, seed=5, what="", p=None):
     rep = check_attention(out, ref, w.dtype, what)
     _, _, _, _, plain, err2 = gpu_step_q8(w, p, return_pools=False)
     assert err2 == 0
-    diff = np.abs(np_oracle.to_f64(out, w.dtype) - np_oracle.to_f64(plain, w.dtype)).max()
-    assert diff <= 4e-3, f"{what}: cascade and plain decode differ by {diff:.3e}"
+    check_same_attention(out, plain, w.dtype, f"{what}: cascade vs plain decode")
     return rep
 
 
@@ -112,3 +111,67 @@ def test_q8_cascade_int8_v_scales_zero_then_jump():
         vs[bt[first, blocks // 2]] *= 100.0
     p.v_scales = vs
     print(_check(w, "int8", w.groups, what="int8 v scales", p=p))
+
+
+def _effective(w, member, first, covered):
+    """The workload with `member`'s first `covered` table entries replaced by
+    those of `first` (the blocks the shared-prefix pass attends for it)."""
+    h = wl.on_host(w)
+    t = np.array(h.block_tables, copy=True)
+    t[member, :covered] = t[first, :covered]
+    h.block_tables = t
+    return h
+
+
+@pytest.mark.parametrize("cache", ["bf16", "fp8_e4m3", "int8"])
+def test_cascade_second_pass_skips_exactly_the_prefix(cache):
+    """The prefix pass attends the shared blocks through the group's first
+    member's table; the second pass must start after them.  Member 1's shared
+    entries are pointed at the other prompt's blocks: its cascade output must
+    be attention over the first member's prefix and its own suffix (which
+    plain decode of the same tables is not), so a second pass that re-read
+    the prefix, or skipped a different count, fails.  40 full blocks of 16
+    are shared: whole units for both the 16-bit (one block per unit) and the
+    8-bit (two) second pass."""
+    w = wl.shared_prefix(47, prompts=2, prompt_len=640, n=4, max_divergent=40)
+    assert (np.asarray(w.groups)[:, 2] == 40).all()
+    h = wl.on_host(w)
+    t = np.array(h.block_tables, copy=True)
+    t[1, :40] = t[4, :40]                      # member 1 now reads prompt 1's blocks
+    h.block_tables = t
+    eff = _effective(h, 1, 0, 40)              # what the cascade must attend for member 1
+    if cache == "bf16":
+        dev = torch.device("cuda")
+        tv = lambda a: wl.value_to_torch(a, h.dtype, dev)
+        outs = []
+        for cascade in (True, False):
+            pool = pagedkv.KVPool(tv(h.k_pool).clone(), tv(h.v_pool).clone())
+            try:
+                pool.copy_blocks(torch.from_numpy(np.ascontiguousarray(h.pairs, dtype=np.int32)).to(dev))
+                pool.append(tv(h.k_new), tv(h.v_new), torch.from_numpy(h.slot_mapping).to(dev))
+                tables = torch.from_numpy(np.ascontiguousarray(h.block_tables)).to(dev)
+                lens = torch.from_numpy(h.seq_lens).to(dev)
+                if cascade:
+                    g = torch.from_numpy(np.ascontiguousarray(h.groups, dtype=np.int32)).to(dev)
+                    out = pool.decode_cascade(tv(h.q), tables, lens, h.scale, g)
+                else:
+                    out = pool.decode(tv(h.q), tables, lens, h.scale)
+                torch.cuda.synchronize()
+                assert pool.get_error() == 0
+                outs.append(wl.value_to_numpy(out, h.dtype))
+            finally:
+                pool.close()
+        from parity import oracle_step
+        _, _, ref = oracle_step(eff)
+        got, plain = outs
+    else:
+        p = wl.q8_pools(h, cache, 8)
+        _, _, _, _, got, err = gpu_step_q8(h, p, return_pools=False, groups=h.groups)
+        assert err == 0
+        _, _, _, _, plain, err = gpu_step_q8(h, p, return_pools=False)
+        assert err == 0
+        _, _, _, _, ref = oracle_step_q8(eff, p)
+    check_attention(got, ref, h.dtype, f"{cache} cascade with member 1's prefix from member 0")
+    g64 = np_oracle.to_f64(got, h.dtype)[1]
+    p64 = np_oracle.to_f64(plain, h.dtype)[1]
+    assert np.abs(g64 - p64).max() > 1e-2, "member 1's output does not depend on the prefix pass"

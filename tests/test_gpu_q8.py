@@ -170,8 +170,10 @@ def test_q8_host_argument_errors():
 
 
 def test_q8_cascade_call_decodes_plainly():
-    """The cascade entry point on an 8-bit pool gives the plain decode's bits."""
-    w = wl.shared_prefix(3, prompts=2, prompt_len=300, n=4, max_divergent=30)
+    """The cascade entry point on an 8-bit pool of a shape without a prefix
+    pass (block size 64) gives the plain decode's bits."""
+    w = wl.shared_prefix(3, prompts=2, prompt_len=300, n=4, max_divergent=30, block_size=64)
+    assert (np.asarray(w.groups)[:, 2] > 0).all()
     p = wl.q8_pools(w, "int8", 1)
     dev = torch.device("cuda")
     tv = lambda a: wl.value_to_torch(a, w.dtype, dev)
