@@ -791,7 +791,17 @@ def run_prefill(args):
         view[n] = dev_in[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
         view[n].copy_(t)
     host_in = dev_in.cpu().pin_memory()
-    pool = pagedkv.KVPool(w.k_pool, w.v_pool)
+    q8 = None
+    if args.kv_cache:
+        # the same rows as 8-bit codes (the 16-bit pools are not used)
+        q8 = wl.q8_pools(w, args.kv_cache, args.seed)
+        w.k_pool = w.v_pool = None
+        torch.cuda.empty_cache()
+        pool = pagedkv.KVPool(q8.k_codes, q8.v_codes, cache=q8.cache, dtype=view["q"].dtype,
+                              k_scales=q8.k_scales, v_scales=q8.v_scales, k_scale=q8.k_scale,
+                              v_scale=q8.v_scale)
+    else:
+        pool = pagedkv.KVPool(w.k_pool, w.v_pool)
     out = torch.empty_like(view["q"])
     maxq = int(np.diff(w.cu_seqlens).max())
 
@@ -856,7 +866,7 @@ def run_prefill(args):
     achieved = flops / (pf_ms * 1e-3) / 1e12
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and q8 is None:
         host_w = wl.on_host(w)
         threads = os.cpu_count() or 1
         reqs = pick_prefill_sample(host_w, 10.0, threads)
@@ -875,8 +885,11 @@ def run_prefill(args):
         "metric": PREFILL_METRIC, "value": round(total_flops / (max_step_ms * 1e-3) / 1e12, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(max_step_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": prefill_config(args, w, world, flops),
+        "vs_baseline": None,
+        "dtype": w.dtype if q8 is None else f"{q8.cache} storage, {w.dtype} MMA, fp32 softmax",
+        "data": "synthetic",
+        "config": {**prefill_config(args, w, world, flops),
+                   "kv_cache": w.dtype if q8 is None else q8.cache},
         "query_tokens_per_s": round(qtok / (max_step_ms * 1e-3), 1),
         "attention_tflops": round(total_flops / (max_pf_ms * 1e-3) / 1e12, 2),
         "roofline": {"bound": "tensor",
@@ -885,7 +898,7 @@ def run_prefill(args):
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind} (bf16 burst)",
                      "traffic": (profiled_traffic("paged_prefill/chunked_prefill/bf16", PREFILL_SOURCE)
                                  if args.batch is None and args.chunk is None and not args.decodes
-                                 and args.seed == 0 else None),
+                                 and args.seed == 0 and q8 is None else None),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
                      "algorithmic_flops": flops},
         "e2e": {"value": round(total_flops / (max_e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

@@ -323,8 +323,9 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
  * iteration and a chunk attends to the cached earlier chunks through the
  * block table, as decode does).
  *
- * q, out: device [num_tokens, num_q_heads, head_dim] of the pool dtype; the
- *   queries of request b are rows cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ * q, out: device [num_tokens, num_q_heads, head_dim] of the pool dtype (the
+ *   query type of an 8-bit pool); the queries of request b are rows
+ *   cu_seqlens[b] .. cu_seqlens[b+1]-1.
  * cu_seqlens: device int32 [batch + 1], non-decreasing, cu_seqlens[batch] <=
  *   num_tokens.  C_b = cu_seqlens[b+1] - cu_seqlens[b] queries for request b.
  * seq_lens: device int32 [batch]: L_b, the request's context length counted
@@ -338,9 +339,13 @@ kv_status paged_attention_decode_cascade(kv_pool_t pool, const void* q, void* ou
  * scale: > 0 and finite.  Arithmetic: fp32 scores and softmax on the tensor
  *   cores (products of 16-bit inputs, fp32 accumulation; the probabilities
  *   enter the second product as two 16-bit halves, so they keep fp32-level
- *   accuracy); one rounding of each output to the pool dtype.
- * Limits: 16-bit pools (KV_F16 or KV_BF16; not 8-bit pools), head_dim 128,
- *   block_size a power of two in [8, 128], num_q_heads / num_kv_heads in
+ *   accuracy); one rounding of each output to the pool dtype.  8-bit pools:
+ *   the codes are turned exactly into the query type in shared memory; FP8
+ *   scales the scores by k_scale and the output by v_scale, INT8 each token's
+ *   scores by its K scale and its probability by its V scale (all in fp32),
+ *   so the result is attention over the dequantised values.
+ * Limits: 16-bit and 8-bit pools, head_dim 128, block_size a power of two in
+ *   [8, 128] (8-bit pools: [16, 128]), num_q_heads / num_kv_heads in
  *   {1, 2, 4, 8}, batch <= 65535.  num_tokens = 0 is a no-op.
  * Needs no workspace.  Output rows of queries that no request covers are not
  *   written.

@@ -333,6 +333,48 @@ def decode_q8(q, in_dtype: str, k_codes, v_codes, k_scales, v_scales, fmt: str,
     return out
 
 
+
+def prefill_q8(q, in_dtype: str, k_codes, v_codes, k_scales, v_scales, fmt: str, cu_seqlens,
+               block_tables, seq_lens, scale: float, num_kv_heads: int, fp8_k_scale: float = 1.0,
+               fp8_v_scale: float = 1.0) -> np.ndarray:
+    """Chunked-prefill attention over an 8-bit pool: the pool's values are the
+    dequantised codes ("Part 3: single node", ch. 10: the reader turns them
+    back into wider numbers), then the definition of ``prefill`` ("Part 3",
+    ch. 13 sec. 1-2): request b's C_b queries sit at positions L_b - C_b + i
+    and attend causally to positions 0 .. L_b - C_b + i of its cache."""
+    T, Hq, D = q.shape
+    if Hq % num_kv_heads:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    group = Hq // num_kv_heads
+    bs = k_codes.shape[1]
+    qf = to_f64(q, in_dtype)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        C = int(cu[b + 1] - cu[b])
+        L = int(seq_lens[b])
+        if C <= 0 or L <= 0:
+            continue
+        ids = np.asarray(block_tables[b][: -(-L // bs)], dtype=np.int64)
+        if np.any((ids < 0) | (ids >= k_codes.shape[0])):
+            raise ValueError("block table names a block outside the pool")
+        K = dequantize(k_codes[ids], None if k_scales is None else k_scales[ids], fmt,
+                       fp8_k_scale).reshape(-1, num_kv_heads, D)[:L]
+        V = dequantize(v_codes[ids], None if v_scales is None else v_scales[ids], fmt,
+                       fp8_v_scale).reshape(-1, num_kv_heads, D)[:L]
+        for i in range(C):
+            pos = L - C + i                                                 # query position
+            if pos < 0:
+                continue
+            for g in range(num_kv_heads):
+                heads = slice(g * group, (g + 1) * group)
+                s = scale * (qf[cu[b] + i, heads] @ K[:pos + 1, g, :].T)   # [group, pos + 1]
+                s = s - s.max(axis=1, keepdims=True)
+                w = np.exp(s)
+                w = w / w.sum(axis=1, keepdims=True)
+                out[cu[b] + i, heads] = w @ V[:pos + 1, g, :]
+    return out
+
 # ------------------------------------------------------- swap to host ----
 #
 # "Lecture 3" (semidirectx.com, CS349D notes), sec. 5.2 and "Part 3: single

@@ -50,6 +50,16 @@
 // Every mbarrier wait is bounded; a wait that gives up sets KV_DEVERR_TIMEOUT,
 // raises the CTA's abort flag, and the CTA drains its copies and MMAs, frees
 // TMEM and exits.
+//
+// 8-bit pools (FMT >= 0: FP8 E4M3 with one K and one V scale per pool, INT8
+// with a scale per token and head).  The producers land a tile's code rows
+// (128 bytes each) in a ring of their own and turn them into the query type
+// in the K / V ring (E4M3 and INT8 codes convert to f16 exactly, and f16
+// values of 8 significant bits to bf16 exactly), so the MMAs run as for
+// 16-bit pools.  FP8: the K scale multiplies the scores (with the softmax
+// scale), the V scale the output.  INT8: the producers also copy the tile's
+// token scales to a ring the softmax reads: K scales multiply the scores'
+// columns, V scales P's columns before the hi / lo split.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -89,6 +99,13 @@ constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = BAR_KF + KST, BAR_VF = BAR_KE + KS
               BAR_VE = BAR_VF + VST, BAR_STREAM = BAR_VE + VST;
 constexpr int SB_SF = 0, SB_SR = 1, SB_PF = 2, SB_OF = 3, SB_DR = 4, SB_N = 5;
 constexpr int NBARS = BAR_STREAM + 2 * SB_N;
+// 8-bit pools: then the K and V code rings' full barriers, and the INT8
+// scale ring's full / empty barriers
+constexpr int CST = 2;                            // code tiles per ring
+constexpr uint32_t CTILE = (uint32_t)BN * 128u;   // a tile's code rows: 64 x 128 B
+constexpr int SCS = 4;                            // INT8 scale ring depth
+constexpr int BAR_CK = NBARS, BAR_CV = BAR_CK + CST, BAR_SCF = BAR_CV + CST,
+              BAR_SCE = BAR_SCF + SCS, NBARS_Q8 = BAR_SCE + SCS;
 // launch order: the requests' costs (up to kMaxRanked of them) and the
 // request this CTA takes
 constexpr int kMaxRanked = 256;
@@ -96,6 +113,25 @@ constexpr uint32_t OFF_ORDER = OFF_BAR + 8u * NBARS;
 constexpr uint32_t OFF_TMEM = OFF_ORDER + 4u * (kMaxRanked + 4);
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4u;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4u + 1024u;   // + slack to align the base to 1 KB
+
+// The layout of one CTA's shared memory: as above for 16-bit pools; 8-bit
+// pools add the code rings (and the INT8 scale ring: K then V scales of a
+// tile, 64 each) after the V ring.
+template <bool Q8>
+struct Lay {
+    static constexpr uint32_t ck = OFF_V + VST * KVTILE;
+    static constexpr uint32_t cv = ck + (Q8 ? CST * CTILE : 0u);
+    static constexpr uint32_t sc = cv + (Q8 ? CST * CTILE : 0u);       // [SCS][K, V][BN]
+    static constexpr uint32_t csc = sc + (Q8 ? SCS * 2u * BN * 4u : 0u); // [K, V][CST][BN]
+    static constexpr uint32_t bar = csc + (Q8 ? 2u * CST * BN * 4u : 0u);
+    static constexpr int nbars = Q8 ? NBARS_Q8 : NBARS;
+    static constexpr uint32_t order = bar + 8u * nbars;
+    static constexpr uint32_t tmem = order + 4u * (kMaxRanked + 4);
+    static constexpr uint32_t abort_flag = tmem + 4u;
+    static constexpr uint32_t bytes = abort_flag + 4u + 1024u;
+};
+static_assert(Lay<false>::bytes == SMEM_BYTES, "16-bit layout");
+static_assert(Lay<true>::bytes <= 227u * 1024u, "8-bit layout fits");
 
 struct Params {
     const void* q;                // [T, Hq, D]
@@ -112,7 +148,11 @@ struct Params {
     int bs;
     int max_q;                    // the largest C_b the grid covers
     int box_rows;                 // rows of one K/V box: min(bs, BN)
-    float qscale;                 // scale * log2(e), > 0
+    float qscale;                 // scale * log2(e) (* the FP8 K scale), > 0
+    float vscale;                 // FP8: the pool's V scale; 1 otherwise
+    const float* k_scales;        // INT8: [num_blocks][num_kv_heads][bs]
+    const float* v_scales;
+    int num_kv_heads;
     unsigned long long wait_ns;   // limit of one pipeline wait (the pool's setting)
 };
 
@@ -258,6 +298,27 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 
+// 16 codes (one 16-byte chunk, FMT a dec:: code format) -> 16 values of T
+// (two 16-byte chunks): E4M3 and INT8 codes convert to f16 exactly, and an
+// f16 of at most 8 significant bits converts to bf16 exactly.
+template <typename T, int FMT>
+__device__ __forceinline__ void codes_to(uint4 c, uint4& lo, uint4& hi) {
+    uint32_t o[8];
+    dec::cvt4<FMT>(c.x, o[0], o[1]);
+    dec::cvt4<FMT>(c.y, o[2], o[3]);
+    dec::cvt4<FMT>(c.z, o[4], o[5]);
+    dec::cvt4<FMT>(c.w, o[6], o[7]);
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[i]));
+            o[i] = H16<__nv_bfloat16>::pack(f.x, f.y);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Bounded wait (limit_ns); on expiry (or when another role already gave up)
 // raise the abort flag and return false.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -271,19 +332,24 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     return false;
 }
 
-template <typename T, int G>
+// FMT: -1 for 16-bit pools (of type T), else the 8-bit pool's code format
+// (T is then the queries' type); the K / V maps address code rows.
+template <typename T, int G, int FMT = -1>
 __global__ void __launch_bounds__(NTHREADS, 1)
     paged_prefill(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+    constexpr bool Q8 = FMT >= 0;
+    constexpr bool SCALES = FMT == dec::kFmtInt8;
+    using LY = Lay<Q8>;
     constexpr int QT = BM / G;                    // queries per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = dec::smem_align_1k(smem_raw);
     const uint32_t sbase = dec::smem_u32(smem);
-    auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
+    auto bar = [&](int i) { return sbase + LY::bar + 8u * (uint32_t)i; };
     auto sbar = [&](int x, int i) { return bar(BAR_STREAM + x * SB_N + i); };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::abort_flag);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::tmem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.bs;
@@ -300,7 +366,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int b = blockIdx.z, g = blockIdx.y;
     int pt = (int)gridDim.x - 1 - (int)blockIdx.x;
     if (p.batch <= kMaxRanked) {
-        int* cost = reinterpret_cast<int*>(smem + OFF_ORDER);
+        int* cost = reinterpret_cast<int*>(smem + LY::order);
         int* pick = cost + kMaxRanked;
         const int k = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
         const int per_req = (int)(gridDim.x * gridDim.y);
@@ -348,12 +414,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // -- set-up: barriers, TMEM ----------------------------------------------
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) {
+        for (int i = 0; i < LY::nbars; ++i) {
             uint32_t count = 1;
             if ((i >= BAR_KE && i < BAR_KE + KST) || (i >= BAR_VE && i < BAR_VE + VST))
                 count = (uint32_t)nstreams;
-            if (i >= BAR_STREAM && ((i - BAR_STREAM) % SB_N == SB_SR || (i - BAR_STREAM) % SB_N == SB_PF))
+            if (i >= BAR_STREAM && i < NBARS &&
+                ((i - BAR_STREAM) % SB_N == SB_SR || (i - BAR_STREAM) % SB_N == SB_PF))
                 count = NSOFT;
+            // INT8 scale ring: written by both producers, read by every softmax warp
+            if (i >= BAR_SCF && i < BAR_SCF + SCS) count = 2;
+            if (i >= BAR_SCE && i < BAR_SCE + SCS) count = (uint32_t)(NSOFT * nstreams);
             dec::mbar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -361,7 +431,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (warp == WARP_MMA) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         sbase + OFF_TMEM),
+                         sbase + LY::tmem),
                      "r"(TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -391,42 +461,132 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             const int32_t* table = p.block_tables + (size_t)b * p.max_blocks;
-            int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const int slot = j % nst;
-                bool ok = true;
-                // tile j reuses the buffer of tile j - nst: freed when every
-                // stream's S (K) or PV (V) of that tile is done
-                if (lane == 0 && j >= nst)
-                    ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err,
-                                       p.wait_ns);
-                if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
-                const int t = j * BN + lane * R;   // first token of this lane's box
-                int row = -1;
-                bool load = false;
-                if (lane < nbox && t < L) {
-                    const int id = table[t / bs];
-                    load = id >= 0 && id < p.num_blocks;
-                    if (!load && is_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-                    row = id * bs + t % bs;
+            if constexpr (Q8) {
+                // Tile jj's code rows land in code stage jj % CST (INT8: its
+                // token scales beside them); tile j is converted into ring
+                // slot j % nst, which then counts as full.
+                const uint32_t code0 = sbase + (is_k ? LY::ck : LY::cv);
+                const int cfull0 = is_k ? BAR_CK : BAR_CV;
+                float* csc = reinterpret_cast<float*>(smem + LY::csc) + (is_k ? 0 : CST * BN);
+                const float* gsc = is_k ? p.k_scales : p.v_scales;
+                int codes_issued = 0;
+                auto issue_codes = [&](int jj) {
+                    const int t = jj * BN + lane * R;   // first token of this lane's box
+                    int row = -1, id = -1;
+                    bool load = false;
+                    if (lane < nbox && t < L) {
+                        id = table[t / bs];
+                        load = id >= 0 && id < p.num_blocks;
+                        if (!load && is_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                        row = id * bs + t % bs;
+                    }
+                    const unsigned mask = __ballot_sync(FULL, load);
+                    const uint32_t cb = bar(cfull0 + jj % CST);
+                    const uint32_t per_box = (uint32_t)R * 128u + (SCALES ? (uint32_t)R * 4u : 0u);
+                    if (lane == 0) dec::mbar_arrive_tx(cb, (uint32_t)__popc(mask) * per_box);
+                    __syncwarp();
+                    if (load) {
+                        dec::tma_load_3d(code0 + (uint32_t)(jj % CST) * CTILE + (uint32_t)lane * R * 128u,
+                                         map, 0, g, row, cb);
+                        if constexpr (SCALES) {
+                            const size_t srow = ((size_t)id * p.num_kv_heads + g) * bs + t % bs;
+                            dec::bulk_load(dec::smem_u32(csc + (jj % CST) * BN + lane * R), gsc + srow,
+                                           (uint32_t)R * 4u, cb);
+                        }
+                    }
+                    codes_issued = jj + 1;
+                };
+                for (int jj = 0; jj < min(CST, ntiles); ++jj) issue_codes(jj);
+                for (int j = 0; j < ntiles; ++j) {
+                    const int slot = j % nst, cs = j % CST;
+                    bool ok = true;
+                    if (lane == 0 && j >= nst)
+                        ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err,
+                                           p.wait_ns);
+                    if (lane == 0 && ok)
+                        ok = wait_or_abort(bar(cfull0 + cs), (j / CST) & 1, abort_flag, p.err, p.wait_ns);
+                    if (SCALES && lane == 0 && ok && j >= SCS)
+                        ok = wait_or_abort(bar(BAR_SCE + j % SCS), (j / SCS - 1) & 1, abort_flag, p.err,
+                                           p.wait_ns);
+                    if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
+                    // lane: token rows lane and lane + 32; code chunk c (dims 16 c ..)
+                    // -> 64-dim half c / 4, its 16-byte chunks 2 (c % 4) and + 1
+                    const unsigned char* crows = smem + (is_k ? LY::ck : LY::cv) + (uint32_t)cs * CTILE;
+                    unsigned char* orows = smem + (is_k ? OFF_K : OFF_V) + (uint32_t)slot * KVTILE;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int r = lane + 32 * rr;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(crows + r * 128 + ((c ^ (r & 7)) << 4));
+                            uint4 lo, hi;
+                            codes_to<T, FMT>(w, lo, hi);
+                            unsigned char* h = orows + (c >> 2) * KVHALF + r * 128;
+                            const int c0 = 2 * (c & 3);
+                            *reinterpret_cast<uint4*>(h + ((c0 ^ (r & 7)) << 4)) = lo;
+                            *reinterpret_cast<uint4*>(h + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+                        }
+                    }
+                    if constexpr (SCALES) {
+                        float* ring = reinterpret_cast<float*>(smem + LY::sc) + (j % SCS) * 2 * BN +
+                                      (is_k ? 0 : BN);
+                        ring[lane] = csc[cs * BN + lane];
+                        ring[lane + 32] = csc[cs * BN + lane + 32];
+                    }
+                    dec::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        dec::mbar_arrive(bar(full0 + slot));
+                        if constexpr (SCALES) dec::mbar_arrive(bar(BAR_SCF + j % SCS));
+                    }
+                    // the code stage is free: tile j + CST's codes into it
+                    if (j + CST < ntiles) issue_codes(j + CST);
                 }
-                const unsigned mask = __ballot_sync(FULL, load);
-                if (lane == 0)
-                    dec::mbar_arrive_tx(bar(full0 + slot), (uint32_t)__popc(mask) * 2u * box_bytes);
-                __syncwarp();
-                if (load) {
-                    const uint32_t d = buf0 + (uint32_t)slot * KVTILE + (uint32_t)lane * box_bytes;
-                    dec::tma_load_3d(d, map, 0, g, row, bar(full0 + slot));
-                    dec::tma_load_3d(d + KVHALF, map, 64, g, row, bar(full0 + slot));
+                // Drain: no copy may still be landing in shared memory at exit.
+                if (lane == 0) {
+                    bool ok = !is_k || dec::mbar_wait(bar(BAR_Q), 0);
+                    for (int jj = max(0, codes_issued - CST); jj < codes_issued; ++jj)
+                        ok &= dec::mbar_wait(bar(cfull0 + jj % CST), (jj / CST) & 1);
+                    if (!ok) atomicOr(p.err, KV_DEVERR_TIMEOUT);
                 }
-                issued = j + 1;
-            }
-            // Drain: no copy may still be landing in shared memory at exit.
-            if (lane == 0) {
-                bool ok = !is_k || dec::mbar_wait(bar(BAR_Q), 0);
-                for (int j = max(0, issued - nst); j < issued; ++j)
-                    ok &= dec::mbar_wait(bar(full0 + j % nst), (j / nst) & 1);
-                if (!ok) atomicOr(p.err, KV_DEVERR_TIMEOUT);
+            } else {
+                int issued = 0;
+                for (int j = 0; j < ntiles; ++j) {
+                    const int slot = j % nst;
+                    bool ok = true;
+                    // tile j reuses the buffer of tile j - nst: freed when every
+                    // stream's S (K) or PV (V) of that tile is done
+                    if (lane == 0 && j >= nst)
+                        ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err,
+                                           p.wait_ns);
+                    if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
+                    const int t = j * BN + lane * R;   // first token of this lane's box
+                    int row = -1;
+                    bool load = false;
+                    if (lane < nbox && t < L) {
+                        const int id = table[t / bs];
+                        load = id >= 0 && id < p.num_blocks;
+                        if (!load && is_k) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                        row = id * bs + t % bs;
+                    }
+                    const unsigned mask = __ballot_sync(FULL, load);
+                    if (lane == 0)
+                        dec::mbar_arrive_tx(bar(full0 + slot), (uint32_t)__popc(mask) * 2u * box_bytes);
+                    __syncwarp();
+                    if (load) {
+                        const uint32_t d = buf0 + (uint32_t)slot * KVTILE + (uint32_t)lane * box_bytes;
+                        dec::tma_load_3d(d, map, 0, g, row, bar(full0 + slot));
+                        dec::tma_load_3d(d + KVHALF, map, 64, g, row, bar(full0 + slot));
+                    }
+                    issued = j + 1;
+                }
+                // Drain: no copy may still be landing in shared memory at exit.
+                if (lane == 0) {
+                    bool ok = !is_k || dec::mbar_wait(bar(BAR_Q), 0);
+                    for (int j = max(0, issued - nst); j < issued; ++j)
+                        ok &= dec::mbar_wait(bar(full0 + j % nst), (j / nst) & 1);
+                    if (!ok) atomicOr(p.err, KV_DEVERR_TIMEOUT);
+                }
             }
         }
     } else if (warp >= WARP_MMA) {
@@ -533,6 +693,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) dec::mbar_arrive(sbar(x, SB_SR));   // S may be overwritten
+            // INT8: the tile's token scales (K, then V), released once P is built
+            const float* tsc = reinterpret_cast<const float*>(smem + LY::sc) + (j % SCS) * 2 * BN;
+            if constexpr (SCALES) {
+                ok = wait_warp(bar(BAR_SCF + j % SCS), (j / SCS) & 1);
+                if (!ok) break;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        sv[c][e] = __float_as_uint(__uint_as_float(sv[c][e]) * tsc[32 * c + e]);
+            }
             // causal / length mask: tokens past `lim` do not exist for this row
             if (t0 + BN - 1 > lim) {
 #pragma unroll
@@ -572,8 +743,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         nmu2);
                     const float2 pp = make_float2(dec::fast_exp2(xx.x), dec::fast_exp2(xx.y));
                     l2[(e >> 1) & 1] = __fadd2_rn(l2[(e >> 1) & 1], pp);
-                    H16<T>::split(pp.x, pp.y, ph[16 * c + e / 2], pl[16 * c + e / 2]);
+                    float2 pv = pp;
+                    if constexpr (SCALES) {
+                        // P times the token's V scale (0 where P is: masked
+                        // tokens' scales may be anything)
+                        const float v0 = tsc[BN + 32 * c + e], v1 = tsc[BN + 32 * c + e + 1];
+                        pv = make_float2(pp.x > 0.f ? pp.x * v0 : 0.f, pp.y > 0.f ? pp.y * v1 : 0.f);
+                    }
+                    H16<T>::split(pv.x, pv.y, ph[16 * c + e / 2], pl[16 * c + e / 2]);
                 }
+            if constexpr (SCALES) {
+                __syncwarp();                     // every lane has read the tile's scales
+                if (lane == 0) dec::mbar_arrive(bar(BAR_SCE + j % SCS));
+            }
             // the last tile: zero V rows past the sequence end (P is 0 there,
             // but 0 x NaN from an unwritten row would poison the product);
             // each stream zeroes before its own PV (both write the same zeros)
@@ -621,7 +803,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (have_o) tc_fence_after();
         const float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
         const bool done = have_o || (ok && ntiles == 0);
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? p.vscale / l : 0.f;   // FP8: the pool's V scale
         T* orow = static_cast<T*>(p.out) +
                   ((size_t)(cu0 + q0 + x * QT + qi) * p.num_q_heads + (size_t)g * G + hh) * D;
 #pragma unroll

@@ -313,3 +313,57 @@ def test_q8_pins_pass_on_the_oracle():
 @pytest.mark.parametrize("name", sorted(Q8_MUTATIONS))
 def test_q8_pins_catch_planted_mistake(name):
     assert not _pins_pass(_q8_mutant(name)), f"mutant {name} passed every pin"
+
+
+# -- chunked prefill over an 8-bit pool -----------------------------------------
+
+@pytest.mark.parametrize("fmt, sk, sv", FMTS)
+def test_prefill_q8_equals_16bit_prefill_on_dequantised_pool(c_oracle, fmt, sk, sv):
+    """Reduction to the pinned prefill oracle: with power-of-two FP8 scales the
+    dequantised values are exact in fp32, so an fp32 pool holding them gives
+    the same output; INT8 (code * fp32 scale needs more than fp32) is checked
+    against the causal definition written out in fp64."""
+    lens = [7, 1, 12, 5]
+    s = _q8_setup(fmt, "f16", 6, lens)
+    sk2, sv2 = (0.5, 2.0) if fmt == "fp8_e4m3" else (sk, sv)
+    c_oracle.append_q8(s["kc"], s["vc"], s["ks"], s["vs"], s["kx"], s["vx"], "f16", s["slots"],
+                       fmt, sk2, sv2)
+    rng = np.random.default_rng(7)
+    C = [3, 1, 12, 2]                                    # queries: the last C_b positions
+    cu = np.concatenate([[0], np.cumsum(C)]).astype(np.int32)
+    q = wl.from_f32(rng.standard_normal((int(cu[-1]), 8, s["d"])).astype(np.float32), "f16")
+    out = npo.prefill_q8(q, "f16", s["kc"], s["vc"], s["ks"], s["vs"], fmt, cu, s["tables"],
+                         s["lens"], 0.3, s["hkv"], fp8_k_scale=sk2, fp8_v_scale=sv2)
+    deqk = npo.dequantize(s["kc"], s["ks"], fmt, sk2)
+    deqv = npo.dequantize(s["vc"], s["vs"], fmt, sv2)
+    if fmt == "fp8_e4m3":
+        assert np.array_equal(deqk, deqk.astype(np.float32), equal_nan=True)
+        q32 = npo.to_f64(q, "f16").astype(np.float32)
+        ref = npo.prefill(q32, deqk.astype(np.float32), deqv.astype(np.float32), "f32", cu,
+                          s["tables"], s["lens"], 0.3, s["hkv"])
+        np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    g = 8 // s["hkv"]
+    for b, (L, c) in enumerate(zip(lens, C)):
+        tb = s["tables"][b]
+        for i in range(c):
+            pos = L - c + i
+            for h in range(8):
+                K = np.stack([deqk[tb[t // s["bs"]], t % s["bs"], h // g] for t in range(pos + 1)])
+                V = np.stack([deqv[tb[t // s["bs"]], t % s["bs"], h // g] for t in range(pos + 1)])
+                sc = 0.3 * (K @ npo.to_f64(q[cu[b] + i, h], "f16"))
+                w = np.exp(sc - sc.max())
+                np.testing.assert_allclose(out[cu[b] + i, h], (w / w.sum()) @ V, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "int8"])
+def test_prefill_q8_one_query_per_request_is_decode_q8(c_oracle, fmt):
+    """C_b = 1 is a decode step: the query sits at the last position and sees
+    the whole context."""
+    s = _q8_setup(fmt, "bf16", 8, [9, 3, 16, 1])
+    c_oracle.append_q8(s["kc"], s["vc"], s["ks"], s["vs"], s["kx"], s["vx"], "bf16", s["slots"], fmt)
+    cu = np.arange(5, dtype=np.int32)
+    a = npo.prefill_q8(s["q"], "bf16", s["kc"], s["vc"], s["ks"], s["vs"], fmt, cu, s["tables"],
+                       s["lens"], 0.4, s["hkv"])
+    d = c_oracle.decode_q8(s["q"], "bf16", s["kc"], s["vc"], s["ks"], s["vs"], fmt, s["tables"],
+                           s["lens"], 0.4, s["hkv"])
+    np.testing.assert_allclose(a, d, rtol=0, atol=1e-12)
