@@ -54,10 +54,12 @@
 // 8-bit pools (FMT >= 0: FP8 E4M3 with one K and one V scale per pool, INT8
 // with a scale per token and head).  The producers land a tile's code rows
 // (128 bytes each) in a ring of their own and turn them into the query type
-// in the K / V ring (E4M3 and INT8 codes convert to f16 exactly, and f16
-// values of 8 significant bits to bf16 exactly), so the MMAs run as for
-// 16-bit pools.  FP8: the K scale multiplies the scores (with the softmax
-// scale), the V scale the output.  INT8: the producers also copy the tile's
+// in the K / V ring as f16 (E4M3 and INT8 codes convert to f16 exactly), and
+// the MMAs run on f16.  bf16 query tiles are turned into f16 in place, each
+// row times a power of two 2^e of its own (its largest |q| in [2^14, 2^15):
+// the conversion is exact), and the row's scores are multiplied by 2^-e.
+// FP8: the K scale multiplies the scores (with the softmax scale), the V
+// scale the output.  INT8: the producers also copy the tile's
 // token scales to a ring the softmax reads: K scales multiply the scores'
 // columns, V scales P's columns before the hi / lo split.
 #pragma once
@@ -105,7 +107,7 @@ constexpr int CST = 2;                            // code tiles per ring
 constexpr uint32_t CTILE = (uint32_t)BN * 128u;   // a tile's code rows: 64 x 128 B
 constexpr int SCS = 4;                            // INT8 scale ring depth
 constexpr int BAR_CK = NBARS, BAR_CV = BAR_CK + CST, BAR_SCF = BAR_CV + CST,
-              BAR_SCE = BAR_SCF + SCS, NBARS_Q8 = BAR_SCE + SCS;
+              BAR_SCE = BAR_SCF + SCS, BAR_QC = BAR_SCE + SCS, NBARS_Q8 = BAR_QC + 1;
 // launch order: the requests' costs (up to kMaxRanked of them) and the
 // request this CTA takes
 constexpr int kMaxRanked = 256;
@@ -123,7 +125,8 @@ struct Lay {
     static constexpr uint32_t cv = ck + (Q8 ? CST * CTILE : 0u);
     static constexpr uint32_t sc = cv + (Q8 ? CST * CTILE : 0u);       // [SCS][K, V][BN]
     static constexpr uint32_t csc = sc + (Q8 ? SCS * 2u * BN * 4u : 0u); // [K, V][CST][BN]
-    static constexpr uint32_t bar = csc + (Q8 ? 2u * CST * BN * 4u : 0u);
+    static constexpr uint32_t qinv = csc + (Q8 ? 2u * CST * BN * 4u : 0u); // [stream][BM] 2^-e
+    static constexpr uint32_t bar = qinv + (Q8 ? 2u * BM * 4u : 0u);
     static constexpr int nbars = Q8 ? NBARS_Q8 : NBARS;
     static constexpr uint32_t order = bar + 8u * nbars;
     static constexpr uint32_t tmem = order + 4u * (kMaxRanked + 4);
@@ -341,6 +344,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
     constexpr bool Q8 = FMT >= 0;
     constexpr bool SCALES = FMT == dec::kFmtInt8;
+    // 8-bit pools: the products run on f16 (bf16 queries are converted)
+    using MT = typename std::conditional<Q8, __half, T>::type;
+    constexpr bool QCONV = Q8 && !std::is_same<T, __half>::value;
     using LY = Lay<Q8>;
     constexpr int QT = BM / G;                    // queries per tile
     extern __shared__ unsigned char smem_raw[];
@@ -424,6 +430,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // INT8 scale ring: written by both producers, read by every softmax warp
             if (i >= BAR_SCF && i < BAR_SCF + SCS) count = 2;
             if (i >= BAR_SCE && i < BAR_SCE + SCS) count = (uint32_t)(NSOFT * nstreams);
+            if (i == BAR_QC) count = (uint32_t)nstreams;   // one producer per query tile
             dec::mbar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -497,6 +504,59 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     codes_issued = jj + 1;
                 };
                 for (int jj = 0; jj < min(CST, ntiles); ++jj) issue_codes(jj);
+                if constexpr (QCONV) {
+                    // query tile x (the K producer stream A's, the V producer
+                    // B's) into f16 in place: lane takes rows lane + 32 k
+                    const int x = is_k ? 0 : 1;
+                    if (x < nstreams) {
+                        bool ok = true;
+                        if (lane == 0) ok = wait_or_abort(bar(BAR_Q), 0, abort_flag, p.err, p.wait_ns);
+                        if (__shfl_sync(FULL, ok ? 1 : 0, 0)) {
+                            unsigned char* qt = smem + OFF_Q + (uint32_t)x * QTILE;
+                            float* qinv = reinterpret_cast<float*>(smem + LY::qinv) + x * BM;
+#pragma unroll 1
+                            for (int k = 0; k < BM / 32; ++k) {
+                                const int r = lane + 32 * k;
+                                // the row's 16-byte chunk c: 64-dim half c / 8, chunk c % 8
+                                auto chunk = [&](int c) {
+                                    return reinterpret_cast<uint4*>(qt + (c >> 3) * QHALF + r * 128 +
+                                                                    (((c & 7) ^ (r & 7)) << 4));
+                                };
+                                float amax = 0.f;
+#pragma unroll 4
+                                for (int c = 0; c < 16; ++c) {
+                                    const uint4 w = *chunk(c);
+                                    const uint32_t e4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        amax = fmaxf(amax, fmaxf(fabsf(H16<T>::low(e4[e])),
+                                                                 fabsf(H16<T>::high(e4[e]))));
+                                }
+                                // 2^e with amax * 2^e in [2^14, 2^15): the exponent field of amax
+                                int ex2 = 0;
+                                if (amax > 0.f && amax <= 3.0e38f) {
+                                    const int ex = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 126;
+                                    ex2 = min(max(15 - ex, -120), 120);
+                                }
+                                const float up = __uint_as_float((uint32_t)(ex2 + 127) << 23);
+                                qinv[r] = __uint_as_float((uint32_t)(127 - ex2) << 23);
+#pragma unroll 4
+                                for (int c = 0; c < 16; ++c) {
+                                    const uint4 w = *chunk(c);
+                                    uint32_t e4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        e4[e] = H16<__half>::pack(H16<T>::low(e4[e]) * up,
+                                                                  H16<T>::high(e4[e]) * up);
+                                    *chunk(c) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
+                                }
+                            }
+                            dec::fence_proxy_async();
+                            __syncwarp();
+                            if (lane == 0) dec::mbar_arrive(bar(BAR_QC));
+                        }
+                    }
+                }
                 for (int j = 0; j < ntiles; ++j) {
                     const int slot = j % nst, cs = j % CST;
                     bool ok = true;
@@ -520,7 +580,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         for (int c = 0; c < 8; ++c) {
                             const uint4 w = *reinterpret_cast<const uint4*>(crows + r * 128 + ((c ^ (r & 7)) << 4));
                             uint4 lo, hi;
-                            codes_to<T, FMT>(w, lo, hi);
+                            codes_to<MT, FMT>(w, lo, hi);
                             unsigned char* h = orows + (c >> 2) * KVHALF + r * 128;
                             const int c0 = 2 * (c & 3);
                             *reinterpret_cast<uint4*>(h + ((c0 ^ (r & 7)) << 4)) = lo;
@@ -595,7 +655,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // is warp-uniform; one elected lane issues each tcgen05 instruction.
         const int x = warp - WARP_MMA;
         if (ntiles > 0 && x < nstreams) {
-            constexpr uint32_t fmt = H16<T>::kFmt;
+            constexpr uint32_t fmt = H16<MT>::kFmt;
             constexpr uint32_t id_s = idesc_f16(fmt, 0, BM, BN);   // S = Q K^T
             constexpr uint32_t id_pv = idesc_f16(fmt, 1, BM, D);   // O += P V (V MN-major)
             const uint32_t tm = __shfl_sync(FULL, tmem, 0) + (uint32_t)x * COL_STREAM;
@@ -606,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             auto wait_all = [&](uint32_t bb, uint32_t parity) {
                 return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err, p.wait_ns));
             };
-            bool ok = wait_all(bar(BAR_Q), 0);
+            bool ok = wait_all(bar(QCONV ? BAR_QC : BAR_Q), 0);
             int done_pv = 0;                       // PV products issued
             auto pv = [&](int jj) -> bool {
                 const int s = jj % VST;
@@ -671,7 +731,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int lim = valid ? P0 + x * QT + qi : -1;   // last visible position
         const uint32_t trow = tmem + (uint32_t)x * COL_STREAM + ((uint32_t)(32 * qd) << 16);
         const int stid = tid - x * NSOFT * 32;     // thread index within the stream
-        const float qs = p.qscale;
+        float qs = p.qscale;
         float m = -CUDART_INF_F;
         float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // partial row sums
         bool ok = true;
@@ -681,6 +741,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto wait_warp = [&](uint32_t bb, uint32_t parity) {
             return __all_sync(FULL, wait_or_abort(bb, parity, abort_flag, p.err, p.wait_ns));
         };
+        if constexpr (QCONV) {
+            // the row's 2^-e, written with the converted query tile
+            if (ntiles > 0) {
+                ok = wait_warp(bar(BAR_QC), 0);
+                if (ok) qs *= reinterpret_cast<const float*>(smem + LY::qinv)[x * BM + r];
+            }
+        }
         for (int j = 0; ok && j < ntiles; ++j) {
             const int t0 = j * BN;
             uint32_t sv[2][32];
@@ -750,7 +817,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const float v0 = tsc[BN + 32 * c + e], v1 = tsc[BN + 32 * c + e + 1];
                         pv = make_float2(pp.x > 0.f ? pp.x * v0 : 0.f, pp.y > 0.f ? pp.y * v1 : 0.f);
                     }
-                    H16<T>::split(pv.x, pv.y, ph[16 * c + e / 2], pl[16 * c + e / 2]);
+                    H16<MT>::split(pv.x, pv.y, ph[16 * c + e / 2], pl[16 * c + e / 2]);
                 }
             if constexpr (SCALES) {
                 __syncwarp();                     // every lane has read the tile's scales
