@@ -73,7 +73,7 @@ cudaError_t launch_typed(const kv_pool& pool, const PrefillCall& c, cudaStream_t
     // one CTA per pair of query tiles
     cfg.gridDim = dim3((unsigned)((c.max_query_len + 2 * QT - 1) / (2 * QT)),
                        (unsigned)pool.num_kv_heads, (unsigned)c.batch);
-    cfg.blockDim = dim3(NTHREADS);
+    cfg.blockDim = dim3(FMT >= 0 ? NTHREADS_Q8 : NTHREADS);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -82,6 +82,12 @@ constexpr int KST = 4, VST = 3;   // K and V ring depths
 constexpr int NSOFT = 4;          // softmax warps per stream: one per TMEM lane quadrant
 constexpr int WARP_TMAK = 2 * NSOFT, WARP_TMAV = WARP_TMAK + 1, WARP_MMA = WARP_TMAK + 2;
 constexpr int NTHREADS = (2 * NSOFT + 4) * 32;
+// 8-bit pools: a second converter warp per side turns half of each tile's
+// code rows into 16-bit values beside the producer.  The helpers take warps
+// 10 and 11 (SM sub-partitions 2 and 3, the ones no producer issues from)
+// and the MMA warps move to 12 and 13.
+constexpr int WARP_CVK = WARP_TMAK + 2, WARP_CVV = WARP_CVK + 1, WARP_MMA_Q8 = WARP_TMAK + 4;
+constexpr int NTHREADS_Q8 = NTHREADS + 2 * 32;
 constexpr uint32_t TMEM_COLS = 512;
 // per stream X: base 256 X; S, then P hi, P lo, then O
 constexpr uint32_t COL_S = 0, COL_PH = 64, COL_PL = 96, COL_O = 128, COL_STREAM = 256;
@@ -101,13 +107,15 @@ constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = BAR_KF + KST, BAR_VF = BAR_KE + KS
               BAR_VE = BAR_VF + VST, BAR_STREAM = BAR_VE + VST;
 constexpr int SB_SF = 0, SB_SR = 1, SB_PF = 2, SB_OF = 3, SB_DR = 4, SB_N = 5;
 constexpr int NBARS = BAR_STREAM + 2 * SB_N;
-// 8-bit pools: then the K and V code rings' full barriers, and the INT8
-// scale ring's full / empty barriers
+// 8-bit pools: then the K and V code rings' full barriers, the INT8 scale
+// ring's full / empty barriers, the converted-query barrier and, per side and
+// code stage, the helper converter's done-reading barrier
 constexpr int CST = 2;                            // code tiles per ring
 constexpr uint32_t CTILE = (uint32_t)BN * 128u;   // a tile's code rows: 64 x 128 B
 constexpr int SCS = 4;                            // INT8 scale ring depth
 constexpr int BAR_CK = NBARS, BAR_CV = BAR_CK + CST, BAR_SCF = BAR_CV + CST,
-              BAR_SCE = BAR_SCF + SCS, BAR_QC = BAR_SCE + SCS, NBARS_Q8 = BAR_QC + 1;
+              BAR_SCE = BAR_SCF + SCS, BAR_QC = BAR_SCE + SCS, BAR_HK = BAR_QC + 1,
+              BAR_HV = BAR_HK + CST, NBARS_Q8 = BAR_HV + CST;
 // launch order: the requests' costs (up to kMaxRanked of them) and the
 // request this CTA takes
 constexpr int kMaxRanked = 256;
@@ -322,6 +330,24 @@ __device__ __forceinline__ void codes_to(uint4 c, uint4& lo, uint4& hi) {
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Code row r of a tile (a code stage: 64 rows x 128 B, 128-byte swizzled) ->
+// row r of a 16-bit ring slot (two 64-dim halves of 64 rows x 128 B, each
+// 128-byte swizzled): code chunk c (dims 16 c ..) becomes 16-byte chunks
+// 2 (c % 4) and 2 (c % 4) + 1 of half c / 4.
+template <typename MT, int FMT>
+__device__ __forceinline__ void convert_row(const unsigned char* crows, unsigned char* orows, int r) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(crows + r * 128 + ((c ^ (r & 7)) << 4));
+        uint4 lo, hi;
+        codes_to<MT, FMT>(w, lo, hi);
+        unsigned char* h = orows + (c >> 2) * KVHALF + r * 128;
+        const int c0 = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(h + ((c0 ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(h + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+    }
+}
+
 // Bounded wait (limit_ns); on expiry (or when another role already gave up)
 // raise the abort flag and return false.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -338,7 +364,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 // FMT: -1 for 16-bit pools (of type T), else the 8-bit pool's code format
 // (T is then the queries' type); the K / V maps address code rows.
 template <typename T, int G, int FMT = -1>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(FMT >= 0 ? NTHREADS_Q8 : NTHREADS, 1)
     paged_prefill(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
@@ -348,6 +374,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     using MT = typename std::conditional<Q8, __half, T>::type;
     constexpr bool QCONV = Q8 && !std::is_same<T, __half>::value;
     using LY = Lay<Q8>;
+    constexpr int WMMA = Q8 ? WARP_MMA_Q8 : WARP_MMA;   // the first MMA warp
     constexpr int QT = BM / G;                    // queries per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = dec::smem_align_1k(smem_raw);
@@ -377,13 +404,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int k = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
         const int per_req = (int)(gridDim.x * gridDim.y);
         const int rank = k / per_req, rem = k % per_req;
-        for (int i = tid; i < p.batch; i += NTHREADS) {
+        for (int i = tid; i < p.batch; i += (int)blockDim.x) {
             const int c0 = p.cu_seqlens[i], c1 = p.cu_seqlens[i + 1];
             const int Li = min(p.seq_lens[i], p.max_blocks * bs);
             cost[i] = (c1 > c0 && Li > 0) ? (Li + BN - 1) / BN : 0;
         }
         __syncthreads();
-        for (int i = tid; i < p.batch; i += NTHREADS) {
+        for (int i = tid; i < p.batch; i += (int)blockDim.x) {
             const int ci = cost[i];
             int above = 0;                         // requests ordered before i
             for (int o = 0; o < p.batch; ++o) above += cost[o] > ci || (cost[o] == ci && o < i);
@@ -424,6 +451,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t count = 1;
             if ((i >= BAR_KE && i < BAR_KE + KST) || (i >= BAR_VE && i < BAR_VE + VST))
                 count = (uint32_t)nstreams;
+            // 8-bit pools: a ring slot is full when both converters of its side
+            // have written their rows
+            if (Q8 && ((i >= BAR_KF && i < BAR_KF + KST) || (i >= BAR_VF && i < BAR_VF + VST)))
+                count = 2;
             if (i >= BAR_STREAM && i < NBARS &&
                 ((i - BAR_STREAM) % SB_N == SB_SR || (i - BAR_STREAM) % SB_N == SB_PF))
                 count = NSOFT;
@@ -436,7 +467,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == WARP_MMA) {
+    if (warp == WMMA) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          sbase + LY::tmem),
                      "r"(TMEM_COLS)
@@ -569,24 +600,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ok = wait_or_abort(bar(BAR_SCE + j % SCS), (j / SCS - 1) & 1, abort_flag, p.err,
                                            p.wait_ns);
                     if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
-                    // lane: token rows lane and lane + 32; code chunk c (dims 16 c ..)
-                    // -> 64-dim half c / 4, its 16-byte chunks 2 (c % 4) and + 1
-                    const unsigned char* crows = smem + (is_k ? LY::ck : LY::cv) + (uint32_t)cs * CTILE;
-                    unsigned char* orows = smem + (is_k ? OFF_K : OFF_V) + (uint32_t)slot * KVTILE;
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int r = lane + 32 * rr;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(crows + r * 128 + ((c ^ (r & 7)) << 4));
-                            uint4 lo, hi;
-                            codes_to<MT, FMT>(w, lo, hi);
-                            unsigned char* h = orows + (c >> 2) * KVHALF + r * 128;
-                            const int c0 = 2 * (c & 3);
-                            *reinterpret_cast<uint4*>(h + ((c0 ^ (r & 7)) << 4)) = lo;
-                            *reinterpret_cast<uint4*>(h + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
-                        }
-                    }
+                    // token rows 0..31 (the helper converter takes 32..63)
+                    convert_row<MT, FMT>(smem + (is_k ? LY::ck : LY::cv) + (uint32_t)cs * CTILE,
+                                         smem + (is_k ? OFF_K : OFF_V) + (uint32_t)slot * KVTILE, lane);
                     if constexpr (SCALES) {
                         float* ring = reinterpret_cast<float*>(smem + LY::sc) + (j % SCS) * 2 * BN +
                                       (is_k ? 0 : BN);
@@ -599,8 +615,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         dec::mbar_arrive(bar(full0 + slot));
                         if constexpr (SCALES) dec::mbar_arrive(bar(BAR_SCF + j % SCS));
                     }
-                    // the code stage is free: tile j + CST's codes into it
-                    if (j + CST < ntiles) issue_codes(j + CST);
+                    // the code stage is free once the helper has read its rows
+                    // too: tile j + CST's codes into it
+                    if (j + CST < ntiles) {
+                        bool hok = true;
+                        if (lane == 0)
+                            hok = wait_or_abort(bar((is_k ? BAR_HK : BAR_HV) + cs), (j / CST) & 1,
+                                                abort_flag, p.err, p.wait_ns);
+                        if (!__shfl_sync(FULL, hok ? 1 : 0, 0)) break;
+                        issue_codes(j + CST);
+                    }
                 }
                 // Drain: no copy may still be landing in shared memory at exit.
                 if (lane == 0) {
@@ -649,11 +673,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp >= WARP_MMA) {
+    } else if (Q8 && (warp == WARP_CVK || warp == WARP_CVV)) {
+      if constexpr (Q8) {
+        // ------------------------------------- helper converters (8-bit) ----
+        // Token rows 32..63 of every tile of its side, from the code stage the
+        // producer loaded into the ring slot the producer fills too; the slot
+        // counts as full after both have arrived, and the code stage is
+        // refilled only after this warp has said it is done reading.
+        const bool is_k = warp == WARP_CVK;
+        const int nst = is_k ? KST : VST;
+        const int full0 = is_k ? BAR_KF : BAR_VF, empty0 = is_k ? BAR_KE : BAR_VE;
+        const int cfull0 = is_k ? BAR_CK : BAR_CV, hdone0 = is_k ? BAR_HK : BAR_HV;
+        for (int j = 0; j < ntiles; ++j) {
+            const int slot = j % nst, cs = j % CST;
+            bool ok = true;
+            if (lane == 0 && j >= nst)
+                ok = wait_or_abort(bar(empty0 + slot), (j / nst - 1) & 1, abort_flag, p.err,
+                                   p.wait_ns);
+            if (lane == 0 && ok)
+                ok = wait_or_abort(bar(cfull0 + cs), (j / CST) & 1, abort_flag, p.err, p.wait_ns);
+            if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) break;
+            convert_row<MT, FMT>(smem + (is_k ? LY::ck : LY::cv) + (uint32_t)cs * CTILE,
+                                 smem + (is_k ? OFF_K : OFF_V) + (uint32_t)slot * KVTILE, lane + 32);
+            dec::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                dec::mbar_arrive(bar(full0 + slot));
+                dec::mbar_arrive(bar(hdone0 + cs));
+            }
+        }
+      }
+    } else if (warp >= WMMA) {
         // ----------------------------------------------------------- MMA ----
         // One warp per stream runs the loop (waits included) so every operand
         // is warp-uniform; one elected lane issues each tcgen05 instruction.
-        const int x = warp - WARP_MMA;
+        const int x = warp - WMMA;
         if (ntiles > 0 && x < nstreams) {
             constexpr uint32_t fmt = H16<MT>::kFmt;
             constexpr uint32_t id_s = idesc_f16(fmt, 0, BM, BN);   // S = Q K^T
@@ -898,7 +952,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // -- teardown: free TMEM once every role is done with it ------------------
     tc_fence_before();
     __syncthreads();
-    if (warp == WARP_MMA) {
+    if (warp == WMMA) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(TMEM_COLS)
