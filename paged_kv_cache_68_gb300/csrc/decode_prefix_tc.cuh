@@ -344,31 +344,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_prefix_tc(
                 ids_nxt = fetch(u + UPB);
             }
             const int id = __shfl_sync(FULL, ids_cur, ((i % UPB) * TB + lane) & 31);
-            if (is_k && first_of(u, x)) {
-                // the piece's 16 query rows into Q buffer pi % 2: lane = (row c, 64-dim half h)
+            // A piece's first unit (K side): its 16 query rows are loaded into
+            // registers first, the tile's copies issued, and only then does the
+            // warp wait for Q buffer pi % 2 and store the rows, so the query
+            // loads and the tile's copies are in flight together.
+            const bool qpiece = is_k && first_of(u, x);
+            const int c = lane >> 1, h = lane & 1, m = c / G, hh = c % G;   // (row c, 64-dim half h)
+            uint4 raw[8];
+            int qb = 0;
+            if (qpiece) {
                 ++pi;
+                qb = pi & 1;
                 const int m0 = gfirst[x.k] + x.sub * MS;
                 const int msz = min(MS, gsize[x.k] - x.sub * MS);
-                const int qb = pi & 1;
-                if (pi >= 2)
-                    ok = warp_wait(sbase + lay.bar(B_QEMPTY + qb), ((pi >> 1) - 1) & 1, abort_flag,
-                                   p.err, p.wait_ns, lane);
-                if (!ok) break;
-                const int c = lane >> 1, h = lane & 1, m = c / G, hh = c % G;
-                uint4 raw[8];
                 const T* src = static_cast<const T*>(p.q) +
                                ((size_t)(m0 + m) * p.num_q_heads + x.g * G + hh) * D + h * 64;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
                     raw[ch] = m < msz ? __ldg(reinterpret_cast<const uint4*>(src) + ch)
                                       : make_uint4(0u, 0u, 0u, 0u);
-                unsigned char* qdst = smem + lay.q + (uint32_t)qb * QBUF + (uint32_t)h * QHALF + c * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4*>(qdst + ((ch ^ (c & 7)) << 4)) = raw[ch];
-                dec::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) dec::mbar_arrive(sbase + lay.bar(B_QFULL + qb));
             }
             // the tile's blocks: lane 2 b + c makes copy c of block b
             const int s = i % nst;
@@ -386,15 +380,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_prefix_tc(
             constexpr uint32_t per_block = 2u * BS * 128u;   // both 64-dim halves
             if (lane == 0) dec::mbar_arrive_tx(fb, (uint32_t)__popc(mask) * per_block);
             __syncwarp();
-            const int b = lane >> 1, c = lane & 1;
-            const int bid = __shfl_sync(FULL, id, b);
-            if (b < TB && ((mask >> b) & 1u)) {
-                // c = the 64-dim half
+            const int bb = lane >> 1, cc = lane & 1;
+            const int bid = __shfl_sync(FULL, id, bb);
+            if (bb < TB && ((mask >> bb) & 1u)) {
+                // cc = the 64-dim half
                 const uint32_t d = sbase + (is_k ? lay.kring : lay.vring) + (uint32_t)s * KVTILE +
-                                   (uint32_t)c * KVHALF + (uint32_t)b * BS * 128u;
-                dec::tma_load_3d(d, map, c * 64, x.g, bid * BS, fb);
+                                   (uint32_t)cc * KVHALF + (uint32_t)bb * BS * 128u;
+                dec::tma_load_3d(d, map, cc * 64, x.g, bid * BS, fb);
             }
             issued = i + 1;
+            if (qpiece) {
+                if (pi >= 2)
+                    ok = warp_wait(sbase + lay.bar(B_QEMPTY + qb), ((pi >> 1) - 1) & 1, abort_flag,
+                                   p.err, p.wait_ns, lane);
+                if (!ok) break;
+                unsigned char* qdst = smem + lay.q + (uint32_t)qb * QBUF + (uint32_t)h * QHALF + c * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(qdst + ((ch ^ (c & 7)) << 4)) = raw[ch];
+                dec::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) dec::mbar_arrive(sbase + lay.bar(B_QFULL + qb));
+            }
         }
         // Drain (full limit): no copy may still be landing at exit.
         if (lane == 0) {
