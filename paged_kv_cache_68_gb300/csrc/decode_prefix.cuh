@@ -473,20 +473,24 @@ struct Tc8Rows : TcRows<T, 128, G, 32, true> {
     }
 };
 
-// One warp: merge the partials of a cut segment into the prefix states.
-template <int D, int G>
+// Merge the partials of a cut segment into the prefix states (pass0, pstep:
+// the element passes this warp takes when several warps share the merge;
+// BATCH: slots whose loads are in flight together).
+template <int D, int G, int BATCH = kMergeBatch>
 __device__ __forceinline__ void merge_prefix_partials(const PParams& p, int seg_start, int chunk,
                                                       int c0, int c1, int rows, int m0, int g,
-                                                      int lane) {
-    merge_cut<kRows, D>(p.part_o, p.part_lse, c0, c1, seg_start == c0 * chunk ? 0 : 1, nullptr,
-                        nullptr, lane, [&](int r, int d0, const float* v, float lse) {
-                            if (r >= rows) return;
-                            const size_t prow = (size_t)(m0 + r / G) * p.num_q_heads + g * G + r % G;
+                                                      int lane, int pass0 = 0, int pstep = 1) {
+    merge_slots<kRows, D, BATCH>(p.part_o, p.part_lse, c0, c1, seg_start == c0 * chunk ? 0 : 1,
+                                 nullptr, nullptr, lane, pass0, pstep,
+                                 [&](int r, int d0, const float* v, float lse) {
+                                     if (r >= rows) return;
+                                     const size_t prow =
+                                         (size_t)(m0 + r / G) * p.num_q_heads + g * G + r % G;
 #pragma unroll
-                            for (int k = 0; k < merge_epl<kRows, D>(); ++k)
-                                p.pst_o[prow * D + d0 + k] = v[k];
-                            if (d0 == 0) p.pst_lse[prow] = lse;
-                        });
+                                     for (int k = 0; k < merge_epl<kRows, D>(); ++k)
+                                         p.pst_o[prow * D + d0 + k] = v[k];
+                                     if (d0 == 0) p.pst_lse[prow] = lse;
+                                 });
 }
 
 // Pol: Tc8Rows (3-D swizzled maps of 128-byte code rows, UB blocks of BS

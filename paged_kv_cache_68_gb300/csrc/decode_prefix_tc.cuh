@@ -641,19 +641,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_prefix_tc(
                 }
             }
             if (!complete) {
-                // the CTA whose piece completes the segment's count merges
+                // the CTA whose piece completes the segment's count merges; all
+                // softmax warps take a share of the element passes
                 __threadfence();
                 dec::named_sync(2);
-                if (warp == 0) {
-                    const int c0 = x.seg / chunk, c1 = (x.seg + x.tiles - 1) / chunk;
-                    int lastp = 0;
-                    if (lane == 0)
-                        lastp = dec::count_piece(p.counters + 2 * ((size_t)m0 * H + x.g), p.tag,
-                                                 c1 - c0 + 1);
-                    if (__shfl_sync(FULL, lastp, 0)) {
-                        __threadfence();
-                        dec::merge_prefix_partials<D, G>(p, x.seg, chunk, c0, c1, rows, m0, x.g, lane);
-                    }
+                const int c0 = x.seg / chunk, c1 = (x.seg + x.tiles - 1) / chunk;
+                int lastp = 0;
+                if (warp == 0 && lane == 0)
+                    lastp = dec::count_piece(p.counters + 2 * ((size_t)m0 * H + x.g), p.tag,
+                                             c1 - c0 + 1);
+                if (soft_sync_any(lastp != 0)) {
+                    __threadfence();
+                    dec::merge_prefix_partials<D, G, 4>(p, x.seg, chunk, c0, c1, rows, m0, x.g, lane,
+                                                        warp, NSOFT);
                 }
             }
         }
