@@ -514,6 +514,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
     volatile int* valid = reinterpret_cast<volatile int*>(smem + lay.valid);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc);
     int* warp_tot = reinterpret_cast<int*>(smem + lay.misc) + 8;
+    // the CTA's last piece, when it completes a cut segment's count: {merge,
+    // seg_start, c0, c1, rows, m0, g}, posted by warp 0 for every attending warp
+    volatile int* fm = reinterpret_cast<volatile int*>(smem + lay.misc) + 1;
     int* gcum = reinterpret_cast<int*>(smem + lay.gcum);
     int* vg = reinterpret_cast<int*>(smem + lay.vg);
     const int* gfirst = vg;
@@ -695,6 +698,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
             const size_t ps = (size_t)blockIdx.x * 2 + ((u == start) ? 0 : 1);
             pol.merge_store(mo, mm, rows, complete, p.pst_o, p.pst_lse, m0, g, p.num_q_heads,
                             p.part_o + ps * kRows * D, p.part_lse + ps * kRows, lane);
+            const bool final_piece = piece_end == end;
+            int merge = 0;
             if (!complete) {
                 __threadfence();
                 __syncwarp();
@@ -702,17 +707,31 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
                 int last = 0;
                 if (lane == 0)
                     last = count_piece(p.counters + 2 * ((size_t)m0 * H + g), p.tag, c1 - c0 + 1);
-                if (__shfl_sync(FULL, last, 0)) {
-                    __threadfence();
+                merge = __shfl_sync(FULL, last, 0);
+                if (merge) __threadfence();
+                if (final_piece) {
+                    // the other warps are done: they share this merge below
+                    if (lane == 0) {
+                        fm[1] = seg_start; fm[2] = c0; fm[3] = c1; fm[4] = rows; fm[5] = m0;
+                        fm[6] = g;
+                    }
+                } else if (merge) {
                     merge_prefix_partials<D, G>(p, seg_start, chunk, c0, c1, rows, m0, g, lane);
                 }
             }
+            if (final_piece && lane == 0) fm[0] = merge;
+            __syncwarp();
             named_arrive(2);
         }
         first_piece = false;
         u = piece_end;
     }
-    if (w != 0 && !first_piece) named_sync(2);
+    if (first_piece) return;
+    if (w != 0) named_sync(2);
+    if (fm[0]) {                                   // every warp: a share of the last piece's merge
+        __threadfence();
+        merge_prefix_partials<D, G>(p, fm[1], chunk, fm[2], fm[3], fm[4], fm[5], fm[6], lane, w, NCW);
+    }
 }
 
 // -- host side: occupancy and launch of one instance ------------------------
