@@ -1592,7 +1592,13 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     pdl_launch_dependents();
-    pdl_wait();                                    // inputs of earlier kernels are visible
+    // A plain decode waits here for the kernels before it (the append writes
+    // K/V rows).  A cascade decode's prefix pass lets this kernel in only
+    // after its own wait, so the pool is complete: this kernel streams its
+    // blocks at once and waits for the prefix pass just before it first
+    // reads the prefix states (and, at the latest, before each warp exits,
+    // so that this grid never ends before the prefix pass).
+    if (!cascade) pdl_wait();
     unit_prefix(p, smem, lay, bsu, cascade, blockIdx.x == 0);
     __syncthreads();
     // sequences no unit covers: zeros, or (cascade) the prefix state alone
@@ -1600,6 +1606,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         if (prefix[b + 1] == prefix[b]) {
             T* ob = static_cast<T*>(p.out) + (size_t)b * p.num_q_heads * D;
             const bool has = cascade && skip_s[b] > 0;
+            if (has) pdl_wait();                   // b's prefix state is written
             for (int i = tid; i < p.num_q_heads * D; i += SPLIT_THREADS) {
                 const size_t row = (size_t)b * p.num_q_heads + i / D;
                 ob[i] = Elt<T>::store(has ? p.pst_o[row * D + i % D] : 0.f);
@@ -1615,7 +1622,10 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
     const WorkCut cut(prefix, B, H, p.num_ctas * NCW);
     const int start = cut.start_unit(worker);
     const int end = cut.start_unit(worker + 1);
-    if (start >= end) return;
+    if (start >= end) {
+        if (cascade) pdl_wait();
+        return;
+    }
 
     // ------------------------------------------------------ the warp's work --
     const int w = warp;
@@ -1758,6 +1768,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         // cascade: stage this (b, g)'s prefix state in shared memory while
         // the piece's blocks are attended
         if (skip > 0) {
+            pdl_wait();                            // the prefix pass's states are written
             __syncwarp();                          // the last piece's reads are done
             for (int i = lane; i < G * D / 4; i += 32)
                 cp_async16(pst_s + 4 * i, p.pst_o + head0 * D + 4 * i);
@@ -1835,6 +1846,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, Pol::kMinBlocks) paged_decode_s
         }
         u = piece_end;
     }
+    if (cascade) pdl_wait();
     // Drain: no copy may still be landing in shared memory at exit (after a
     // timeout the waits above were skipped).  The issues that reached a
     // barrier are the first na; their last per_warp hold distinct stages,

@@ -535,8 +535,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) paged_decode_prefix(
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    pdl_launch_dependents();
+    // The second pass is let in only after this wait: the pool is then
+    // complete, so that pass may stream its blocks before this one ends.
     pdl_wait();
+    pdl_launch_dependents();
 
     // -- used groups, their units (sub-groups x KV heads x shared units) -------
     const int NG = load_groups(p.g_first, p.g_size, p.g_blocks, K, p.seq_lens, B, BS, cap, UB, vg,

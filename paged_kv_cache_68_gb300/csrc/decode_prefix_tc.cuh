@@ -231,8 +231,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_prefix_tc(
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    dec::pdl_launch_dependents();
+    // The second pass is let in only after this wait: the pool is then
+    // complete, so that pass may stream its blocks before this one ends.
     dec::pdl_wait();
+    dec::pdl_launch_dependents();
 
     // -- used groups and their units (sub-groups x KV heads x tiles) ----------
     const int NG = dec::load_groups(p.g_first, p.g_size, p.g_blocks, K, p.seq_lens, B, BS, cap, ub,
