@@ -164,8 +164,10 @@ def _decode_args(w):
 @pytest.mark.parametrize("cache", ["fp8_e4m3", "int8"])
 def test_q8_decode_wait_gives_up(cache):
     """The 8-bit split kernel: code tiles by TMA, INT8 scales by bulk copy, all
-    counted on the stages' barriers and drained after the give-up."""
-    w = wl.llama3_8b_gqa(45, batch=64, median=700, hi=3000)
+    counted on the stages' barriers and drained after the give-up.  The full
+    Llama-3-8B-shaped step: with INT8's three stages per warp a smaller step
+    can find every tile landed by the time it is waited for."""
+    w = wl.llama3_8b_gqa(45)
     q, tables, lens = _decode_args(w)
     _q8_expire_then_recover(w, cache, lambda pool: pool.decode(q, tables, lens, w.scale),
                             lambda p: oracle_step_q8(w, p)[4])
